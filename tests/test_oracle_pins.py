@@ -1,0 +1,113 @@
+"""The fp64 oracle against facts that do not come from it (CPU only).
+
+Also plants plausible mistakes in the oracle (on the CPU, via monkeypatch)
+and checks that at least one pin catches each of them.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.numerics as onum
+import oracle.swiglu as osw
+import oracle.swish as osh
+
+from . import _pins
+
+
+@pytest.mark.parametrize("pin", _pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def _sig_wrong_sign(z):
+    z = np.asarray(z, np.float64)
+    return 1.0 / (1.0 + np.exp(np.clip(z, -700, 700)))
+
+
+def _silu_grad_drop_term(z):
+    s = osw.sigmoid(z)
+    return s * (1.0 + z)
+
+
+def _b_drop_fc(dy, g, fc):
+    dy, g, fc = (np.asarray(a, np.float64) for a in (dy, g, fc))
+    s = osw.sigmoid(g)
+    dg = dy * (s * (1.0 + g * (1.0 - s)))
+    dfc = dy * g * s
+    return dg, dfc, dg.sum(0, keepdims=True), dfc.sum(0, keepdims=True)
+
+
+def _b_dfc_sigma_only(dy, g, fc):
+    dy, g, fc = (np.asarray(a, np.float64) for a in (dy, g, fc))
+    s = osw.sigmoid(g)
+    dg = dy * fc * (s * (1.0 + g * (1.0 - s)))
+    dfc = dy * s
+    return dg, dfc, dg.sum(0, keepdims=True), dfc.sum(0, keepdims=True)
+
+
+def _b_db_mean(dy, g, fc):
+    dg, dfc, _, _ = osw.__dict__["_orig_b"](dy, g, fc)
+    return dg, dfc, dg.mean(0, keepdims=True), dfc.mean(0, keepdims=True)
+
+
+def _w_swapped(x, dg, dfc):
+    xt = np.asarray(x, np.float64).T
+    return xt @ np.asarray(dfc, np.float64), xt @ np.asarray(dg, np.float64)
+
+
+def _x_drop_fc_term(dg, dfc, w_g, w_fc):
+    return np.asarray(dg, np.float64) @ np.asarray(w_g, np.float64).T
+
+
+def _x_wrong_sign(dg, dfc, w_g, w_fc):
+    return (np.asarray(dg, np.float64) @ np.asarray(w_g, np.float64).T
+            - np.asarray(dfc, np.float64) @ np.asarray(w_fc, np.float64).T)
+
+
+def _swish_no_beta_inside(grad, x, scale=1.0):
+    x = np.asarray(x, np.float64)
+    t = x
+    s = osw.sigmoid(float(np.float32(scale)) * x)
+    return np.asarray(grad, np.float64) * (s * (1.0 + t * (1.0 - s)))
+
+
+def _swish_beta_not_f32(grad, x, scale=1.0):
+    x = np.asarray(x, np.float64)
+    b = 1.0 if scale is None else float(scale)
+    t = b * x
+    s = osw.sigmoid(t)
+    return np.asarray(grad, np.float64) * (s * (1.0 + t * (1.0 - s)))
+
+
+def _bf16_truncate(x):
+    v = np.asarray(x, np.float64).astype(np.float32)
+    return ((v.view(np.uint32) >> 16) << 16).view(np.float32).astype(np.float64)
+
+
+MUTANTS = {
+    "sigmoid_sign": [(osw, "sigmoid", _sig_wrong_sign), (osh, "sigmoid", _sig_wrong_sign)],
+    "silu_grad_drops_1_minus_s": [(osw, "silu_grad", _silu_grad_drop_term)],
+    "dg_drops_fc": [(osw, "swiglu_bwd_b", _b_drop_fc)],
+    "dfc_sigma_only": [(osw, "swiglu_bwd_b", _b_dfc_sigma_only)],
+    "db_mean_not_sum": [(osw, "swiglu_bwd_b", _b_db_mean)],
+    "dw_outputs_swapped": [(osw, "swiglu_bwd_w", _w_swapped)],
+    "dx_drops_fc_term": [(osw, "swiglu_bwd_x", _x_drop_fc_term)],
+    "dx_wrong_sign": [(osw, "swiglu_bwd_x", _x_wrong_sign)],
+    "swish_beta_missing_in_bracket": [(osh, "swish_grad", _swish_no_beta_inside)],
+    "swish_beta_not_rounded_to_f32": [(osh, "swish_grad", _swish_beta_not_f32)],
+    "bf16_truncates": [(onum, "f64_to_bf16_value", _bf16_truncate)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    monkeypatch.setitem(osw.__dict__, "_orig_b", osw.swiglu_bwd_b)
+    for mod, attr, fn in MUTANTS[name]:
+        monkeypatch.setattr(mod, attr, fn)
+    caught = []
+    for pin in _pins.ALL_PINS:
+        try:
+            pin()
+        except Exception as e:  # AssertionError, or a shape error from a bad transpose
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"no pin caught the planted mistake {name}"
