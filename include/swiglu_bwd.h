@@ -1,0 +1,151 @@
+/*
+ * swiglu_bwd.h -- C ABI of the GB300 (sm_103a) SwiGLU-FFN backward and SwishGrad.
+ *
+ * Operations (sources are web pages; each function cites the section it follows):
+ *   [P1] "PyPTO-Gym in practice: the fused SwiGLU backward operator"
+ *        (hnwysp.cn/news/34787)
+ *   [P2] "SwishGrad in CANN ops-nn: principle, implementation and the
+ *        aclnnSwishBackward guide" (bhfrc.com/news/37500)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, row-major, contiguous, on the current CUDA device.
+ *   SwiGLU tensors are bf16 (2 bytes, stored as uint16 bit patterns).
+ *   Shapes follow [P1] "Kernel signatures": x [M,K]; w_g, w_fc [K,N];
+ *   dy, g, fc, dg, dfc [M,N]; db_g, db_fc [1,N]; dw_g, dw_fc [K,N]; dx [M,K].
+ * - Ownership: the caller owns every buffer, including the workspace, whose
+ *   size comes from the matching *_workspace_size query (the two-phase model of
+ *   [P2] section 3.2). The library keeps no per-call state and allocates no
+ *   device memory; a 4-byte device status word (see swg_check) is its only
+ *   module-level device state.
+ * - Streams: every call is asynchronous on `stream` (NULL = legacy default
+ *   stream), like aclnnSwishBackward ([P2] section 3.4). Argument errors are
+ *   returned synchronously with nothing launched. A failed launch returns
+ *   SWG_ERR_CUDA.
+ * - Dynamic M ([P1] "Dynamic axis M"): any M >= 0 without recompilation; a
+ *   tail of M that does not fill a tile is handled inside the kernels.
+ *   K and N must be positive multiples of 8 (16-byte rows for TMA); other
+ *   values return SWG_ERR_UNSUPPORTED. Base pointers of SwiGLU tensors and of
+ *   the workspace must be 16-byte aligned (SWG_ERR_UNSUPPORTED otherwise).
+ * - Empty calls: M == 0 (or n == 0) launches no element-wise work ([P2]
+ *   section 3.5, empty-tensor short circuit); outputs that are sums over the
+ *   M rows (db_*, dw_*) are still written, as zeros.
+ * - Outputs are OVERWRITTEN. [P1] asks callers to zero db/dw and accumulates
+ *   into them; overwriting gives the same values without the zeroing.
+ * - Outputs must not overlap inputs or each other (SWG_ERR_PARAM_INVALID when
+ *   an overlap is detected from the pointer ranges). Exception: swish_grad's
+ *   grad_x may alias grad or x exactly.
+ * - Arithmetic: bf16 inputs are widened to fp32; element-wise math, sums and
+ *   tensor-core accumulation are fp32; each output is rounded once to bf16,
+ *   round-to-nearest-even ([P1] "Dtype conversion flow": bf16 storage, fp32
+ *   compute; [P2] section 2.4, CAST_RINT).
+ */
+#ifndef SWIGLU_BWD_H
+#define SWIGLU_BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* swg_stream_t;
+
+typedef enum {
+  SWG_OK = 0,
+  SWG_ERR_NULLPTR = 1,       /* a required pointer is NULL ([P2] 3.3: ACLNN_ERR_PARAM_NULLPTR) */
+  SWG_ERR_PARAM_INVALID = 2, /* bad dtype / negative size / overlapping buffers
+                                ([P2] 3.3: ACLNN_ERR_PARAM_INVALID) */
+  SWG_ERR_UNSUPPORTED = 3,   /* K or N not a positive multiple of 8, misaligned
+                                pointer, or the current device is not sm_103 */
+  SWG_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than the size query */
+  SWG_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  SWG_ERR_TIMEOUT = 6        /* a kernel gave up waiting on one of its pipeline barriers */
+} swg_status;
+
+typedef enum { SWG_F32 = 0, SWG_F16 = 1, SWG_BF16 = 2 } swg_dtype;
+
+/* flags for swiglu_bwd */
+#define SWG_UNFUSED 0u /* b stage, then the w and x GEMMs on the stored dg, dfc */
+#define SWG_FUSED 1u   /* the GEMMs recompute dg, dfc from dy, g, fc in their
+                          operand producer; dg, dfc never round-trip HBM */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* swg_status_string(swg_status s);
+
+/* Synchronises `stream`, then reports and clears the device status word that
+ * kernels set when a bounded pipeline wait runs out (SWG_ERR_TIMEOUT), or
+ * returns SWG_ERR_CUDA if the stream reports an error. SWG_OK otherwise. */
+swg_status swg_check(swg_stream_t stream);
+
+/* ---- b stage -----------------------------------------------------------------
+ * [P1] "Algorithm overview and formulas" items 1-2; "Kernel signatures",
+ * fused_swiglu_bwd_b_kernel(dy, g, fc, dg, dfc, db_g, db_fc):
+ *   s = sigma(g);  dg = dy * fc * s * (1 + g * (1 - s));  dfc = dy * g * s;
+ *   db_g[n] = sum_m dg[m,n];  db_fc[n] = sum_m dfc[m,n].
+ * The column sums are taken over the fp32 dg, dfc (before bf16 rounding), as
+ * fp32 per-block partials reduced in a fixed order (deterministic).
+ * Inputs: dy, g, fc [M,N]. Outputs: dg, dfc [M,N]; db_g, db_fc [1,N].
+ * Workspace: swiglu_bwd_b_workspace_size(M, N) bytes, 16-byte aligned. */
+size_t swiglu_bwd_b_workspace_size(int64_t M, int64_t N);
+swg_status swiglu_bwd_b(const void* dy, const void* g, const void* fc,
+                        void* dg, void* dfc, void* db_g, void* db_fc,
+                        int64_t M, int64_t N, void* workspace, size_t workspace_bytes,
+                        swg_stream_t stream);
+
+/* ---- w stage -----------------------------------------------------------------
+ * [P1] item 3; fused_swiglu_bwd_w_kernel(x, dg, dfc, dw_g, dw_fc):
+ *   dw_g = x^T dg;  dw_fc = x^T dfc      (x [M,K]; dg, dfc [M,N]; dw_* [K,N])
+ * One tcgen05 GEMM launch covers both outputs; the reduction runs over M and
+ * may be split over M into fp32 partials (workspace) that a second kernel sums
+ * in a fixed order before the single bf16 rounding.
+ * Workspace: swiglu_bwd_w_workspace_size(M, K, N) bytes (may be 0). */
+size_t swiglu_bwd_w_workspace_size(int64_t M, int64_t K, int64_t N);
+swg_status swiglu_bwd_w(const void* x, const void* dg, const void* dfc,
+                        void* dw_g, void* dw_fc, int64_t M, int64_t K, int64_t N,
+                        void* workspace, size_t workspace_bytes, swg_stream_t stream);
+
+/* ---- x stage -----------------------------------------------------------------
+ * [P1] item 4; fused_swiglu_bwd_x_kernel(dg, dfc, w_g, w_fc, dx):
+ *   dx = dg W_g^T + dfc W_fc^T           (dx [M,K])
+ * computed as one GEMM [dg | dfc] [W_g | W_fc]^T with reduction length 2N;
+ * no workspace. */
+swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const void* w_fc,
+                        void* dx, int64_t M, int64_t K, int64_t N, swg_stream_t stream);
+
+/* ---- whole backward ----------------------------------------------------------
+ * [P1] "Kernel overview and call chain": b, then w and x on b's dg, dfc.
+ * dg, dfc are optional outputs: pass NULL to skip them. With SWG_UNFUSED and
+ * NULL dg/dfc, the workspace holds them (4*M*N bytes more). With SWG_FUSED the
+ * w and x GEMMs compute dg, dfc tile by tile in shared memory from dy, g, fc
+ * (the recompute-instead-of-store principle); their operands are the bf16
+ * roundings of the fp32 dg, dfc, exactly as in the unfused chain.
+ * Workspace: swiglu_bwd_workspace_size(M, K, N, flags) bytes; with non-NULL
+ * dg/dfc the smaller figure swiglu_bwd_workspace_size(M, K, N, flags |
+ * SWG_WS_DG_GIVEN) suffices. */
+#define SWG_WS_DG_GIVEN 0x100u
+size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags);
+swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc,
+                      const void* dy, const void* g, const void* fc,
+                      void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc,
+                      void* db_g, void* db_fc, int64_t M, int64_t K, int64_t N,
+                      unsigned flags, void* workspace, size_t workspace_bytes,
+                      swg_stream_t stream);
+
+/* ---- SwishGrad ---------------------------------------------------------------
+ * [P2] section 1.2: grad_x = grad * sigma(beta x) * (1 + beta x (1 - sigma(beta x))),
+ * beta = *scale, or 1.0 when scale is NULL ([P2] 3.5). grad, x, grad_x hold n
+ * elements of `dtype` (fp32 / fp16 / bf16; any shape, treated as 1-D; any
+ * alignment; any n >= 0). Math is fp32; fp16/bf16 results are rounded to
+ * nearest even ([P2] 2.4, CAST_RINT). grad_x may alias grad or x exactly.
+ * No workspace ([P2]'s workspace query returns 0 for this op as well). */
+swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x,
+                      int64_t n, swg_dtype dtype, swg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_BWD_H */

@@ -1,0 +1,23 @@
+"""GB300 (sm_103a) SwiGLU-FFN backward and SwishGrad.
+
+The compute runs in hand-written CUDA kernels behind the C ABI of
+include/swiglu_bwd.h; this package is the thin Python binding over it.
+"""
+
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    SWG_FUSED,
+    SWG_UNFUSED,
+    SwgError,
+    status_string,
+    swg_check,
+    swiglu_bwd,
+    swiglu_bwd_b,
+    swiglu_bwd_b_workspace_size,
+    swiglu_bwd_w,
+    swiglu_bwd_w_workspace_size,
+    swiglu_bwd_workspace_size,
+    swiglu_bwd_x,
+    swish_grad,
+)

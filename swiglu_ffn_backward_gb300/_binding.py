@@ -1,0 +1,235 @@
+"""ctypes binding of include/swiglu_bwd.h: argument marshalling only.
+
+Every step of the backward runs in the library's sm_103a kernels. torch is
+used for device memory (outputs and workspace are allocated with torch.empty
+when the caller passes none) and for the current CUDA stream. If the shared
+library is missing the import of this module raises: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libswiglu_bwd.so")
+
+# status codes (swg_status)
+SWG_OK = 0
+SWG_ERR_NULLPTR = 1
+SWG_ERR_PARAM_INVALID = 2
+SWG_ERR_UNSUPPORTED = 3
+SWG_ERR_WORKSPACE = 4
+SWG_ERR_CUDA = 5
+SWG_ERR_TIMEOUT = 6
+
+# dtypes (swg_dtype)
+SWG_F32, SWG_F16, SWG_BF16 = 0, 1, 2
+_DTYPE = {torch.float32: SWG_F32, torch.float16: SWG_F16, torch.bfloat16: SWG_BF16}
+
+# flags
+SWG_UNFUSED = 0
+SWG_FUSED = 1
+SWG_WS_DG_GIVEN = 0x100
+
+EXPORTS = (
+    "swg_status_string", "swg_check",
+    "swiglu_bwd_b_workspace_size", "swiglu_bwd_b",
+    "swiglu_bwd_w_workspace_size", "swiglu_bwd_w",
+    "swiglu_bwd_x",
+    "swiglu_bwd_workspace_size", "swiglu_bwd",
+    "swish_grad",
+)
+
+
+class SwgError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -m swiglu_ffn_backward_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, SZ, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint
+    st = ctypes.c_int
+    lib.swg_status_string.argtypes = [st]
+    lib.swg_status_string.restype = ctypes.c_char_p
+    lib.swg_check.argtypes = [P]
+    lib.swg_check.restype = st
+    lib.swiglu_bwd_b_workspace_size.argtypes = [I64, I64]
+    lib.swiglu_bwd_b_workspace_size.restype = SZ
+    lib.swiglu_bwd_b.argtypes = [P, P, P, P, P, P, P, I64, I64, P, SZ, P]
+    lib.swiglu_bwd_b.restype = st
+    lib.swiglu_bwd_w_workspace_size.argtypes = [I64, I64, I64]
+    lib.swiglu_bwd_w_workspace_size.restype = SZ
+    lib.swiglu_bwd_w.argtypes = [P, P, P, P, P, I64, I64, I64, P, SZ, P]
+    lib.swiglu_bwd_w.restype = st
+    lib.swiglu_bwd_x.argtypes = [P, P, P, P, P, I64, I64, I64, P]
+    lib.swiglu_bwd_x.restype = st
+    lib.swiglu_bwd_workspace_size.argtypes = [I64, I64, I64, U]
+    lib.swiglu_bwd_workspace_size.restype = SZ
+    lib.swiglu_bwd.argtypes = [P] * 13 + [I64, I64, I64, U, P, SZ, P]
+    lib.swiglu_bwd.restype = st
+    lib.swish_grad.argtypes = [P, P, ctypes.POINTER(ctypes.c_float), P, I64, ctypes.c_int, P]
+    lib.swish_grad.restype = st
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.swg_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != SWG_OK:
+        raise SwgError(status, f"{what}: {status_string(status)}")
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dev_bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bf16, got {t.dtype}")
+    return t.contiguous()
+
+
+def _workspace(nbytes: int, device, given):
+    if given is not None:
+        return given
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+# ---------------------------------------------------------------- public API
+def swg_check(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a barrier timeout."""
+    _check(lib.swg_check(_stream(stream)), "swg_check")
+
+
+def swiglu_bwd_b_workspace_size(M: int, N: int) -> int:
+    return lib.swiglu_bwd_b_workspace_size(M, N)
+
+
+def swiglu_bwd_w_workspace_size(M: int, K: int, N: int) -> int:
+    return lib.swiglu_bwd_w_workspace_size(M, K, N)
+
+
+def swiglu_bwd_workspace_size(M: int, K: int, N: int, flags: int = SWG_UNFUSED) -> int:
+    return lib.swiglu_bwd_workspace_size(M, K, N, flags)
+
+
+def swiglu_bwd_b(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, workspace=None, stream=None):
+    """b stage: returns (dg, dfc, db_g, db_fc); db_* have shape [1, N]."""
+    dy, g, fc = (_dev_bf16(t, n) for t, n in ((dy, "dy"), (g, "g"), (fc, "fc")))
+    M, N = dy.shape
+    if g.shape != dy.shape or fc.shape != dy.shape:
+        raise ValueError("dy, g, fc must have the same [M, N] shape")
+    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
+    db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
+    ws = _workspace(lib.swiglu_bwd_b_workspace_size(M, N), dy.device, workspace)
+    _check(lib.swiglu_bwd_b(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),
+                            db_g.data_ptr(), db_fc.data_ptr(), M, N, _ptr(ws), _nbytes(ws),
+                            _stream(stream)), "swiglu_bwd_b")
+    return dg, dfc, db_g, db_fc
+
+
+def swiglu_bwd_w(x, dg, dfc, dw_g=None, dw_fc=None, workspace=None, stream=None):
+    """w stage: returns (dw_g, dw_fc), each [K, N]."""
+    x, dg, dfc = (_dev_bf16(t, n) for t, n in ((x, "x"), (dg, "dg"), (dfc, "dfc")))
+    M, K = x.shape
+    N = dg.shape[1]
+    if dg.shape != (M, N) or dfc.shape != (M, N):
+        raise ValueError("dg, dfc must be [M, N] with M = x.shape[0]")
+    if dw_g is None:
+        dw_g = torch.empty((K, N), dtype=torch.bfloat16, device=x.device)
+    if dw_fc is None:
+        dw_fc = torch.empty((K, N), dtype=torch.bfloat16, device=x.device)
+    ws = _workspace(lib.swiglu_bwd_w_workspace_size(M, K, N), x.device, workspace)
+    _check(lib.swiglu_bwd_w(x.data_ptr(), dg.data_ptr(), dfc.data_ptr(), dw_g.data_ptr(), dw_fc.data_ptr(),
+                            M, K, N, _ptr(ws), _nbytes(ws), _stream(stream)), "swiglu_bwd_w")
+    return dw_g, dw_fc
+
+
+def swiglu_bwd_x(dg, dfc, w_g, w_fc, dx=None, stream=None):
+    """x stage: returns dx [M, K]."""
+    dg, dfc, w_g, w_fc = (_dev_bf16(t, n) for t, n in ((dg, "dg"), (dfc, "dfc"), (w_g, "w_g"), (w_fc, "w_fc")))
+    M, N = dg.shape
+    K = w_g.shape[0]
+    if dfc.shape != (M, N) or w_g.shape != (K, N) or w_fc.shape != (K, N):
+        raise ValueError("shape mismatch: dg, dfc [M, N]; w_g, w_fc [K, N]")
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dg.device)
+    _check(lib.swiglu_bwd_x(dg.data_ptr(), dfc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dx.data_ptr(),
+                            M, K, N, _stream(stream)), "swiglu_bwd_x")
+    return dx
+
+
+def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = True,
+               out: dict | None = None, workspace=None, stream=None) -> dict:
+    """The whole backward. Returns a dict with dx, dw_g, dw_fc, db_g, db_fc
+    (and dg, dfc when return_dg). `out` may supply any of those tensors."""
+    x, w_g, w_fc, dy, g, fc = (_dev_bf16(t, n) for t, n in (
+        (x, "x"), (w_g, "w_g"), (w_fc, "w_fc"), (dy, "dy"), (g, "g"), (fc, "fc")))
+    M, K = x.shape
+    N = w_g.shape[1]
+    for t, n, shp in ((w_fc, "w_fc", (K, N)), (dy, "dy", (M, N)), (g, "g", (M, N)), (fc, "fc", (M, N)),
+                      (w_g, "w_g", (K, N))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{n} must have shape {shp}, got {tuple(t.shape)}")
+    out = dict(out or {})
+    shapes = dict(dx=(M, K), dw_g=(K, N), dw_fc=(K, N), db_g=(1, N), db_fc=(1, N))
+    if return_dg:
+        shapes.update(dg=(M, N), dfc=(M, N))
+    for k, shp in shapes.items():
+        if out.get(k) is None:
+            out[k] = torch.empty(shp, dtype=torch.bfloat16, device=x.device)
+    flags = SWG_FUSED if fused else SWG_UNFUSED
+    ws_flags = flags | (SWG_WS_DG_GIVEN if return_dg else 0)
+    ws = _workspace(lib.swiglu_bwd_workspace_size(M, K, N, ws_flags), x.device, workspace)
+    _check(lib.swiglu_bwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dy.data_ptr(), g.data_ptr(),
+                          fc.data_ptr(), _ptr(out.get("dg")), _ptr(out.get("dfc")), out["dx"].data_ptr(),
+                          out["dw_g"].data_ptr(), out["dw_fc"].data_ptr(), out["db_g"].data_ptr(),
+                          out["db_fc"].data_ptr(), M, K, N, flags, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "swiglu_bwd")
+    return out
+
+
+def swish_grad(grad, x, scale=None, grad_x=None, stream=None):
+    """SwishGrad: grad_x = grad * sigma(beta x) * (1 + beta x (1 - sigma(beta x))); beta = scale or 1.0."""
+    if not (isinstance(grad, torch.Tensor) and isinstance(x, torch.Tensor) and grad.is_cuda and x.is_cuda):
+        raise TypeError("grad and x must be CUDA tensors")
+    if grad.dtype != x.dtype or grad.shape != x.shape:
+        raise ValueError("grad and x must have the same dtype and shape")
+    if grad.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {grad.dtype}")
+    grad, x = grad.contiguous(), x.contiguous()
+    if grad_x is None:
+        grad_x = torch.empty_like(grad)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
+    _check(lib.swish_grad(grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
+                          _DTYPE[grad.dtype], _stream(stream)), "swish_grad")
+    return grad_x

@@ -1,0 +1,301 @@
+// C ABI of the library (declared in include/swiglu_bwd.h): argument checks,
+// workspace layout and kernel dispatch. No device memory is allocated here.
+//
+// Error model after the two-phase aclnn interface described in "SwishGrad in
+// CANN ops-nn: principle, implementation and the aclnnSwishBackward guide",
+// section 3.3 (null pointer -> its own code; unsupported dtype, mismatched
+// dtype or shape -> invalid parameter) and section 3.5 (empty tensors
+// short-circuit with no launch; a missing beta means 1.0).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/swiglu_bwd.h"
+#include "swg_launch.h"
+
+namespace {
+
+using swg::WPlan;
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;  // TMA coordinates are 32-bit
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+inline Range rng(const void* p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + static_cast<uintptr_t>(bytes)};
+}
+inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// true if any output range overlaps another output or any input range
+bool any_overlap(const Range* outs, int nout, const Range* ins, int nin) {
+  for (int i = 0; i < nout; ++i) {
+    for (int j = i + 1; j < nout; ++j)
+      if (overlap(outs[i], outs[j])) return true;
+    for (int j = 0; j < nin; ++j)
+      if (overlap(outs[i], ins[j])) return true;
+  }
+  return false;
+}
+
+// current device must be sm_103 (the kernels are built for sm_103a only)
+swg_status check_device() {
+  static std::mutex mu;
+  static int known[64] = {0};  // 0 unknown, 1 ok, 2 not ok
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SWG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(mu);
+  if (known[dev] == 0) {
+    int maj = 0, min = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SWG_ERR_CUDA;
+    known[dev] = (maj == 10 && min == 3) ? 1 : 2;
+  }
+  return known[dev] == 1 ? SWG_OK : SWG_ERR_UNSUPPORTED;
+}
+
+inline swg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SWG_OK : SWG_ERR_CUDA; }
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+swg_status check_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K < 0 || N < 0) return SWG_ERR_PARAM_INVALID;
+  if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWG_ERR_UNSUPPORTED;
+  if ((K % 8) != 0 || (N % 8) != 0) return SWG_ERR_UNSUPPORTED;
+  return SWG_OK;
+}
+
+// zero-fill a bf16 buffer of n elements (used for sums over zero rows)
+swg_status zero_bf16(void* p, int64_t n, cudaStream_t st) {
+  if (n <= 0) return SWG_OK;
+  return cuda_status(cudaMemsetAsync(p, 0, static_cast<size_t>(n) * 2, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* swg_status_string(swg_status s) {
+  switch (s) {
+    case SWG_OK: return "SWG_OK";
+    case SWG_ERR_NULLPTR: return "SWG_ERR_NULLPTR: a required pointer is NULL";
+    case SWG_ERR_PARAM_INVALID: return "SWG_ERR_PARAM_INVALID: invalid dtype, size or overlapping buffers";
+    case SWG_ERR_UNSUPPORTED:
+      return "SWG_ERR_UNSUPPORTED: K/N not a multiple of 8, misaligned pointer or device is not sm_103";
+    case SWG_ERR_WORKSPACE: return "SWG_ERR_WORKSPACE: workspace missing or smaller than the query";
+    case SWG_ERR_CUDA: return "SWG_ERR_CUDA: a CUDA call or kernel launch failed";
+    case SWG_ERR_TIMEOUT: return "SWG_ERR_TIMEOUT: a kernel gave up waiting on a pipeline barrier";
+  }
+  return "SWG_ERR_?: unknown status";
+}
+
+swg_status swg_check(swg_stream_t stream) {
+  uint32_t v = 0;
+  cudaError_t e = swg::read_and_clear_status(&v, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return SWG_ERR_CUDA;
+  return v != 0 ? SWG_ERR_TIMEOUT : SWG_OK;
+}
+
+// ---------------------------------------------------------------- SwishGrad
+swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x, int64_t n,
+                      swg_dtype dtype, swg_stream_t stream) {
+  if (grad == nullptr || x == nullptr || grad_x == nullptr) return SWG_ERR_NULLPTR;
+  if (n < 0 || (dtype != SWG_F32 && dtype != SWG_F16 && dtype != SWG_BF16)) return SWG_ERR_PARAM_INVALID;
+  const int64_t es = dtype == SWG_F32 ? 4 : 2;
+  const uintptr_t mask = static_cast<uintptr_t>(es - 1);
+  if ((reinterpret_cast<uintptr_t>(grad) & mask) || (reinterpret_cast<uintptr_t>(x) & mask) ||
+      (reinterpret_cast<uintptr_t>(grad_x) & mask))
+    return SWG_ERR_UNSUPPORTED;
+  if (n == 0) return SWG_OK;
+  // grad_x may alias grad or x exactly, but must not partially overlap either
+  const Range o = rng(grad_x, n * es), a = rng(grad, n * es), b = rng(x, n * es);
+  if ((overlap(o, a) && o.lo != a.lo) || (overlap(o, b) && o.lo != b.lo)) return SWG_ERR_PARAM_INVALID;
+  swg_status st = check_device();
+  if (st != SWG_OK) return st;
+  const float beta = scale != nullptr ? *scale : 1.0f;
+  return cuda_status(swg::launch_swish_grad(grad, x, beta, grad_x, n, static_cast<int>(dtype),
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- b stage
+size_t swiglu_bwd_b_workspace_size(int64_t M, int64_t N) {
+  if (M <= 0 || N <= 0) return 0;
+  return swg::b_workspace_bytes(M, N);
+}
+
+swg_status swiglu_bwd_b(const void* dy, const void* g, const void* fc, void* dg, void* dfc, void* db_g,
+                        void* db_fc, int64_t M, int64_t N, void* workspace, size_t workspace_bytes,
+                        swg_stream_t stream) {
+  if (!dy || !g || !fc || !dg || !dfc || !db_g || !db_fc) return SWG_ERR_NULLPTR;
+  swg_status st = check_shape(M, 8, N);
+  if (st != SWG_OK) return st;
+  if (N == 0) return SWG_OK;
+  const void* all[] = {dy, g, fc, dg, dfc, db_g, db_fc};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const int64_t mn = M * N * 2;
+  const Range outs[] = {rng(dg, mn), rng(dfc, mn), rng(db_g, N * 2), rng(db_fc, N * 2)};
+  const Range ins[] = {rng(dy, mn), rng(g, mn), rng(fc, mn)};
+  if (any_overlap(outs, 4, ins, 3)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    st = zero_bf16(db_g, N, s);
+    return st != SWG_OK ? st : zero_bf16(db_fc, N, s);
+  }
+  const size_t need = swg::b_workspace_bytes(M, N);
+  if (workspace == nullptr || workspace_bytes < need) return SWG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SWG_ERR_UNSUPPORTED;
+  const Range w = rng(workspace, static_cast<int64_t>(need));
+  if (any_overlap(&w, 1, outs, 4) || any_overlap(&w, 1, ins, 3)) return SWG_ERR_PARAM_INVALID;
+  return cuda_status(swg::launch_b_stage(
+      static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+      static_cast<uint16_t*>(dg), static_cast<uint16_t*>(dfc), static_cast<uint16_t*>(db_g),
+      static_cast<uint16_t*>(db_fc), M, N, workspace, s));
+}
+
+// ---------------------------------------------------------------- w stage
+size_t swiglu_bwd_w_workspace_size(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  return swg::w_plan(M, K, N, swg::device_sm_count()).ws_bytes;
+}
+
+swg_status swiglu_bwd_w(const void* x, const void* dg, const void* dfc, void* dw_g, void* dw_fc, int64_t M,
+                        int64_t K, int64_t N, void* workspace, size_t workspace_bytes, swg_stream_t stream) {
+  if (!x || !dg || !dfc || !dw_g || !dw_fc) return SWG_ERR_NULLPTR;
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (K == 0 || N == 0) return SWG_OK;
+  const void* all[] = {x, dg, dfc, dw_g, dw_fc};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const Range outs[] = {rng(dw_g, K * N * 2), rng(dw_fc, K * N * 2)};
+  const Range ins[] = {rng(x, M * K * 2), rng(dg, M * N * 2), rng(dfc, M * N * 2)};
+  if (any_overlap(outs, 2, ins, 3)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    st = zero_bf16(dw_g, K * N, s);
+    return st != SWG_OK ? st : zero_bf16(dw_fc, K * N, s);
+  }
+  const WPlan plan = swg::w_plan(M, K, N, swg::device_sm_count());
+  if (plan.ws_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return SWG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SWG_ERR_UNSUPPORTED;
+    const Range w = rng(workspace, static_cast<int64_t>(plan.ws_bytes));
+    if (any_overlap(&w, 1, outs, 2) || any_overlap(&w, 1, ins, 3)) return SWG_ERR_PARAM_INVALID;
+  }
+  return cuda_status(swg::launch_w_gemm(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dg),
+                                        static_cast<const uint16_t*>(dfc), static_cast<uint16_t*>(dw_g),
+                                        static_cast<uint16_t*>(dw_fc), M, K, N, workspace, plan, s));
+}
+
+// ---------------------------------------------------------------- x stage
+swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const void* w_fc, void* dx, int64_t M,
+                        int64_t K, int64_t N, swg_stream_t stream) {
+  if (!dg || !dfc || !w_g || !w_fc || !dx) return SWG_ERR_NULLPTR;
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (M == 0 || K == 0) return SWG_OK;
+  const void* all[] = {dg, dfc, w_g, w_fc, dx};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const Range outs[] = {rng(dx, M * K * 2)};
+  const Range ins[] = {rng(dg, M * N * 2), rng(dfc, M * N * 2), rng(w_g, K * N * 2), rng(w_fc, K * N * 2)};
+  if (any_overlap(outs, 1, ins, 4)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (N == 0) return cuda_status(cudaMemsetAsync(dx, 0, static_cast<size_t>(M * K * 2), s));
+  return cuda_status(swg::launch_x_gemm(static_cast<const uint16_t*>(dg), static_cast<const uint16_t*>(dfc),
+                                        static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc),
+                                        static_cast<uint16_t*>(dx), M, K, N, s));
+}
+
+// ---------------------------------------------------------------- whole backward
+// Unfused workspace layout: [dg scratch 2MN | dfc scratch 2MN] (only when the
+// caller passes NULL dg/dfc) | b-stage partials | w-stage partials; each
+// region starts on a 256-byte boundary.
+size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags) {
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  const bool fused = (flags & SWG_FUSED) != 0;
+  if (fused) return 0;  // fused path not available in this build (see swiglu_bwd)
+  size_t total = 0;
+  if (!(flags & SWG_WS_DG_GIVEN)) total += 2 * align256(static_cast<size_t>(M) * N * 2);
+  total += align256(swg::b_workspace_bytes(M, N));
+  total += align256(swg::w_plan(M, K, N, swg::device_sm_count()).ws_bytes);
+  return total;
+}
+
+swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const void* dy, const void* g,
+                      const void* fc, void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc, void* db_g,
+                      void* db_fc, int64_t M, int64_t K, int64_t N, unsigned flags, void* workspace,
+                      size_t workspace_bytes, swg_stream_t stream) {
+  if (!x || !w_g || !w_fc || !dy || !g || !fc || !dx || !dw_g || !dw_fc || !db_g || !db_fc)
+    return SWG_ERR_NULLPTR;
+  if ((dg == nullptr) != (dfc == nullptr)) return SWG_ERR_NULLPTR;
+  if ((flags & ~(SWG_FUSED | SWG_WS_DG_GIVEN)) != 0) return SWG_ERR_PARAM_INVALID;
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (K == 0 || N == 0) return SWG_OK;
+  const void* all[] = {x, w_g, w_fc, dy, g, fc, dx, dw_g, dw_fc, db_g, db_fc};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  if (dg != nullptr && (!aligned16(dg) || !aligned16(dfc))) return SWG_ERR_UNSUPPORTED;
+  const int64_t mn = M * N * 2, kn = K * N * 2;
+  const Range outs[] = {rng(dx, M * K * 2), rng(dw_g, kn), rng(dw_fc, kn), rng(db_g, N * 2), rng(db_fc, N * 2),
+                        rng(dg, dg ? mn : 0), rng(dfc, dfc ? mn : 0)};
+  const Range ins[] = {rng(x, M * K * 2), rng(w_g, kn), rng(w_fc, kn), rng(dy, mn), rng(g, mn), rng(fc, mn)};
+  if (any_overlap(outs, 7, ins, 6)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  if (flags & SWG_FUSED) return SWG_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    st = zero_bf16(dw_g, K * N, s);
+    if (st == SWG_OK) st = zero_bf16(dw_fc, K * N, s);
+    if (st == SWG_OK) st = zero_bf16(db_g, N, s);
+    if (st == SWG_OK) st = zero_bf16(db_fc, N, s);
+    return st;
+  }
+  const unsigned wsflags = flags | (dg != nullptr ? SWG_WS_DG_GIVEN : 0u);
+  const size_t need = swiglu_bwd_workspace_size(M, K, N, wsflags);
+  if (workspace == nullptr || workspace_bytes < need) return SWG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SWG_ERR_UNSUPPORTED;
+  const Range w = rng(workspace, static_cast<int64_t>(need));
+  if (any_overlap(&w, 1, outs, 7) || any_overlap(&w, 1, ins, 6)) return SWG_ERR_PARAM_INVALID;
+
+  uint8_t* wp = static_cast<uint8_t*>(workspace);
+  uint16_t* dgp = static_cast<uint16_t*>(dg);
+  uint16_t* dfcp = static_cast<uint16_t*>(dfc);
+  if (dgp == nullptr) {
+    dgp = reinterpret_cast<uint16_t*>(wp);
+    wp += align256(static_cast<size_t>(mn));
+    dfcp = reinterpret_cast<uint16_t*>(wp);
+    wp += align256(static_cast<size_t>(mn));
+  }
+  void* bws = wp;
+  wp += align256(swg::b_workspace_bytes(M, N));
+  void* wws = wp;
+  const WPlan plan = swg::w_plan(M, K, N, swg::device_sm_count());
+
+  cudaError_t e = swg::launch_b_stage(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g),
+                                      static_cast<const uint16_t*>(fc), dgp, dfcp, static_cast<uint16_t*>(db_g),
+                                      static_cast<uint16_t*>(db_fc), M, N, bws, s);
+  if (e != cudaSuccess) return SWG_ERR_CUDA;
+  e = swg::launch_w_gemm(static_cast<const uint16_t*>(x), dgp, dfcp, static_cast<uint16_t*>(dw_g),
+                         static_cast<uint16_t*>(dw_fc), M, K, N, wws, plan, s);
+  if (e != cudaSuccess) return SWG_ERR_CUDA;
+  e = swg::launch_x_gemm(dgp, dfcp, static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc),
+                         static_cast<uint16_t*>(dx), M, K, N, s);
+  return cuda_status(e);
+}
+
+}  // extern "C"

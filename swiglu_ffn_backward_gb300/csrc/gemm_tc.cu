@@ -1,0 +1,429 @@
+// w and x stages of the SwiGLU-FFN backward as tcgen05 (TMEM-accumulator) bf16
+// GEMMs fed by TMA.
+//
+// Source: "PyPTO-Gym in practice: the fused SwiGLU backward operator",
+// "Algorithm overview and formulas" items 3-4 and the w/x rows of "Kernel
+// signatures":
+//   x stage: dx = dg W_g^T + dfc W_fc^T  -- one GEMM [dg | dfc] [W_g | W_fc]^T,
+//            reduction length 2N; the k loop walks (dg, W_g) then (dfc, W_fc).
+//   w stage: dw_g = x^T dg, dw_fc = x^T dfc -- one launch, the two outputs are
+//            two tile sets; the reduction runs over M and is split into S
+//            chunks whose fp32 partials a second kernel adds in a fixed order.
+// bf16 operands, fp32 accumulation in TMEM, one bf16 rounding per output
+// ("Dtype conversion flow": matmul accumulates in fp32).
+//
+// CTA = 6 warps: warp 0 lane 0 issues TMA loads into a STAGES-deep ring of
+// shared-memory operand tiles; warp 1 owns the TMEM allocation and lane 0
+// issues tcgen05.mma (M=128, N=256, K=16 per instruction) and tcgen05.commit;
+// warps 2-5 read the 128x256 fp32 accumulator out of TMEM (each warp its own
+// 32-lane quarter) and store bf16 (or fp32 partials).
+//
+// Operand layouts (shared memory, 128-byte swizzle, written by TMA):
+//   x stage, K-major: A tile = 128 rows of dg/dfc x 64 reduction elements;
+//     B tile = 256 rows of W x 64 reduction elements; 8-row groups 1024 B
+//     apart (SBO), +32 B per K=16 step.
+//   w stage, MN-major: the reduction index m is the strided one. A tile =
+//     x[m0:m0+64, k0:k0+128] as two 64x64 boxes (8 KB apart = LBO, the stride
+//     between 64-element MN chunks), B tile = dg[m0:m0+64, n0:n0+256] as four
+//     boxes; 8-row k groups 1024 B apart (SBO), +2048 B per K=16 step.
+// Tails of M, K and N are zero-filled by TMA on load and masked on store.
+//
+// Every mbarrier wait is bounded; on timeout the kernel ORs a flag into the
+// module status word, stops issuing, waits (bounded) for its own TMA copies
+// and MMAs still in flight, frees TMEM and returns.
+#include <mutex>
+
+#include "swg_device.cuh"
+#include "swg_launch.h"
+
+namespace swg {
+
+__device__ uint32_t g_status = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+
+enum Mode : int { kModeX = 0, kModeW = 1 };
+
+struct __align__(1024) Smem {
+  uint8_t a[STAGES][A_BYTES];
+  uint8_t b[STAGES][B_BYTES];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t accum;
+  uint32_t tmem_base;
+  volatile uint32_t abort_flag;
+  volatile uint32_t issued;
+  volatile uint32_t consumed;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct GemmArgs {
+  int M, K, N;
+  // x stage
+  uint16_t* dx;
+  int tiles_k;  // dx column tiles
+  int nkb_half; // reduction blocks per half (ceil(N / 64))
+  // w stage
+  uint16_t* dw[2];
+  float* ws;
+  int splits, kb_per, nkb_total;
+  int tiles_kw, tiles_nw;  // dw tile grid per problem
+};
+
+__device__ __forceinline__ void flag_timeout(Smem& s) {
+  atomicOr(&g_status, kStatusTimeout);
+  s.abort_flag = 1u;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- tile coordinates
+  int m0 = 0, n0 = 0, prob = 0, split = 0, kb_begin = 0, kb_end = 0;
+  if (MODE == kModeX) {
+    const int t = blockIdx.x;
+    n0 = (t % args.tiles_k) * BN;      // dx columns (index k of W)
+    m0 = (t / args.tiles_k) * BM;      // dx rows
+    kb_begin = 0;
+    kb_end = 2 * args.nkb_half;
+  } else {
+    int t = blockIdx.x;
+    const int nt = t % args.tiles_nw;
+    t /= args.tiles_nw;
+    const int kt = t % args.tiles_kw;
+    t /= args.tiles_kw;
+    prob = t % 2;
+    split = t / 2;
+    m0 = kt * BM;                      // dw rows (index k)
+    n0 = nt * BN;                      // dw columns (index n)
+    kb_begin = split * args.kb_per;
+    kb_end = min(args.nkb_total, kb_begin + args.kb_per);
+  }
+  const int nkb = kb_end - kb_begin;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(&s.accum, 1);
+    s.abort_flag = 0u;
+    s.issued = 0u;
+    s.consumed = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    uint32_t issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % STAGES;
+      const int use = i / STAGES;
+      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1)) {
+        flag_timeout(s);
+        break;
+      }
+      if (s.abort_flag) break;
+      mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+      const int kb = kb_begin + i;
+      if (MODE == kModeX) {
+        const bool second = kb >= args.nkb_half;
+        const int r0 = (second ? kb - args.nkb_half : kb) * BK;  // reduction offset within N
+        tma_load_2d(s.a[st], second ? &tmA1 : &tmA0, &s.full[st], r0, m0);
+        tma_load_2d(s.b[st], second ? &tmB1 : &tmB0, &s.full[st], r0, n0);
+      } else {
+        const int mr = kb * BK;  // reduction rows of M
+        tma_load_2d(s.a[st], &tmA0, &s.full[st], m0, mr);
+        tma_load_2d(s.a[st] + 8192, &tmA0, &s.full[st], m0 + 64, mr);
+        const CUtensorMap* tb = prob ? &tmB1 : &tmB0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_load_2d(s.b[st] + j * 8192, tb, &s.full[st], n0 + 64 * j, mr);
+      }
+      issued = i + 1;
+      s.issued = issued;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, MODE == kModeW, MODE == kModeW);
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % STAGES;
+      if (!mbar_wait(&s.full[st], (i / STAGES) & 1)) {
+        flag_timeout(s);
+        break;
+      }
+      s.consumed = i + 1;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(s.a[st]);
+      const uint32_t b_addr = smem_u32(s.b[st]);
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        uint64_t ad, bd;
+        if (MODE == kModeX) {
+          ad = smem_desc(a_addr + 32 * k, 16, 1024);
+          bd = smem_desc(b_addr + 32 * k, 16, 1024);
+        } else {
+          ad = smem_desc(a_addr + 2048 * k, 8192, 1024);
+          bd = smem_desc(b_addr + 2048 * k, 8192, 1024);
+        }
+        umma_bf16(tmem, ad, bd, idesc, (i > 0 || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&s.empty[st]);
+    }
+    umma_commit(&s.accum);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const bool ok = mbar_wait(&s.accum, 0);
+    if (!ok) flag_timeout(s);
+    tc_fence_after();
+    const int r = q * 32 + lane;  // accumulator row
+    if (ok && !s.abort_flag && nkb > 0) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+        tmem_ld_wait();
+        const int row = m0 + r;
+        const int col = n0 + c * 32;
+        if (MODE == kModeX) {
+          if (row < args.M) {
+            uint4* dst = reinterpret_cast<uint4*>(args.dx + static_cast<int64_t>(row) * args.K + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (col + 8 * j < args.K) {
+                dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+              }
+            }
+          }
+        } else {
+          if (row < args.K) {
+            if (args.splits == 1) {
+              uint4* dst = reinterpret_cast<uint4*>(args.dw[prob] + static_cast<int64_t>(row) * args.N + col);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (col + 8 * j < args.N) {
+                  dst[j] =
+                      make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                }
+              }
+            } else {
+              float* dst = args.ws + (static_cast<int64_t>(split * 2 + prob) * args.K + row) * args.N + col;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (col + 4 * j < args.N) {
+                  reinterpret_cast<uint4*>(dst)[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && s.abort_flag) {
+    // drain: TMA copies issued but never consumed must land before the CTA exits
+    for (uint32_t i = s.consumed; i < s.issued; ++i) {
+      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dw[p][k][n] = sum_s ws[s][p][k][n] (fixed order), rounded once to bf16.
+__global__ void __launch_bounds__(256) w_split_reduce_kernel(const float4* __restrict__ ws, int splits,
+                                                             int64_t per_prob4, uint2* __restrict__ dw_g,
+                                                             uint2* __restrict__ dw_fc) {
+  const int64_t total4 = 2 * per_prob4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 acc = ws[i];
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 v = ws[static_cast<int64_t>(sp) * total4 + i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const uint2 o = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    if (i < per_prob4)
+      dw_g[i] = o;
+    else
+      dw_fc[i - per_prob4] = o;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+template <int MODE>
+cudaError_t prepare_kernel() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+
+}  // namespace
+
+bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+WPlan w_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
+  WPlan p;
+  const int64_t nkb = (M + BK - 1) / BK;
+  const int64_t tiles = 2 * ((K + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int64_t splits = num_sms / tiles;
+  if (splits < 1) splits = 1;
+  // keep at least 8 reduction blocks (512 rows) per split
+  const int64_t max_by_len = nkb / 8 > 0 ? nkb / 8 : 1;
+  if (splits > max_by_len) splits = max_by_len;
+  if (splits > 64) splits = 64;
+  p.kb_per = nkb > 0 ? (nkb + splits - 1) / splits : 0;
+  p.splits = p.kb_per > 0 ? (nkb + p.kb_per - 1) / p.kb_per : 1;
+  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * 2 * K * N * sizeof(float) : 0;
+  return p;
+}
+
+cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_t* w_g, const uint16_t* w_fc,
+                          uint16_t* dx, int64_t M, int64_t K, int64_t N, cudaStream_t stream) {
+  CUtensorMap a0, a1, b0, b1;
+  const uint64_t rs = static_cast<uint64_t>(N) * 2;
+  if (!encode_tmap_2d_bf16(&a0, dg, N, M, rs, BK, BM) || !encode_tmap_2d_bf16(&a1, dfc, N, M, rs, BK, BM) ||
+      !encode_tmap_2d_bf16(&b0, w_g, N, K, rs, BK, BN) || !encode_tmap_2d_bf16(&b1, w_fc, N, K, rs, BK, BN))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.dx = dx;
+  a.tiles_k = static_cast<int>((K + BN - 1) / BN);
+  a.nkb_half = static_cast<int>((N + BK - 1) / BK);
+  const int64_t tiles = ((M + BM - 1) / BM) * a.tiles_k;
+  cudaError_t e = prepare_kernel<kModeX>();
+  if (e != cudaSuccess) return e;
+  tc_gemm_kernel<kModeX><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(a0, a1, b0, b1, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
+                          uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
+                          cudaStream_t stream) {
+  CUtensorMap a0, b0, b1;
+  if (!encode_tmap_2d_bf16(&a0, x, K, M, static_cast<uint64_t>(K) * 2, 64, BK) ||
+      !encode_tmap_2d_bf16(&b0, dg, N, M, static_cast<uint64_t>(N) * 2, 64, BK) ||
+      !encode_tmap_2d_bf16(&b1, dfc, N, M, static_cast<uint64_t>(N) * 2, 64, BK))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.dw[0] = dw_g;
+  a.dw[1] = dw_fc;
+  a.ws = static_cast<float*>(ws);
+  a.splits = static_cast<int>(plan.splits);
+  a.kb_per = static_cast<int>(plan.kb_per);
+  a.nkb_total = static_cast<int>((M + BK - 1) / BK);
+  a.tiles_kw = static_cast<int>((K + BM - 1) / BM);
+  a.tiles_nw = static_cast<int>((N + BN - 1) / BN);
+  const int64_t ctas = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
+  cudaError_t e = prepare_kernel<kModeW>();
+  if (e != cudaSuccess) return e;
+  tc_gemm_kernel<kModeW><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(a0, a0, b0, b1, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || plan.splits == 1) return e;
+  const int64_t per_prob4 = K * N / 4;
+  int64_t blocks = (2 * per_prob4 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  w_split_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const float4*>(ws), static_cast<int>(plan.splits), per_prob4, reinterpret_cast<uint2*>(dw_g),
+      reinterpret_cast<uint2*>(dw_fc));
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
+}  // namespace swg

@@ -1,0 +1,52 @@
+// Internal host-side launchers (C++ linkage). The C ABI in include/swiglu_bwd.h
+// validates arguments and then calls these.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace swg {
+
+// ---- SwishGrad: dtype 0 = f32, 1 = f16, 2 = bf16
+cudaError_t launch_swish_grad(const void* grad, const void* x, float beta, void* grad_x, int64_t n, int dtype,
+                              cudaStream_t stream);
+
+// ---- b stage
+struct BPlan {
+  int64_t rows_per_chunk;  // rows of M per CTA row-chunk (multiple of 8)
+  int64_t chunks;          // number of row chunks = fp32 partial rows in the workspace
+};
+BPlan b_plan(int64_t M, int64_t N);
+size_t b_workspace_bytes(int64_t M, int64_t N);
+// dg/dfc may be null (then only the column sums are produced)
+cudaError_t launch_b_stage(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, uint16_t* dg, uint16_t* dfc,
+                           uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t N, void* ws, cudaStream_t stream);
+// db from fp32 partials [chunks][2N] -> bf16 db_g, db_fc (fixed order)
+cudaError_t launch_db_reduce(const float* partials, int64_t chunks, int64_t N, uint16_t* db_g, uint16_t* db_fc,
+                             cudaStream_t stream);
+
+// ---- tcgen05 GEMMs
+struct WPlan {
+  int64_t splits;     // M split count for the dw reduction
+  int64_t kb_per;     // 64-row reduction blocks per split
+  size_t ws_bytes;    // fp32 partials (0 when splits == 1)
+};
+WPlan w_plan(int64_t M, int64_t K, int64_t N, int num_sms);
+int device_sm_count();
+
+cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_t* w_g, const uint16_t* w_fc,
+                          uint16_t* dx, int64_t M, int64_t K, int64_t N, cudaStream_t stream);
+cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
+                          uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
+                          cudaStream_t stream);
+
+// module status word (timeouts)
+cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream);
+
+// tensor-map encoding (driver entry point resolved once)
+bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace swg

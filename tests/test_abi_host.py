@@ -1,0 +1,133 @@
+"""The C-ABI library on the host: it loads, exports every function that
+include/*.h declares, and rejects bad arguments before any device work.
+
+These calls pass fake, never-dereferenced addresses: every case returns from
+the argument checks before any CUDA call, so no GPU is needed.
+"""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def swg():
+    import swiglu_ffn_backward_gb300 as m
+    return m
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("swiglu_bwd", "swiglu_bwd_b", "swiglu_bwd_w", "swiglu_bwd_x", "swish_grad",
+              "swiglu_bwd_workspace_size", "swg_status_string", "swg_check"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(swg):
+    lib = ctypes.CDLL(swg.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(swg.EXPORTS) <= _declared_functions()
+
+
+def test_status_strings(swg):
+    from swiglu_ffn_backward_gb300 import _binding as b
+    for code in range(7):
+        s = b.status_string(code)
+        assert s.startswith("SWG_")
+    assert "unknown" in b.status_string(99)
+
+
+FAKE = 0x7f0000000000  # 16-byte aligned, never dereferenced
+
+
+def _lib(swg):
+    from swiglu_ffn_backward_gb300 import _binding as b
+    return b.lib, b
+
+
+def test_null_pointers(swg):
+    lib, b = _lib(swg)
+    assert lib.swish_grad(None, FAKE, None, FAKE, 10, b.SWG_F32, None) == b.SWG_ERR_NULLPTR
+    assert lib.swiglu_bwd_b(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, None, 0, None) == b.SWG_ERR_NULLPTR
+    assert lib.swiglu_bwd_w(FAKE, FAKE, None, FAKE, FAKE, 4, 8, 8, None, 0, None) == b.SWG_ERR_NULLPTR
+    assert lib.swiglu_bwd_x(FAKE, FAKE, FAKE, FAKE, None, 4, 8, 8, None) == b.SWG_ERR_NULLPTR
+    # dg given without dfc
+    args = [FAKE + i * 0x1000000 for i in range(13)]
+    args[7] = None
+    assert lib.swiglu_bwd(*args, 4, 8, 8, 0, None, 0, None) == b.SWG_ERR_NULLPTR
+
+
+def test_invalid_sizes_and_dtypes(swg):
+    lib, b = _lib(swg)
+    assert lib.swish_grad(FAKE, FAKE + 4096, None, FAKE + 8192, -1, b.SWG_F32, None) == b.SWG_ERR_PARAM_INVALID
+    assert lib.swish_grad(FAKE, FAKE + 4096, None, FAKE + 8192, 10, 7, None) == b.SWG_ERR_PARAM_INVALID
+    assert lib.swiglu_bwd_x(FAKE, FAKE + 2**24, FAKE + 2**25, FAKE + 2**26, FAKE + 2**27, -1, 8, 8,
+                            None) == b.SWG_ERR_PARAM_INVALID
+    base = [FAKE + i * 2**26 for i in range(13)]
+    assert lib.swiglu_bwd(*base, 4, 8, 8, 0x40, None, 0, None) == b.SWG_ERR_PARAM_INVALID  # unknown flag
+
+
+def test_unsupported_shapes_and_alignment(swg):
+    lib, b = _lib(swg)
+    p = [FAKE + i * 2**26 for i in range(7)]
+    # N not a multiple of 8
+    assert lib.swiglu_bwd_b(*p, 16, 12, None, 0, None) == b.SWG_ERR_UNSUPPORTED
+    # K not a multiple of 8
+    assert lib.swiglu_bwd_x(p[0], p[1], p[2], p[3], p[4], 16, 12, 16, None) == b.SWG_ERR_UNSUPPORTED
+    # misaligned pointer
+    q = list(p)
+    q[2] += 2
+    assert lib.swiglu_bwd_b(*q, 16, 16, None, 0, None) == b.SWG_ERR_UNSUPPORTED
+    # fp32 swish_grad pointer not 4-byte aligned
+    assert lib.swish_grad(FAKE + 2, FAKE + 4096, None, FAKE + 8192, 10, b.SWG_F32, None) == b.SWG_ERR_UNSUPPORTED
+    # M beyond 32-bit TMA coordinates
+    assert lib.swiglu_bwd_x(p[0], p[1], p[2], p[3], p[4], 2**31, 8, 8, None) == b.SWG_ERR_UNSUPPORTED
+
+
+def test_overlapping_buffers(swg):
+    lib, b = _lib(swg)
+    M, N = 64, 64
+    mn = M * N * 2
+    dy, g, fc = FAKE, FAKE + mn, FAKE + 2 * mn
+    # dg overlaps fc
+    assert lib.swiglu_bwd_b(dy, g, fc, fc + 16, FAKE + 8 * mn, FAKE + 10 * mn, FAKE + 11 * mn, M, N,
+                            None, 0, None) == b.SWG_ERR_PARAM_INVALID
+    # grad_x partially overlapping grad is rejected (exact aliasing is allowed)
+    assert lib.swish_grad(FAKE, FAKE + 4096, None, FAKE + 16, 100, b.SWG_F32, None) == b.SWG_ERR_PARAM_INVALID
+
+
+def test_workspace_queries(swg):
+    assert swg.swiglu_bwd_b_workspace_size(0, 1024) == 0
+    assert swg.swiglu_bwd_b_workspace_size(220000, 1024) > 0
+    assert swg.swiglu_bwd_b_workspace_size(220000, 1024) % 16 == 0
+    # the unfused whole backward needs room for dg, dfc unless the caller passes them
+    M, K, N = 220000, 512, 1024
+    assert swg.swiglu_bwd_workspace_size(M, K, N, 0) >= 4 * M * N
+    assert swg.swiglu_bwd_workspace_size(M, K, N, 0x100) < 4 * M * N
+
+
+def test_python_binding_requires_cuda_tensors(swg):
+    import torch
+    t = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        swg.swiglu_bwd_b(t, t, t)
+    with pytest.raises(TypeError):
+        swg.swish_grad(t, t, 1.0)

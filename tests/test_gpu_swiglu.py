@@ -1,0 +1,159 @@
+"""SwiGLU-FFN backward through the C ABI vs the fp64 oracle (GPU).
+
+Inputs are drawn once on the GPU from the seeded recipes in `synth` and copied
+to the host for the oracle, so both sides see the same bf16 bits.
+
+Stage calls (b, w, x) are compared with the oracle's stage functions fed the
+SAME inputs the stage received: the w and x stages get the GPU b stage's bf16
+dg, dfc, so their comparison isolates the GEMM. The whole backward is compared
+with the oracle's whole backward, in which dg, dfc enter the w and x stages as
+bf16 values, and additionally (scale-aware checks only) with the exact
+gradient without that rounding.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import SWIGLU_CONFIGS, SwigluShape, swiglu_inputs
+
+from ._parity import assert_all, compare, to_f64
+
+pytestmark = pytest.mark.gpu
+
+FULL_ORACLE_MAX_MN = 5_000_000  # above this, sample rows/columns
+
+
+def _swg():
+    import swiglu_ffn_backward_gb300 as swg
+    return swg
+
+
+def _np(inp):
+    return {k: to_f64(v) for k, v in inp.items()}
+
+
+def _full_case(shape: SwigluShape, fused: bool):
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    out = swg.swiglu_bwd(**inp, fused=fused, return_dg=True)
+    swg.swg_check()
+    h = _np(inp)
+    ref = oracle.swiglu_bwd(h["x"], h["w_g"], h["w_fc"], h["dy"], h["g"], h["fc"], stage_dtype="bf16")
+    reps = [compare(k, out[k], ref[k]) for k in ("dg", "dfc", "db_g", "db_fc", "dw_g", "dw_fc", "dx")]
+    exact = oracle.swiglu_bwd(h["x"], h["w_g"], h["w_fc"], h["dy"], h["g"], h["fc"], stage_dtype=None)
+    for k in ("dw_g", "dw_fc", "dx"):
+        r = compare(k, out[k], exact[k])
+        r["ok"] = r["finite"] and r["max_err"] <= 2.0 ** -6 * r["max_ref"] and r["rel_l2"] <= 2.0 ** -8
+        r["name"] = k + "(exact)"
+        reps.append(r)
+    return reps
+
+
+def _sampled_case(shape: SwigluShape, fused: bool, n_rows=384, n_cols=96):
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    out = swg.swiglu_bwd(**inp, fused=fused, return_dg=True)
+    swg.swg_check()
+    rng = np.random.default_rng(shape.seed + 101)
+    M, N = shape.M, shape.N
+    rows = np.unique(np.concatenate([rng.choice(M, size=min(n_rows, M), replace=False), [0, M - 1]]))
+    cols = np.unique(np.concatenate([rng.choice(N, size=min(n_cols, N), replace=False), [0, N - 1]]))
+    cpu = {k: v.cpu() for k, v in inp.items()}
+    ref = oracle.swiglu_bwd_sampled(cpu["x"], cpu["w_g"], cpu["w_fc"], cpu["dy"], cpu["g"], cpu["fc"],
+                                    rows, cols, stage_dtype="bf16")
+    rt = torch.as_tensor(rows, device="cuda")
+    ct = torch.as_tensor(cols, device="cuda")
+    reps = [compare("dg", out["dg"][rt], ref["dg"]), compare("dfc", out["dfc"][rt], ref["dfc"]),
+            compare("dx", out["dx"][rt], ref["dx"])]
+    for k in ("db_g", "db_fc", "dw_g", "dw_fc"):
+        reps.append(compare(k, out[k][:, ct], ref[k]))
+    return reps
+
+
+def _shapes(names):
+    return [s for n in names for s in SWIGLU_CONFIGS[n]]
+
+
+@pytest.mark.parametrize("shape", _shapes(["tiny", "tail"]), ids=lambda s: s.name)
+def test_swiglu_bwd_unfused(shape):
+    if shape.M * shape.N <= FULL_ORACLE_MAX_MN:
+        assert_all(_full_case(shape, fused=False))
+    else:
+        assert_all(_sampled_case(shape, fused=False))
+
+
+@pytest.mark.parametrize("shape", _shapes(["pages", "llm"]), ids=lambda s: s.name)
+def test_swiglu_bwd_unfused_full_size(shape):
+    assert_all(_sampled_case(shape, fused=False))
+
+
+ODD = [SwigluShape("odd_M300_K72_N200", 300, 72, 200, 4, "tail"),
+       SwigluShape("odd_M129_K8_N8", 129, 8, 8, 5, "tail"),
+       SwigluShape("odd_M2_K520_N264", 2, 520, 264, 6, "tail")]
+
+
+@pytest.mark.parametrize("shape", ODD, ids=lambda s: s.name)
+def test_swiglu_bwd_odd_shapes(shape):
+    assert_all(_full_case(shape, fused=False))
+
+
+@pytest.mark.parametrize("shape", _shapes(["tiny"]) + [SWIGLU_CONFIGS["tail"][2], ODD[0]], ids=lambda s: s.name)
+def test_stage_calls(shape):
+    """b, then w and x on the GPU's own bf16 dg, dfc (stage oracles)."""
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    dg, dfc, db_g, db_fc = swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"])
+    dw_g, dw_fc = swg.swiglu_bwd_w(inp["x"], dg, dfc)
+    dx = swg.swiglu_bwd_x(dg, dfc, inp["w_g"], inp["w_fc"])
+    swg.swg_check()
+    h = _np(inp)
+    rdg, rdfc, rdbg, rdbfc = oracle.swiglu_bwd_b(h["dy"], h["g"], h["fc"])
+    gdg, gdfc = to_f64(dg), to_f64(dfc)
+    rdwg, rdwfc = oracle.swiglu_bwd_w(h["x"], gdg, gdfc)
+    rdx = oracle.swiglu_bwd_x(gdg, gdfc, h["w_g"], h["w_fc"])
+    assert_all([compare("dg", dg, rdg), compare("dfc", dfc, rdfc), compare("db_g", db_g, rdbg),
+                compare("db_fc", db_fc, rdbfc), compare("dw_g", dw_g, rdwg), compare("dw_fc", dw_fc, rdwfc),
+                compare("dx", dx, rdx)])
+
+
+def test_empty_M_writes_zero_sums():
+    swg = _swg()
+    K, N = 64, 128
+    z = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
+    out = dict(dx=z(0, K), dw_g=z(K, N).fill_(7), dw_fc=z(K, N).fill_(7), db_g=z(1, N).fill_(7),
+               db_fc=z(1, N).fill_(7), dg=z(0, N), dfc=z(0, N))
+    swg.swiglu_bwd(z(0, K), z(K, N), z(K, N), z(0, N), z(0, N), z(0, N), out=out)
+    torch.cuda.synchronize()
+    for k in ("dw_g", "dw_fc", "db_g", "db_fc"):
+        assert torch.count_nonzero(out[k]) == 0, k
+
+
+def test_db_equals_sum_of_dg_and_linearity():
+    """db_g agrees with the fp64 sum of the GPU's dg (up to dg's bf16 rounding),
+    and doubling dy doubles every output exactly."""
+    swg = _swg()
+    shape = SWIGLU_CONFIGS["tail"][3]  # M=4097
+    inp = swiglu_inputs(shape, device="cuda")
+    a = swg.swiglu_bwd(**inp)
+    inp2 = dict(inp, dy=inp["dy"] * 2)
+    b = swg.swiglu_bwd(**inp2)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(b[k].float(), a[k].float() * 2), k
+    s = to_f64(a["dg"]).sum(axis=0)
+    db = to_f64(a["db_g"]).ravel()
+    # each bf16 dg is within 2^-9 relative of the fp32 value that db sums
+    slack = 2.0 ** -9 * np.abs(to_f64(a["dg"])).sum(axis=0) + 2.0 ** -8 * np.abs(db) + 1e-6
+    assert np.all(np.abs(s - db) <= slack)
+
+
+def test_deterministic():
+    swg = _swg()
+    inp = swiglu_inputs(SWIGLU_CONFIGS["tail"][3], device="cuda")
+    a = swg.swiglu_bwd(**inp)
+    b = swg.swiglu_bwd(**inp)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
