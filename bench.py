@@ -1,0 +1,419 @@
+"""Benchmark of the SwiGLU-FFN backward (M=220000, K=512, N=1024, bf16) and SwishGrad.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one whole backward over the seeded synthetic workload: the b stage
+(dg, dfc, db), the w stage (dw_g, dw_fc) and the x stage (dx), issued as the
+three stage calls of the C ABI -- exactly the launches swiglu_bwd runs
+unfused -- with CUDA events between them so each kernel's time is measured
+inside the timed region. Inputs (dy, g, fc: 450 MB each) are larger than the
+129 MB L2, so no flush is needed between steps; SwishGrad (100 MB of bf16 I/O)
+is timed with an L2 flush before every launch.
+
+Prints ONE JSON line (rank 0). `value` is milliseconds per backward (lower is
+better); `pct_roofline` is the roofline time max(8MKN / tensor peak,
+(6MN + 4MK + 8KN + 4N) / HBM peak) over the measured time. `--impl reference`
+times the fp64 CPU oracle on a row sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, K, N = 220000, 512, 1024
+METRIC = "SwiGLU-bwd ms & % roofline (M220000 K512 N1024 bf16); SwishGrad GB/s"
+WORKLOAD = "swiglu_bwd M=220000 K=512 N=1024 bf16 (pages' test shape), seed 0"
+SWISH_N = 1 << 24
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def _roofline_ms(pk):
+    flop = 8.0 * M * K * N
+    byts = 6.0 * M * N + 4.0 * M * K + 8.0 * K * N + 4.0 * N  # every input read once, outputs written once
+    return max(flop / (pk["bf16"] * 1e12), byts / (pk["hbm"] * 1e9)) * 1e3
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def _dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("SWG_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- traffic from the committed ncu summary
+def _src_sha(name):
+    p = os.path.join(ROOT, "swiglu_ffn_backward_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """Per-launch DRAM bytes from profiles/dram_traffic.json, or None when the
+    kernel's source changed since those counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            t = json.load(f)[kernel]
+        if t["source_sha"] != _src_sha(t["source"]):
+            return None
+        return float(t["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+
+    import swiglu_ffn_backward_gb300 as swg
+    from synth import SWIGLU_CONFIGS, swiglu_inputs, swish_inputs
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    pk = _peaks()
+    shape = SWIGLU_CONFIGS["pages"][0]
+    if M != shape.M:
+        from synth import SwigluShape
+        shape = SwigluShape(f"pages_M{M}", M, K, N, shape.seed, shape.dist)
+    inp = swiglu_inputs(shape, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    dg = torch.empty((M, N), **bf)
+    dfc = torch.empty((M, N), **bf)
+    db_g = torch.empty((1, N), **bf)
+    db_fc = torch.empty((1, N), **bf)
+    dw_g = torch.empty((K, N), **bf)
+    dw_fc = torch.empty((K, N), **bf)
+    dx = torch.empty((M, K), **bf)
+    ws_b = torch.empty(max(swg.swiglu_bwd_b_workspace_size(M, N), 16), dtype=torch.uint8, device=dev)
+    ws_w_bytes = swg.swiglu_bwd_w_workspace_size(M, K, N)
+    ws_w = torch.empty(max(ws_w_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"], dg, dfc, db_g, db_fc, workspace=ws_b)
+        if ev is not None:
+            ev[1].record(stream)
+        swg.swiglu_bwd_w(inp["x"], dg, dfc, dw_g, dw_fc, workspace=ws_w)
+        if ev is not None:
+            ev[2].record(stream)
+        swg.swiglu_bwd_x(dg, dfc, inp["w_g"], inp["w_fc"], dx)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    swg.swg_check()
+    if args.profile_only:
+        # a plain launch sequence for ncu captures: no timing is reported
+        for _ in range(args.steps):
+            step()
+        swg.swg_check()
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "M": M, "K": K, "N": N, "steps": args.steps}), flush=True)
+        return
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(torch.cuda.current_device())
+    _barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    _barrier(world)
+    swg.swg_check()
+    total_ms = t_start.elapsed_time(t_end)
+    ms = _max_over_ranks(total_ms / args.steps, world)
+    per = {"b_stage": [], "w_gemm": [], "x_gemm": []}
+    for e in evs:
+        per["b_stage"].append(e[0].elapsed_time(e[1]))
+        per["w_gemm"].append(e[1].elapsed_time(e[2]))
+        per["x_gemm"].append(e[2].elapsed_time(e[3]))
+    avg = {k: sum(v) / len(v) for k, v in per.items()}
+
+    # algorithmic work per launch (bytes for HBM-bound, flops for tensor-bound)
+    b_bytes = 10.0 * M * N + 4.0 * N
+    gemm_flop = 4.0 * M * K * N
+    kernels = {
+        "b_stage": dict(bound="hbm", work=b_bytes, peak=pk["hbm"], unit="GB/s", src="b_stage.cu"),
+        "w_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
+        "x_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
+    }
+    dom = max(avg, key=avg.get)
+    kd = kernels[dom]
+    scale = 1e-9 if kd["unit"] == "GB/s" else 1e-12
+    achieved = kd["work"] * scale / (avg[dom] * 1e-3)
+    roof = {"kernel": dom, "bound": kd["bound"], "achieved": round(achieved, 1), "peak": kd["peak"],
+            "unit": kd["unit"], "frac": round(achieved / kd["peak"], 4), "traffic": _traffic(dom),
+            "peak_source": pk["source"] + (" burst" if kd["unit"] == "TFLOP/s" else "")}
+    stages = {}
+    for k, kd2 in kernels.items():
+        sc = 1e-9 if kd2["unit"] == "GB/s" else 1e-12
+        a = kd2["work"] * sc / (avg[k] * 1e-3)
+        stages[k] = {"ms": round(avg[k], 4), "achieved": round(a, 1), "unit": kd2["unit"],
+                     "frac": round(a / kd2["peak"], 4)}
+
+    # SwishGrad GB/s, bf16, n = 2^24, beta = 1.702, L2 flushed before each launch
+    grad, xs = swish_inputs(SWISH_N, torch.bfloat16, device=dev, seed=1)
+    gx = torch.empty_like(grad)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    sw_t = []
+    for i in range(max(3, args.warmup) + 20):
+        flush.zero_()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        swg.swish_grad(grad, xs, 1.702, grad_x=gx)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        if i >= max(3, args.warmup):
+            sw_t.append(a0.elapsed_time(a1))
+    sw_ms = statistics.median(sw_t)
+    sw_gbs = 3.0 * SWISH_N * 2 / (sw_ms * 1e-3) / 1e9
+    del flush
+
+    # e2e: host buffers in pinned memory, H2D of every input and D2H of the
+    # results inside the timed region, through the public swiglu_bwd call
+    host_in = {k: v.cpu().pin_memory() for k, v in inp.items()}
+    dev_in = {k: torch.empty_like(v) for k, v in inp.items()}
+    outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    ws_full = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 0), 16), dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        swg.swiglu_bwd(**dev_in, return_dg=False, out=outs, workspace=ws_full)
+        for k in host_out:
+            host_out[k].copy_(outs[k], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    swg.swg_check()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, sample_rows=args.cpu_rows)
+
+    launches_per_step = 3 + (1 if ws_w_bytes > 0 else 0) + 1  # b + db reduce, w (+ split reduce), x
+    roof_ms = _roofline_ms(pk)
+    line = {
+        "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded randn, bf16)",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "path": "unfused: b, w, x stage calls",
+                   "l2": "inputs larger than L2 (dy, g, fc 450 MB each); SwishGrad: L2 flushed per launch",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_roofline": round(roof_ms / ms, 4), "roofline_ms": round(roof_ms, 4),
+        "tflops": round(8.0 * M * K * N / (ms * 1e-3) / 1e12, 1),
+        "roofline": roof, "stages": stages,
+        "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
+                       "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
+        "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "call": "swiglu_bwd (unfused, dg/dfc not returned)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "peaks": pk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_baseline(inp=None, sample_rows=32768, repeats=1):
+    """Time the fp64 oracle on the first `sample_rows` rows of the workload and
+    scale to the full M (the oracle's cost is linear in M)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from synth import SWIGLU_CONFIGS, swiglu_inputs
+
+    if inp is None:
+        inp = swiglu_inputs(SWIGLU_CONFIGS["pages"][0], device="cpu")
+    ms_ = min(sample_rows, M)
+    h = {}
+    for k, v in inp.items():
+        t = v[:ms_] if k in ("x", "dy", "g", "fc") else v
+        h[k] = t.detach().float().cpu().numpy().astype(np.float64)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.swiglu_bwd(h["x"], h["w_g"], h["w_fc"], h["dy"], h["g"], h["fc"], stage_dtype="bf16")
+        times.append(time.perf_counter() - t0)
+    t = min(times)
+    full_ms = t * (M / ms_) * 1e3
+    del torch
+    return {"value": round(full_ms, 1), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {ms_} of {M} rows (K={K}, N={N}), fp64 numpy, scaled by M/{ms_}; "
+                      f"sample wall time {t:.2f} s; BLAS threads = library default"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from synth import SWIGLU_CONFIGS, swiglu_inputs
+
+    inp = swiglu_inputs(SWIGLU_CONFIGS["pages"][0], device="cpu")
+    # size each step's row sample so that warmup + steps finish in about two minutes
+    probe = cpu_baseline(inp, sample_rows=2048)
+    sec_per_row = probe["value"] * 1e-3 / M
+    budget = 120.0 / (args.steps + args.warmup + 1)
+    rows = int(min(args.ref_rows, max(256, budget / max(sec_per_row, 1e-12))))
+    for _ in range(args.warmup):
+        cpu_baseline(inp, sample_rows=rows)
+    vals = [cpu_baseline(inp, sample_rows=rows)["value"] for _ in range(args.steps)]
+    cb = cpu_baseline(inp, sample_rows=rows)
+    v = statistics.median(vals)
+    cb["value"] = v
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, bf16 inputs widened to fp64)",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
+                   "path": "fp64 CPU oracle (numpy), row sample scaled to the full M"},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=32768)
+    ap.add_argument("--ref-rows", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--m", type=int, default=None,
+                    help="rows M of a smaller case of the same kernels (profiling only; the metric is M=220000)")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run warmup + steps of the timed step without timing or the other legs (for ncu)")
+    args = ap.parse_args()
+    if args.m is not None:
+        global M
+        M = args.m
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world = _dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

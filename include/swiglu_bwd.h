@@ -29,7 +29,9 @@
  *   the workspace must be 16-byte aligned (SWG_ERR_UNSUPPORTED otherwise).
  * - Empty calls: M == 0 (or n == 0) launches no element-wise work ([P2]
  *   section 3.5, empty-tensor short circuit); outputs that are sums over the
- *   M rows (db_*, dw_*) are still written, as zeros.
+ *   M rows (db_*, dw_*) are still written, as zeros. Pointers of empty
+ *   tensors (those with an M dimension when M == 0, all of swish_grad's
+ *   when n == 0) may be NULL.
  * - Outputs are OVERWRITTEN. [P1] asks callers to zero db/dw and accumulates
  *   into them; overwriting gives the same values without the zeroing.
  * - Outputs must not overlap inputs or each other (SWG_ERR_PARAM_INVALID when

@@ -54,7 +54,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build the CUDA library first "
-            "(python -m swiglu_ffn_backward_gb300.build)")
+            "(python swiglu_ffn_backward_gb300/build.py)")
     lib = ctypes.CDLL(LIB_PATH)
     P, I64, SZ, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint
     st = ctypes.c_int

@@ -1,6 +1,8 @@
 """Build the sm_103a shared library in-tree with nvcc (no torch extension machinery).
 
-    python -m swiglu_ffn_backward_gb300.build
+    python swiglu_ffn_backward_gb300/build.py [-f] [-v]
+
+(run it as a script: importing the package loads the library this builds)
 
 Compiles every csrc/*.cu in parallel for -gencode arch=compute_103a,code=sm_103a
 and links lib/libswiglu_bwd.so (static CUDA runtime; only the driver is needed

@@ -104,14 +104,14 @@ swg_status swg_check(swg_stream_t stream) {
 // ---------------------------------------------------------------- SwishGrad
 swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x, int64_t n,
                       swg_dtype dtype, swg_stream_t stream) {
-  if (grad == nullptr || x == nullptr || grad_x == nullptr) return SWG_ERR_NULLPTR;
   if (n < 0 || (dtype != SWG_F32 && dtype != SWG_F16 && dtype != SWG_BF16)) return SWG_ERR_PARAM_INVALID;
+  if (n == 0) return SWG_OK;  // empty tensors may carry NULL data pointers
+  if (grad == nullptr || x == nullptr || grad_x == nullptr) return SWG_ERR_NULLPTR;
   const int64_t es = dtype == SWG_F32 ? 4 : 2;
   const uintptr_t mask = static_cast<uintptr_t>(es - 1);
   if ((reinterpret_cast<uintptr_t>(grad) & mask) || (reinterpret_cast<uintptr_t>(x) & mask) ||
       (reinterpret_cast<uintptr_t>(grad_x) & mask))
     return SWG_ERR_UNSUPPORTED;
-  if (n == 0) return SWG_OK;
   // grad_x may alias grad or x exactly, but must not partially overlap either
   const Range o = rng(grad_x, n * es), a = rng(grad, n * es), b = rng(x, n * es);
   if ((overlap(o, a) && o.lo != a.lo) || (overlap(o, b) && o.lo != b.lo)) return SWG_ERR_PARAM_INVALID;
@@ -131,10 +131,11 @@ size_t swiglu_bwd_b_workspace_size(int64_t M, int64_t N) {
 swg_status swiglu_bwd_b(const void* dy, const void* g, const void* fc, void* dg, void* dfc, void* db_g,
                         void* db_fc, int64_t M, int64_t N, void* workspace, size_t workspace_bytes,
                         swg_stream_t stream) {
-  if (!dy || !g || !fc || !dg || !dfc || !db_g || !db_fc) return SWG_ERR_NULLPTR;
   swg_status st = check_shape(M, 8, N);
   if (st != SWG_OK) return st;
   if (N == 0) return SWG_OK;
+  // [M,N] tensors may be NULL when M == 0 (empty); [1,N] outputs are required
+  if (!db_g || !db_fc || (M > 0 && (!dy || !g || !fc || !dg || !dfc))) return SWG_ERR_NULLPTR;
   const void* all[] = {dy, g, fc, dg, dfc, db_g, db_fc};
   for (const void* p : all)
     if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
@@ -168,10 +169,10 @@ size_t swiglu_bwd_w_workspace_size(int64_t M, int64_t K, int64_t N) {
 
 swg_status swiglu_bwd_w(const void* x, const void* dg, const void* dfc, void* dw_g, void* dw_fc, int64_t M,
                         int64_t K, int64_t N, void* workspace, size_t workspace_bytes, swg_stream_t stream) {
-  if (!x || !dg || !dfc || !dw_g || !dw_fc) return SWG_ERR_NULLPTR;
   swg_status st = check_shape(M, K, N);
   if (st != SWG_OK) return st;
   if (K == 0 || N == 0) return SWG_OK;
+  if (!dw_g || !dw_fc || (M > 0 && (!x || !dg || !dfc))) return SWG_ERR_NULLPTR;
   const void* all[] = {x, dg, dfc, dw_g, dw_fc};
   for (const void* p : all)
     if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
@@ -200,10 +201,10 @@ swg_status swiglu_bwd_w(const void* x, const void* dg, const void* dfc, void* dw
 // ---------------------------------------------------------------- x stage
 swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const void* w_fc, void* dx, int64_t M,
                         int64_t K, int64_t N, swg_stream_t stream) {
-  if (!dg || !dfc || !w_g || !w_fc || !dx) return SWG_ERR_NULLPTR;
   swg_status st = check_shape(M, K, N);
   if (st != SWG_OK) return st;
   if (M == 0 || K == 0) return SWG_OK;
+  if (!dg || !dfc || !w_g || !w_fc || !dx) return SWG_ERR_NULLPTR;
   const void* all[] = {dg, dfc, w_g, w_fc, dx};
   for (const void* p : all)
     if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
@@ -238,13 +239,15 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
                       const void* fc, void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc, void* db_g,
                       void* db_fc, int64_t M, int64_t K, int64_t N, unsigned flags, void* workspace,
                       size_t workspace_bytes, swg_stream_t stream) {
-  if (!x || !w_g || !w_fc || !dy || !g || !fc || !dx || !dw_g || !dw_fc || !db_g || !db_fc)
-    return SWG_ERR_NULLPTR;
-  if ((dg == nullptr) != (dfc == nullptr)) return SWG_ERR_NULLPTR;
   if ((flags & ~(SWG_FUSED | SWG_WS_DG_GIVEN)) != 0) return SWG_ERR_PARAM_INVALID;
   swg_status st = check_shape(M, K, N);
   if (st != SWG_OK) return st;
   if (K == 0 || N == 0) return SWG_OK;
+  // tensors with an M dimension may be NULL when M == 0 (empty)
+  if (!w_g || !w_fc || !dw_g || !dw_fc || !db_g || !db_fc) return SWG_ERR_NULLPTR;
+  if (M > 0 && (!x || !dy || !g || !fc || !dx)) return SWG_ERR_NULLPTR;
+  if (M > 0 && (dg == nullptr) != (dfc == nullptr)) return SWG_ERR_NULLPTR;
+  if (M == 0) dg = dfc = nullptr;
   const void* all[] = {x, w_g, w_fc, dy, g, fc, dx, dw_g, dw_fc, db_g, db_fc};
   for (const void* p : all)
     if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
