@@ -97,6 +97,27 @@ swg_status swiglu_bwd_b(const void* dy, const void* g, const void* fc,
                         int64_t M, int64_t N, void* workspace, size_t workspace_bytes,
                         swg_stream_t stream);
 
+/* ---- b stage without a workspace ----------------------------------------------
+ * No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory and cannot hold a workspace between calls (for example a host
+ * framework whose memory pool owns all of device memory, or a loop that cannot
+ * afford cudaMalloc's implicit synchronisation). Same inputs, outputs and
+ * results as swiglu_bwd_b; the fp32 column partials live in a 4 MiB array
+ * compiled into the library (SWG_NOALLOC_SCRATCH_BYTES), held by every GPU that
+ * loads the library until the process exits. Nothing is allocated.
+ * - Limit: the partials must fit the array, which holds for every M when
+ *   N <= 524288; larger shapes return SWG_ERR_WORKSPACE with nothing launched.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ * - Every call shares the array and it keeps the last call's contents (no
+ *   call needs it zeroed). Calls that overlap on the GPU, e.g. on two streams
+ *   at once, race on it and give wrong db; serialise them. */
+#define SWG_NOALLOC_SCRATCH_BYTES (4u << 20)
+swg_status swiglu_bwd_b_noalloc(const void* dy, const void* g, const void* fc,
+                                void* dg, void* dfc, void* db_g, void* db_fc,
+                                int64_t M, int64_t N, swg_stream_t stream);
+
 /* ---- w stage -----------------------------------------------------------------
  * [P1] item 3; fused_swiglu_bwd_w_kernel(x, dg, dfc, dw_g, dw_fc):
  *   dw_g = x^T dg;  dw_fc = x^T dfc      (x [M,K]; dg, dfc [M,N]; dw_* [K,N])

@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     swg_check,
     swiglu_bwd,
     swiglu_bwd_b,
+    swiglu_bwd_b_noalloc,
     swiglu_bwd_b_workspace_size,
     swiglu_bwd_w,
     swiglu_bwd_w_workspace_size,

@@ -41,6 +41,7 @@ EXPORTS = (
     "swiglu_bwd_x",
     "swiglu_bwd_workspace_size", "swiglu_bwd",
     "swish_grad",
+    "swiglu_bwd_b_noalloc",
 )
 
 
@@ -78,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_bwd.restype = st
     lib.swish_grad.argtypes = [P, P, ctypes.POINTER(ctypes.c_float), P, I64, ctypes.c_int, P]
     lib.swish_grad.restype = st
+    lib.swiglu_bwd_b_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, P]
+    lib.swiglu_bwd_b_noalloc.restype = st
     return lib
 
 
@@ -233,3 +236,21 @@ def swish_grad(grad, x, scale=None, grad_x=None, stream=None):
     _check(lib.swish_grad(grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
                           _DTYPE[grad.dtype], _stream(stream)), "swish_grad")
     return grad_x
+
+
+def swiglu_bwd_b_noalloc(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, stream=None):
+    """b stage without a workspace: the column partials use a fixed array
+    inside the library, so the call itself allocates nothing on the device
+    (outputs not passed in are still created here with torch.empty). Calls
+    must not overlap on the GPU; see include/swiglu_bwd.h."""
+    dy, g, fc = (_dev_bf16(t, n) for t, n in ((dy, "dy"), (g, "g"), (fc, "fc")))
+    M, N = dy.shape
+    if g.shape != dy.shape or fc.shape != dy.shape:
+        raise ValueError("dy, g, fc must have the same [M, N] shape")
+    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
+    db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
+    _check(lib.swiglu_bwd_b_noalloc(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),
+                                    db_g.data_ptr(), db_fc.data_ptr(), M, N, _stream(stream)),
+           "swiglu_bwd_b_noalloc")
+    return dg, dfc, db_g, db_fc
