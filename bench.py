@@ -174,78 +174,103 @@ def run_ours(args, rank, world):
     ws_b = torch.empty(max(swg.swiglu_bwd_b_workspace_size(M, N), 16), dtype=torch.uint8, device=dev)
     ws_w_bytes = swg.swiglu_bwd_w_workspace_size(M, K, N)
     ws_w = torch.empty(max(ws_w_bytes, 16), dtype=torch.uint8, device=dev)
+    ws_fw_bytes = swg.swiglu_bwd_w_fused_workspace_size(M, K, N)
+    ws_fw = torch.empty(max(ws_fw_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"], dg, dfc, db_g, db_fc, workspace=ws_b)
-        if ev is not None:
-            ev[1].record(stream)
-        swg.swiglu_bwd_w(inp["x"], dg, dfc, dw_g, dw_fc, workspace=ws_w)
-        if ev is not None:
-            ev[2].record(stream)
-        swg.swiglu_bwd_x(dg, dfc, inp["w_g"], inp["w_fc"], dx)
-        if ev is not None:
-            ev[3].record(stream)
+    # each path: a list of (kernel name, launch) issued in order; CUDA events
+    # go between them so every kernel is timed inside the timed region
+    unfused = [
+        ("b_stage", lambda: swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"], dg, dfc, db_g, db_fc, workspace=ws_b)),
+        ("w_gemm", lambda: swg.swiglu_bwd_w(inp["x"], dg, dfc, dw_g, dw_fc, workspace=ws_w)),
+        ("x_gemm", lambda: swg.swiglu_bwd_x(dg, dfc, inp["w_g"], inp["w_fc"], dx)),
+    ]
+    fused = [
+        ("x_fused", lambda: swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"], dx)),
+        ("w_fused", lambda: swg.swiglu_bwd_w_fused(inp["x"], inp["dy"], inp["g"], inp["fc"], dw_g, dw_fc,
+                                                   db_g, db_fc, workspace=ws_fw)),
+    ]
+    paths = {"unfused": unfused, "fused": fused}
+    launches = {"unfused": 3 + 1 + (1 if ws_w_bytes > 0 else 0),
+                "fused": 3 + (1 if ws_fw_bytes > (2 * N * 4 + 255) // 256 * 256 else 0)}
 
-    for _ in range(args.warmup):
-        step()
+    def step(seq, ev=None):
+        for j, (_, fn) in enumerate(seq):
+            if ev is not None:
+                ev[j].record(stream)
+            fn()
+        if ev is not None:
+            ev[len(seq)].record(stream)
+
+    main_path = paths[args.path]
+    for seq in paths.values():
+        for _ in range(args.warmup):
+            step(seq)
     swg.swg_check()
     if args.profile_only:
         # a plain launch sequence for ncu captures: no timing is reported
         for _ in range(args.steps):
-            step()
+            step(main_path)
         swg.swg_check()
         if rank == 0:
-            print(json.dumps({"profile_only": True, "M": M, "K": K, "N": N, "steps": args.steps}), flush=True)
+            print(json.dumps({"profile_only": True, "path": args.path, "M": M, "K": K, "N": N,
+                              "steps": args.steps}), flush=True)
         return
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    clocks = Clocks(torch.cuda.current_device())
-    _barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    _barrier(world)
-    swg.swg_check()
-    total_ms = t_start.elapsed_time(t_end)
-    ms = _max_over_ranks(total_ms / args.steps, world)
-    per = {"b_stage": [], "w_gemm": [], "x_gemm": []}
-    for e in evs:
-        per["b_stage"].append(e[0].elapsed_time(e[1]))
-        per["w_gemm"].append(e[1].elapsed_time(e[2]))
-        per["x_gemm"].append(e[2].elapsed_time(e[3]))
-    avg = {k: sum(v) / len(v) for k, v in per.items()}
+
+    def timed(seq, steps, with_clocks):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)] for _ in range(steps)]
+        clocks = Clocks(torch.cuda.current_device()) if with_clocks else None
+        _barrier(world)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.start()
+            time.sleep(0.3)  # let the sampler start before the timed region
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            step(seq, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop() if clocks else None
+        _barrier(world)
+        swg.swg_check()
+        ms_ = _max_over_ranks(t0.elapsed_time(t1) / steps, world)
+        per = {}
+        for j, (name, _) in enumerate(seq):
+            per[name] = sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps
+        return ms_, per, clk
 
     # algorithmic work per launch (bytes for HBM-bound, flops for tensor-bound)
-    b_bytes = 10.0 * M * N + 4.0 * N
     gemm_flop = 4.0 * M * K * N
     kernels = {
-        "b_stage": dict(bound="hbm", work=b_bytes, peak=pk["hbm"], unit="GB/s", src="b_stage.cu"),
+        "b_stage": dict(bound="hbm", work=10.0 * M * N + 4.0 * N, peak=pk["hbm"], unit="GB/s", src="b_stage.cu"),
         "w_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
         "x_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
+        "x_fused": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="fused_tc.cu"),
+        "w_fused": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="fused_tc.cu"),
     }
-    dom = max(avg, key=avg.get)
+
+    def describe(per):
+        out = {}
+        for k, t in per.items():
+            kd = kernels[k]
+            sc = 1e-9 if kd["unit"] == "GB/s" else 1e-12
+            a = kd["work"] * sc / (t * 1e-3)
+            out[k] = {"ms": round(t, 4), "achieved": round(a, 1), "unit": kd["unit"], "frac": round(a / kd["peak"], 4)}
+        return out
+
+    ms, per_main, clk = timed(main_path, args.steps, True)
+    other = "unfused" if args.path == "fused" else "fused"
+    ms_other, per_other, _ = timed(paths[other], max(args.steps // 4, 10), False)
+    dom = max(per_main, key=per_main.get)
     kd = kernels[dom]
     scale = 1e-9 if kd["unit"] == "GB/s" else 1e-12
-    achieved = kd["work"] * scale / (avg[dom] * 1e-3)
+    achieved = kd["work"] * scale / (per_main[dom] * 1e-3)
     roof = {"kernel": dom, "bound": kd["bound"], "achieved": round(achieved, 1), "peak": kd["peak"],
             "unit": kd["unit"], "frac": round(achieved / kd["peak"], 4), "traffic": _traffic(dom),
             "peak_source": pk["source"] + (" burst" if kd["unit"] == "TFLOP/s" else "")}
-    stages = {}
-    for k, kd2 in kernels.items():
-        sc = 1e-9 if kd2["unit"] == "GB/s" else 1e-12
-        a = kd2["work"] * sc / (avg[k] * 1e-3)
-        stages[k] = {"ms": round(avg[k], 4), "achieved": round(a, 1), "unit": kd2["unit"],
-                     "frac": round(a / kd2["peak"], 4)}
+    stages = describe(per_main)
 
     # SwishGrad GB/s, bf16, n = 2^24, beta = 1.702, L2 flushed before each launch
     grad, xs = swish_inputs(SWISH_N, torch.bfloat16, device=dev, seed=1)
@@ -272,14 +297,16 @@ def run_ours(args, rank, world):
     dev_in = {k: torch.empty_like(v) for k, v in inp.items()}
     outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
-    ws_full = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 0), 16), dtype=torch.uint8, device=dev)
+    use_fused = args.path == "fused"
+    ws_full = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 1 if use_fused else 0), 16),
+                          dtype=torch.uint8, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def e2e_step():
         for k in dev_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        swg.swiglu_bwd(**dev_in, return_dg=False, out=outs, workspace=ws_full)
+        swg.swiglu_bwd(**dev_in, fused=use_fused, return_dg=False, out=outs, workspace=ws_full)
         for k in host_out:
             host_out[k].copy_(outs[k], non_blocking=True)
 
@@ -302,23 +329,25 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, sample_rows=args.cpu_rows)
 
-    launches_per_step = 3 + (1 if ws_w_bytes > 0 else 0) + 1  # b + db reduce, w (+ split reduce), x
     roof_ms = _roofline_ms(pk)
     line = {
         "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded randn, bf16)",
-        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "path": "unfused: b, w, x stage calls",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
+                   "path": (args.path + ": " + ", ".join(n for n, _ in main_path) + " stage calls"),
                    "l2": "inputs larger than L2 (dy, g, fc 450 MB each); SwishGrad: L2 flushed per launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_roofline": round(roof_ms / ms, 4), "roofline_ms": round(roof_ms, 4),
         "tflops": round(8.0 * M * K * N / (ms * 1e-3) / 1e12, 1),
         "roofline": roof, "stages": stages,
+        "other_path": {"path": other, "ms": round(ms_other, 4), "pct_roofline": round(roof_ms / ms_other, 4),
+                       "stages": describe(per_other)},
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
                        "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "call": "swiglu_bwd (unfused, dg/dfc not returned)"},
-        "gpu_launches": launches_per_step * args.steps,
+                "steps": e2e_steps, "call": f"swiglu_bwd ({args.path}, dg/dfc not returned)"},
+        "gpu_launches": launches[args.path] * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "peaks": pk,
@@ -392,6 +421,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+                    help="which chain the timed step runs (the other is timed too and reported beside it)")
     ap.add_argument("--cpu-rows", type=int, default=32768)
     ap.add_argument("--ref-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -138,13 +138,37 @@ swg_status swiglu_bwd_w(const void* x, const void* dg, const void* dfc,
 swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const void* w_fc,
                         void* dx, int64_t M, int64_t K, int64_t N, swg_stream_t stream);
 
+/* ---- fused stages -------------------------------------------------------------
+ * The b-stage math of [P1] item 1 runs inside the GEMMs' operand producer:
+ * dg, dfc are computed from dy, g, fc tile by tile in shared memory, rounded to
+ * bf16 exactly as the b stage stores them, and fed to the tensor cores; they
+ * are never written to or read back from HBM (the recompute-instead-of-store
+ * principle).
+ *
+ * swiglu_bwd_x_fused: dx = dg W_g^T + dfc W_fc^T ([P1] item 4) from dy, g, fc
+ *   [M,N] and w_g, w_fc [K,N]. dg, dfc [M,N] are optional outputs (NULL to
+ *   skip; both or neither). No workspace.
+ * swiglu_bwd_w_fused: dw_g = x^T dg, dw_fc = x^T dfc ([P1] item 3) and the
+ *   column sums db_g, db_fc ([P1] item 2) from x [M,K] and dy, g, fc.
+ *   Workspace: split-M fp32 partials of dw and db,
+ *   swiglu_bwd_w_fused_workspace_size(M, K, N) bytes.
+ * Same shape, alignment, overlap and error rules as the unfused stages. */
+swg_status swiglu_bwd_x_fused(const void* dy, const void* g, const void* fc,
+                              const void* w_g, const void* w_fc, void* dx, void* dg, void* dfc,
+                              int64_t M, int64_t K, int64_t N, swg_stream_t stream);
+size_t swiglu_bwd_w_fused_workspace_size(int64_t M, int64_t K, int64_t N);
+swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, const void* fc,
+                              void* dw_g, void* dw_fc, void* db_g, void* db_fc,
+                              int64_t M, int64_t K, int64_t N,
+                              void* workspace, size_t workspace_bytes, swg_stream_t stream);
+
 /* ---- whole backward ----------------------------------------------------------
  * [P1] "Kernel overview and call chain": b, then w and x on b's dg, dfc.
  * dg, dfc are optional outputs: pass NULL to skip them. With SWG_UNFUSED and
  * NULL dg/dfc, the workspace holds them (4*M*N bytes more). With SWG_FUSED the
- * w and x GEMMs compute dg, dfc tile by tile in shared memory from dy, g, fc
- * (the recompute-instead-of-store principle); their operands are the bf16
- * roundings of the fp32 dg, dfc, exactly as in the unfused chain.
+ * call runs swiglu_bwd_x_fused then swiglu_bwd_w_fused: the w and x GEMMs
+ * compute dg, dfc tile by tile in shared memory from dy, g, fc; their operands
+ * are the bf16 roundings of the fp32 dg, dfc, exactly as in the unfused chain.
  * Workspace: swiglu_bwd_workspace_size(M, K, N, flags) bytes; with non-NULL
  * dg/dfc the smaller figure swiglu_bwd_workspace_size(M, K, N, flags |
  * SWG_WS_DG_GIVEN) suffices. */

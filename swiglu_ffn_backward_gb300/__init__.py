@@ -19,6 +19,9 @@ from ._binding import (  # noqa: F401
     swiglu_bwd_w,
     swiglu_bwd_w_workspace_size,
     swiglu_bwd_workspace_size,
+    swiglu_bwd_w_fused,
+    swiglu_bwd_w_fused_workspace_size,
     swiglu_bwd_x,
+    swiglu_bwd_x_fused,
     swish_grad,
 )

@@ -42,6 +42,8 @@ EXPORTS = (
     "swiglu_bwd_workspace_size", "swiglu_bwd",
     "swish_grad",
     "swiglu_bwd_b_noalloc",
+    "swiglu_bwd_x_fused",
+    "swiglu_bwd_w_fused_workspace_size", "swiglu_bwd_w_fused",
 )
 
 
@@ -81,6 +83,12 @@ def _load() -> ctypes.CDLL:
     lib.swish_grad.restype = st
     lib.swiglu_bwd_b_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, P]
     lib.swiglu_bwd_b_noalloc.restype = st
+    lib.swiglu_bwd_x_fused.argtypes = [P] * 8 + [I64, I64, I64, P]
+    lib.swiglu_bwd_x_fused.restype = st
+    lib.swiglu_bwd_w_fused_workspace_size.argtypes = [I64, I64, I64]
+    lib.swiglu_bwd_w_fused_workspace_size.restype = SZ
+    lib.swiglu_bwd_w_fused.argtypes = [P] * 8 + [I64, I64, I64, P, SZ, P]
+    lib.swiglu_bwd_w_fused.restype = st
     return lib
 
 
@@ -127,6 +135,47 @@ def _nbytes(t):
 
 
 # ---------------------------------------------------------------- public API
+def swiglu_bwd_w_fused_workspace_size(M: int, K: int, N: int) -> int:
+    return lib.swiglu_bwd_w_fused_workspace_size(M, K, N)
+
+
+def swiglu_bwd_x_fused(dy, g, fc, w_g, w_fc, dx=None, dg=None, dfc=None, return_dg=False, stream=None):
+    """Fused x stage: dx from dy, g, fc and the weights (dg, dfc formed on chip;
+    written out too when return_dg or when passed in). Returns (dx, dg, dfc)."""
+    dy, g, fc, w_g, w_fc = (_dev_bf16(t, n) for t, n in (
+        (dy, "dy"), (g, "g"), (fc, "fc"), (w_g, "w_g"), (w_fc, "w_fc")))
+    M, N = dy.shape
+    K = w_g.shape[0]
+    if g.shape != dy.shape or fc.shape != dy.shape or w_g.shape != (K, N) or w_fc.shape != (K, N):
+        raise ValueError("shape mismatch: dy, g, fc [M, N]; w_g, w_fc [K, N]")
+    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    dx = mk(dx, (M, K))
+    if return_dg:
+        dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
+    _check(lib.swiglu_bwd_x_fused(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(),
+                                  dx.data_ptr(), _ptr(dg), _ptr(dfc), M, K, N, _stream(stream)),
+           "swiglu_bwd_x_fused")
+    return dx, dg, dfc
+
+
+def swiglu_bwd_w_fused(x, dy, g, fc, dw_g=None, dw_fc=None, db_g=None, db_fc=None, workspace=None, stream=None):
+    """Fused w stage: dw_g, dw_fc and db_g, db_fc from x and dy, g, fc (dg, dfc
+    formed on chip). Returns (dw_g, dw_fc, db_g, db_fc)."""
+    x, dy, g, fc = (_dev_bf16(t, n) for t, n in ((x, "x"), (dy, "dy"), (g, "g"), (fc, "fc")))
+    M, K = x.shape
+    N = dy.shape[1]
+    if dy.shape != (M, N) or g.shape != (M, N) or fc.shape != (M, N):
+        raise ValueError("dy, g, fc must be [M, N] with M = x.shape[0]")
+    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=x.device) if t is None else t  # noqa: E731
+    dw_g, dw_fc = mk(dw_g, (K, N)), mk(dw_fc, (K, N))
+    db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
+    ws = _workspace(lib.swiglu_bwd_w_fused_workspace_size(M, K, N), x.device, workspace)
+    _check(lib.swiglu_bwd_w_fused(x.data_ptr(), dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dw_g.data_ptr(),
+                                  dw_fc.data_ptr(), db_g.data_ptr(), db_fc.data_ptr(), M, K, N, _ptr(ws),
+                                  _nbytes(ws), _stream(stream)), "swiglu_bwd_w_fused")
+    return dw_g, dw_fc, db_g, db_fc
+
+
 def swg_check(stream=None) -> None:
     """Synchronise the stream and raise if a kernel reported a barrier timeout."""
     _check(lib.swg_check(_stream(stream)), "swg_check")

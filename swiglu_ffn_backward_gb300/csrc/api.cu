@@ -220,6 +220,70 @@ swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const 
                                         static_cast<uint16_t*>(dx), M, K, N, s));
 }
 
+// ---------------------------------------------------------------- fused stages
+swg_status swiglu_bwd_x_fused(const void* dy, const void* g, const void* fc, const void* w_g, const void* w_fc,
+                              void* dx, void* dg, void* dfc, int64_t M, int64_t K, int64_t N, swg_stream_t stream) {
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (M == 0 || K == 0) return SWG_OK;
+  if (!dy || !g || !fc || !w_g || !w_fc || !dx) return SWG_ERR_NULLPTR;
+  if ((dg == nullptr) != (dfc == nullptr)) return SWG_ERR_NULLPTR;
+  const void* all[] = {dy, g, fc, w_g, w_fc, dx, dg, dfc};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const int64_t mn = M * N * 2, kn = K * N * 2;
+  const Range outs[] = {rng(dx, M * K * 2), rng(dg, dg ? mn : 0), rng(dfc, dfc ? mn : 0)};
+  const Range ins[] = {rng(dy, mn), rng(g, mn), rng(fc, mn), rng(w_g, kn), rng(w_fc, kn)};
+  if (any_overlap(outs, 3, ins, 5)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (N == 0) return cuda_status(cudaMemsetAsync(dx, 0, static_cast<size_t>(M * K * 2), s));
+  return cuda_status(swg::launch_fused_x(
+      static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+      static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc), static_cast<uint16_t*>(dx),
+      static_cast<uint16_t*>(dg), static_cast<uint16_t*>(dfc), M, K, N, s));
+}
+
+size_t swiglu_bwd_w_fused_workspace_size(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  return swg::fw_plan(M, K, N, swg::device_sm_count()).ws_bytes;
+}
+
+swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, const void* fc, void* dw_g,
+                              void* dw_fc, void* db_g, void* db_fc, int64_t M, int64_t K, int64_t N, void* workspace,
+                              size_t workspace_bytes, swg_stream_t stream) {
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (K == 0 || N == 0) return SWG_OK;
+  if (!dw_g || !dw_fc || !db_g || !db_fc || (M > 0 && (!x || !dy || !g || !fc))) return SWG_ERR_NULLPTR;
+  const void* all[] = {x, dy, g, fc, dw_g, dw_fc, db_g, db_fc};
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const int64_t mn = M * N * 2, kn = K * N * 2;
+  const Range outs[] = {rng(dw_g, kn), rng(dw_fc, kn), rng(db_g, N * 2), rng(db_fc, N * 2)};
+  const Range ins[] = {rng(x, M * K * 2), rng(dy, mn), rng(g, mn), rng(fc, mn)};
+  if (any_overlap(outs, 4, ins, 4)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    st = zero_bf16(dw_g, K * N, s);
+    if (st == SWG_OK) st = zero_bf16(dw_fc, K * N, s);
+    if (st == SWG_OK) st = zero_bf16(db_g, N, s);
+    return st != SWG_OK ? st : zero_bf16(db_fc, N, s);
+  }
+  const swg::FwPlan plan = swg::fw_plan(M, K, N, swg::device_sm_count());
+  if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return SWG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SWG_ERR_UNSUPPORTED;
+  const Range w = rng(workspace, static_cast<int64_t>(plan.ws_bytes));
+  if (any_overlap(&w, 1, outs, 4) || any_overlap(&w, 1, ins, 4)) return SWG_ERR_PARAM_INVALID;
+  return cuda_status(swg::launch_fused_w(
+      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g),
+      static_cast<const uint16_t*>(fc), static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
+      static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, workspace, plan, s));
+}
+
 // ---------------------------------------------------------------- whole backward
 // Unfused workspace layout: [dg scratch 2MN | dfc scratch 2MN] (only when the
 // caller passes NULL dg/dfc) | b-stage partials | w-stage partials; each
@@ -227,7 +291,7 @@ swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const 
 size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags) {
   if (M <= 0 || K <= 0 || N <= 0) return 0;
   const bool fused = (flags & SWG_FUSED) != 0;
-  if (fused) return 0;  // fused path not available in this build (see swiglu_bwd)
+  if (fused) return swg::fw_plan(M, K, N, swg::device_sm_count()).ws_bytes;
   size_t total = 0;
   if (!(flags & SWG_WS_DG_GIVEN)) total += 2 * align256(static_cast<size_t>(M) * N * 2);
   total += align256(swg::b_workspace_bytes(M, N));
@@ -259,7 +323,6 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
   if (any_overlap(outs, 7, ins, 6)) return SWG_ERR_PARAM_INVALID;
   st = check_device();
   if (st != SWG_OK) return st;
-  if (flags & SWG_FUSED) return SWG_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M == 0) {
     st = zero_bf16(dw_g, K * N, s);
@@ -276,6 +339,19 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
   if (any_overlap(&w, 1, outs, 7) || any_overlap(&w, 1, ins, 6)) return SWG_ERR_PARAM_INVALID;
 
   uint8_t* wp = static_cast<uint8_t*>(workspace);
+  if (flags & SWG_FUSED) {
+    const swg::FwPlan fplan = swg::fw_plan(M, K, N, swg::device_sm_count());
+    cudaError_t e = swg::launch_fused_x(
+        static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+        static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc), static_cast<uint16_t*>(dx),
+        static_cast<uint16_t*>(dg), static_cast<uint16_t*>(dfc), M, K, N, s);
+    if (e != cudaSuccess) return SWG_ERR_CUDA;
+    e = swg::launch_fused_w(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
+                            static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+                            static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
+                            static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, wp, fplan, s);
+    return cuda_status(e);
+  }
   uint16_t* dgp = static_cast<uint16_t*>(dg);
   uint16_t* dfcp = static_cast<uint16_t*>(dfc);
   if (dgp == nullptr) {

@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) flag_timeout(s);
     tc_fence_after();
     const int r = q * 32 + lane;  // accumulator row
-    if (ok && !s.abort_flag && nkb > 0) {
+    // tcgen05.ld is warp-collective: decide for the whole warp
+    if (__all_sync(0xffffffffu, ok && !s.abort_flag && nkb > 0)) {
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
@@ -320,8 +321,12 @@ cudaError_t prepare_kernel() {
 
 }  // namespace
 
+static CUtensorMapSwizzle swizzle_mode(int bytes) {
+  return bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+}
+
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
-                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
   EncodeFn enc = get_encode();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -329,7 +334,20 @@ bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_mode(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+                         const uint32_t box[3], int swizzle_bytes) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t b[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), d, st, b, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_mode(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -403,13 +421,32 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
   tc_gemm_kernel<kModeW><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(a0, a0, b0, b1, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.splits == 1) return e;
+  return launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream);
+}
+
+cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
+                                  uint16_t* dw_fc, cudaStream_t stream) {
   const int64_t per_prob4 = K * N / 4;
   int64_t blocks = (2 * per_prob4 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   w_split_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const float4*>(ws), static_cast<int>(plan.splits), per_prob4, reinterpret_cast<uint2*>(dw_g),
+      reinterpret_cast<const float4*>(ws), static_cast<int>(splits), per_prob4, reinterpret_cast<uint2*>(dw_g),
       reinterpret_cast<uint2*>(dw_fc));
   return cudaGetLastError();
+}
+
+uint32_t* status_word_ptr() {
+  static std::mutex mu;
+  static uint32_t* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
 }
 
 cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream) {

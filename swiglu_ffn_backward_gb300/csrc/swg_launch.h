@@ -26,6 +26,9 @@ cudaError_t launch_b_stage(const uint16_t* dy, const uint16_t* g, const uint16_t
 // db from fp32 partials [chunks][2N] -> bf16 db_g, db_fc (fixed order)
 cudaError_t launch_db_reduce(const float* partials, int64_t chunks, int64_t N, uint16_t* db_g, uint16_t* db_fc,
                              cudaStream_t stream);
+// 3-D tensor-map encoding (dims/strides innermost first; strides[i] is the byte stride of dim i+1)
+bool encode_tmap_3d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+                         const uint32_t box[3], int swizzle_bytes);
 
 // ---- tcgen05 GEMMs
 struct WPlan {
@@ -44,9 +47,29 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
 
 // module status word (timeouts)
 cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream);
+// device address of the status word on the current device (for kernels in other files)
+uint32_t* status_word_ptr();
+
+// ---- fused variant: b-stage math in the GEMM operand producer
+struct FwPlan {
+  int64_t splits, kb_per;
+  size_t ws_bytes;
+};
+// ws_bytes = split-M dw partials (when splits > 1) + db partials [splits][2N], 256-B aligned parts
+FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms);
+// dx (and optionally dg, dfc) from dy, g, fc, W
+cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, const uint16_t* w_g,
+                           const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
+                           int64_t N, cudaStream_t stream);
+// dw and db from x, dy, g, fc; ws holds the split-M dw partials, then the db partials
+cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                           uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
+                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream);
+cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
+                                  uint16_t* dw_fc, cudaStream_t stream);
 
 // tensor-map encoding (driver entry point resolved once)
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                         uint32_t box_inner, uint32_t box_outer);
+                         uint32_t box_inner, uint32_t box_outer, int swizzle_bytes = 128);
 
 }  // namespace swg

@@ -102,17 +102,22 @@ def _shapes(names):
     return [s for n in names for s in SWIGLU_CONFIGS[n]]
 
 
+FUSED = pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused"])
+
+
+@FUSED
 @pytest.mark.parametrize("shape", _shapes(["tiny", "tail"]), ids=lambda s: s.name)
-def test_swiglu_bwd_unfused(shape):
+def test_swiglu_bwd(shape, fused):
     if shape.M * shape.N <= FULL_ORACLE_MAX_MN:
-        assert_all(_full_case(shape, fused=False))
+        assert_all(_full_case(shape, fused=fused))
     else:
-        assert_all(_sampled_case(shape, fused=False))
+        assert_all(_sampled_case(shape, fused=fused))
 
 
+@FUSED
 @pytest.mark.parametrize("shape", _shapes(["pages", "llm"]), ids=lambda s: s.name)
-def test_swiglu_bwd_unfused_full_size(shape):
-    assert_all(_sampled_case(shape, fused=False))
+def test_swiglu_bwd_full_size(shape, fused):
+    assert_all(_sampled_case(shape, fused=fused))
 
 
 ODD = [SwigluShape("odd_M300_K72_N200", 300, 72, 200, 4, "tail"),
@@ -120,9 +125,11 @@ ODD = [SwigluShape("odd_M300_K72_N200", 300, 72, 200, 4, "tail"),
        SwigluShape("odd_M2_K520_N264", 2, 520, 264, 6, "tail")]
 
 
-@pytest.mark.parametrize("shape", ODD, ids=lambda s: s.name)
-def test_swiglu_bwd_odd_shapes(shape):
-    assert_all(_full_case(shape, fused=False))
+@FUSED
+@pytest.mark.parametrize("shape", ODD + [SwigluShape("odd_M200_K1032_N136", 200, 1032, 136, 7, "tail")],
+                         ids=lambda s: s.name)
+def test_swiglu_bwd_odd_shapes(shape, fused):
+    assert_all(_full_case(shape, fused=fused))
 
 
 @pytest.mark.parametrize("shape", _shapes(["tiny"]) + [SWIGLU_CONFIGS["tail"][2], ODD[0]], ids=lambda s: s.name)
@@ -144,16 +151,53 @@ def test_stage_calls(shape):
                 compare("dx", dx, rdx)])
 
 
+@pytest.mark.parametrize("shape", _shapes(["tiny"]) + [SWIGLU_CONFIGS["tail"][2], ODD[0]], ids=lambda s: s.name)
+def test_fused_stage_calls(shape):
+    """The fused x and w stages called separately; dw, dx against the oracle's
+    stages fed the b stage's bf16 dg, dfc, which the fused kernels reproduce."""
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    dx, dg, dfc = swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"], return_dg=True)
+    dx2, _, _ = swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"])
+    dw_g, dw_fc, db_g, db_fc = swg.swiglu_bwd_w_fused(inp["x"], inp["dy"], inp["g"], inp["fc"])
+    swg.swg_check()
+    h = _np(inp)
+    rdg, rdfc, rdbg, rdbfc = oracle.swiglu_bwd_b(h["dy"], h["g"], h["fc"])
+    gdg, gdfc = to_f64(dg), to_f64(dfc)
+    rdwg, rdwfc = oracle.swiglu_bwd_w(h["x"], gdg, gdfc)
+    rdx = oracle.swiglu_bwd_x(gdg, gdfc, h["w_g"], h["w_fc"])
+    assert_all([compare("dg", dg, rdg), compare("dfc", dfc, rdfc), compare("db_g", db_g, rdbg),
+                compare("db_fc", db_fc, rdbfc), compare("dw_g", dw_g, rdwg), compare("dw_fc", dw_fc, rdwfc),
+                compare("dx", dx, rdx)])
+    # without the optional dg, dfc outputs dx is the same bits
+    assert torch.equal(dx, dx2)
+
+
+@pytest.mark.parametrize("shape", [SWIGLU_CONFIGS["tail"][3], ODD[0]], ids=lambda s: s.name)
+def test_fused_operands_match_b_stage_bits(shape):
+    """dg, dfc formed on chip by the fused kernel are bit-identical to the b stage's."""
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    dg, dfc, _, _ = swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"])
+    _, fdg, fdfc = swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"],
+                                          return_dg=True)
+    swg.swg_check()
+    assert torch.equal(dg, fdg) and torch.equal(dfc, fdfc)
+
+
 def test_empty_M_writes_zero_sums():
     swg = _swg()
     K, N = 64, 128
     z = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
     out = dict(dx=z(0, K), dw_g=z(K, N).fill_(7), dw_fc=z(K, N).fill_(7), db_g=z(1, N).fill_(7),
                db_fc=z(1, N).fill_(7), dg=z(0, N), dfc=z(0, N))
-    swg.swiglu_bwd(z(0, K), z(K, N), z(K, N), z(0, N), z(0, N), z(0, N), out=out)
-    torch.cuda.synchronize()
-    for k in ("dw_g", "dw_fc", "db_g", "db_fc"):
-        assert torch.count_nonzero(out[k]) == 0, k
+    for fused in (False, True):
+        for k in ("dw_g", "dw_fc", "db_g", "db_fc"):
+            out[k].fill_(7)
+        swg.swiglu_bwd(z(0, K), z(K, N), z(K, N), z(0, N), z(0, N), z(0, N), out=out, fused=fused)
+        torch.cuda.synchronize()
+        for k in ("dw_g", "dw_fc", "db_g", "db_fc"):
+            assert torch.count_nonzero(out[k]) == 0, (k, fused)
 
 
 def test_db_equals_sum_of_dg_and_linearity():
@@ -175,11 +219,12 @@ def test_db_equals_sum_of_dg_and_linearity():
     assert np.all(np.abs(s - db) <= slack)
 
 
-def test_deterministic():
+@FUSED
+def test_deterministic(fused):
     swg = _swg()
     inp = swiglu_inputs(SWIGLU_CONFIGS["tail"][3], device="cuda")
-    a = swg.swiglu_bwd(**inp)
-    b = swg.swiglu_bwd(**inp)
+    a = swg.swiglu_bwd(**inp, fused=fused)
+    b = swg.swiglu_bwd(**inp, fused=fused)
     torch.cuda.synchronize()
     for k in a:
         assert torch.equal(a[k], b[k]), k
