@@ -36,15 +36,14 @@ __device__ __forceinline__ void grad8(const uint4& dy, const uint4& g, const uin
   uint32_t og[4], of[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float g0, f0, g1, f1;
-    swiglu_grad_elem(bf16lo(dyw[i]), bf16lo(gw[i]), bf16lo(fw[i]), g0, f0);
-    swiglu_grad_elem(bf16hi(dyw[i]), bf16hi(gw[i]), bf16hi(fw[i]), g1, f1);
-    ag[2 * i] += g0;
-    ag[2 * i + 1] += g1;
-    af[2 * i] += f0;
-    af[2 * i + 1] += f1;
-    og[i] = pack_bf16x2(g0, g1);
-    of[i] = pack_bf16x2(f0, f1);
+    float2 pg, pf;
+    swiglu_grad_pair(bf16x2_to_f2(dyw[i]), bf16x2_to_f2(gw[i]), bf16x2_to_f2(fw[i]), pg, pf);
+    ag[2 * i] += pg.x;
+    ag[2 * i + 1] += pg.y;
+    af[2 * i] += pf.x;
+    af[2 * i + 1] += pf.y;
+    og[i] = pack_bf16x2(pg.x, pg.y);
+    of[i] = pack_bf16x2(pf.x, pf.y);
   }
   dg = make_uint4(og[0], og[1], og[2], og[3]);
   dfc = make_uint4(of[0], of[1], of[2], of[3]);

@@ -7,27 +7,27 @@
 // recompute-instead-of-store principle stated in the Ascend C backward blog
 // post (Swish section: recompute sigma in the backward rather than keep it).
 //
-// Two kernels, both one CTA per SM with eleven warps:
-//   warp 0 lane 0   TMA producer of the raw ring (dy, g, fc tiles)
-//   warp 10 lane 0  TMA producer of the operand ring (W chunks, or x chunks)
+// Two kernels, both one CTA per SM with ten warps:
+//   warp 0 lane 0   TMA producer of the operand ring (W chunks, or x chunks)
 //   warp 1          TMEM allocation (512 columns); lane 0 issues tcgen05.mma
-//   warps 2-9       transform: read dy, g, fc from shared memory, compute dg,
-//                   dfc in fp32, write them as bf16 IN PLACE over g and fc
-//                   (the TMA swizzle permutes 16-byte chunks within each row
-//                   the same way for all three tiles, so an element-wise map
-//                   needs no layout work); then the epilogue, two warps per
+//   warps 2-9       transform: load dy, g, fc straight from global memory into
+//                   registers (16-byte coalesced loads, one stage ahead of the
+//                   math, with an L2 prefetch of the tile a few stages further
+//                   ahead), compute dg, dfc in fp32 and store them as bf16 into
+//                   a ring of A-operand slots in the 128-byte-swizzled layout
+//                   the tensor cores read; then the epilogue, two warps per
 //                   32-lane TMEM quarter, one per 256-column accumulator half.
+//   The raw inputs never pass through shared memory: only the operand does.
 //
 // fused x (FX): D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulators.
-//   Stages of 64 reduction columns, 128-byte swizzle: a raw stage is 3 x 16 KB,
-//   an operand entry is one W chunk [256 k x 64 n] (32 KB). A = dg or dfc
-//   [128 m x 64 n] (K-major, in the g/fc slots), B = W_g / W_fc. Each dg
-//   element is computed once per 512 columns of dx (once when K <= 512); dg,
-//   dfc can also be written to HBM as optional outputs.
+//   Stages of 64 reduction columns. A = dg or dfc [128 m x 64 n] (K-major),
+//   B = W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries). Each dg element
+//   is computed once per 512 columns of dx (once when K <= 512); dg, dfc can
+//   also be written to HBM as optional outputs.
 // fused w (FW): D = [dw_g^T ; dw_fc^T][n0:n0+64, k0:k0+512]: the A operand
-//   stacks 64 columns of dg over the same 64 columns of dfc (MN-major, 128-byte
-//   swizzle; the g slot and the fc slot are the two 64-element MN chunks,
-//   LBO = 8 KB apart), so one accumulator pair holds both outputs for all k.
+//   stacks 64 columns of dg over the same 64 columns of dfc (MN-major; the two
+//   8 KB halves of a slot are the two 64-element MN chunks, LBO = 8 KB), so one
+//   accumulator pair holds both outputs for all k. Stages of 64 rows of m;
 //   B = x [64 m x 256 k] (MN-major). The CTA owns a fixed band of 64 columns
 //   for its whole M range, so it also sums dg, dfc over its rows in registers
 //   (db column partials, one row per M split). The reduction over M is split
@@ -52,53 +52,55 @@ namespace {
 
 enum FusedMode : int { kFX = 0, kFW = 1 };
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 320;
 constexpr int kXThreads = 256;  // transform / epilogue threads (warps 2-9)
-constexpr int kRingWarp = 10;
-constexpr int kClusterX = 4;  // CTAs sharing each W chunk in the fused x kernel
-constexpr int kClusterW = 4;  // CTAs sharing each x chunk in the fused w kernel
+constexpr int kClusterX = 2;    // CTAs sharing each W chunk in the fused x kernel
+constexpr int kClusterW = 4;    // CTAs sharing each x chunk in the fused w kernel
 constexpr uint32_t kTmemCols = 512;
 
 template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kFX> {
-  static constexpr int kRawRows = 128;     // m rows of a raw tile
-  static constexpr int kRowBytes = 128;    // 64 bf16 reduction columns, 128-byte swizzle
-  static constexpr int kRawStages = 2;
+  static constexpr int kRows = 128;        // m rows of a stage's tile (64 columns of n)
+  static constexpr int kAStages = 3;       // A-operand slots (dg + dfc, 2 x 16 KB each)
   static constexpr int kEntryBytes = 32768;
   static constexpr int kEntries = 4;
+  static constexpr int kPrefetch = 8;      // stages prefetched into L2 ahead of the loads
 };
 template <>
 struct Cfg<kFW> {
-  static constexpr int kRawRows = 64;
-  static constexpr int kRowBytes = 128;    // 64 bf16 columns of n, 128-byte swizzle
-  static constexpr int kRawStages = 4;
+  static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
+  static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
   static constexpr int kEntryBytes = 32768;
-  static constexpr int kEntries = 4;
+  static constexpr int kEntries = 5;
+  static constexpr int kPrefetch = 4;
 };
 
 template <int MODE>
 struct __align__(1024) FSmem {
   using C = Cfg<MODE>;
-  static constexpr int kSlot = C::kRawRows * C::kRowBytes;
+  static constexpr int kHalf = C::kRows * 128;  // one 64-column bf16 tile (dg or dfc)
   uint8_t ring[C::kEntries][C::kEntryBytes];
-  uint8_t raw[C::kRawStages][3][kSlot];  // dy, g (-> dg), fc (-> dfc)
-  uint64_t raw_full[C::kRawStages];
-  uint64_t raw_empty[C::kRawStages];
-  uint64_t a_ready[C::kRawStages];
+  uint8_t aop[C::kAStages][2 * kHalf];          // [dg | dfc]
+  uint64_t a_full[C::kAStages];
+  uint64_t a_empty[C::kAStages];
   uint64_t ring_full[C::kEntries];
   uint64_t ring_empty[C::kEntries];
-  uint64_t accum;
+  uint64_t accum;      // one phase per tile: the tile's MMAs are done
+  uint64_t tmem_free;  // one phase per tile: the epilogue has read the accumulator
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
-  volatile uint32_t raw_issued, raw_consumed, ring_issued, ring_consumed;
+  volatile uint32_t ring_issued, ring_consumed;
 };
 
 struct FusedArgs {
   int M, K, N;
   uint32_t* status;
   int tiles_k;  // 512-column blocks of K
+  const uint16_t* dy;
+  const uint16_t* g;
+  const uint16_t* fc;
   // FX
   uint16_t* dx;
   uint16_t* dg_out;
@@ -109,8 +111,40 @@ struct FusedArgs {
   float* ws;       // [splits][2][K][N] dw partials (splits > 1)
   float* db_part;  // [splits][2N]
   int splits, kb_per, nkb_total, tiles_n;
-  int x3d;  // x entries come from one 3-D box (else four 2-D boxes)
+  int x3d;  // x entries come from one 3-D box (else 2-D boxes)
+  int cluster_tiles;  // work items of CS CTAs; cluster c takes c, c + nclusters, ...
+  int mtiles;         // FX: 128-row tiles of M
 };
+
+// One CTA's share of one cluster tile.
+struct Tile {
+  int m0, n0, k0, kt, split, nst, kb_begin, nh, eps;
+};
+
+template <int MODE, int CS>
+__device__ __forceinline__ Tile tile_of(int ct, uint32_t crank, const FusedArgs& args) {
+  Tile t;
+  t.m0 = t.n0 = t.split = t.kb_begin = 0;
+  if (MODE == kFX) {
+    // cluster tile = CS consecutive m tiles at one 512-column block of K
+    t.kt = ct % args.tiles_k;
+    t.m0 = ((ct / args.tiles_k) * CS + static_cast<int>(crank)) * 128;
+    t.nst = (args.N + 63) / 64;  // stages: 64 columns of n each
+  } else {
+    // cluster tile = CS consecutive 64-column bands of n, one K block, one M split
+    const int bands = args.tiles_n / CS;
+    t.n0 = ((ct % bands) * CS + static_cast<int>(crank)) * 64;
+    const int rest = ct / bands;
+    t.kt = rest % args.tiles_k;
+    t.split = rest / args.tiles_k;
+    t.kb_begin = t.split * args.kb_per;
+    t.nst = min(args.nkb_total, t.kb_begin + args.kb_per) - t.kb_begin;  // stages: 64 rows of m each
+  }
+  t.k0 = t.kt * 512;
+  t.nh = (args.K - t.k0) > 256 ? 2 : 1;             // 256-column accumulator halves in use
+  t.eps = (MODE == kFX) ? 2 * t.nh : t.nh;          // ring entries per stage
+  return t;
+}
 
 template <int MODE>
 __device__ __forceinline__ void flag_timeout(FSmem<MODE>& s, uint32_t* status) {
@@ -118,14 +152,16 @@ __device__ __forceinline__ void flag_timeout(FSmem<MODE>& s, uint32_t* status) {
   s.abort_flag = 1u;
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+__device__ __forceinline__ uint4 ldg_stream(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 __device__ __forceinline__ void named_sync_transform() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -140,15 +176,16 @@ __device__ __forceinline__ void grad8_sum(const uint4& dy, const uint4& g, const
   uint32_t og[4], of[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float g0, f0, g1, f1;
-    swiglu_grad_elem(bf16lo(dyw[i]), bf16lo(gw[i]), bf16lo(fw[i]), g0, f0);
-    swiglu_grad_elem(bf16hi(dyw[i]), bf16hi(gw[i]), bf16hi(fw[i]), g1, f1);
-    sg[2 * i] += g0;
-    sg[2 * i + 1] += g1;
-    sf[2 * i] += f0;
-    sf[2 * i + 1] += f1;
-    og[i] = pack_bf16x2(g0, g1);
-    of[i] = pack_bf16x2(f0, f1);
+    float2 pg, pf;
+    swiglu_grad_pair(bf16x2_to_f2(dyw[i]), bf16x2_to_f2(gw[i]), bf16x2_to_f2(fw[i]), pg, pf);
+    const float2 ag = __fadd2_rn(make_float2(sg[2 * i], sg[2 * i + 1]), pg);
+    const float2 af = __fadd2_rn(make_float2(sf[2 * i], sf[2 * i + 1]), pf);
+    sg[2 * i] = ag.x;
+    sg[2 * i + 1] = ag.y;
+    sf[2 * i] = af.x;
+    sf[2 * i + 1] = af.y;
+    og[i] = pack_bf16x2(pg.x, pg.y);
+    of[i] = pack_bf16x2(pf.x, pf.y);
   }
   dg = make_uint4(og[0], og[1], og[2], og[3]);
   dfc = make_uint4(of[0], of[1], of[2], of[3]);
@@ -165,56 +202,38 @@ template <int MODE, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_g,
                  const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_b0,
-                 const __grid_constant__ CUtensorMap tm_b1, const FusedArgs args) {
+                 const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_out,
+                 const FusedArgs args) {
   using S = FSmem<MODE>;
   using C = Cfg<MODE>;
-  constexpr int kRS = C::kRawStages;
+  constexpr int kAS = C::kAStages;
   constexpr int kRE = C::kEntries;
-  constexpr int kRows = C::kRawRows;
-  constexpr int kSlot = S::kSlot;
+  constexpr int kRows = C::kRows;
+  constexpr int kHalf = S::kHalf;
+  constexpr int kRPT = kRows / 32;  // rows per transform thread per stage
   extern __shared__ uint8_t smem_raw[];
   S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- tile coordinates
   const uint32_t crank = CS > 1 ? cluster_ctarank() : 0u;
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CS) - 1u);
-  int m0 = 0, n0 = 0, k0 = 0, kt = 0, split = 0, nst = 0, kb_begin = 0;
-  if (MODE == kFX) {
-    // clusters of CS consecutive m tiles share kt (and so every W chunk)
-    const int cid = blockIdx.x / CS;
-    kt = cid % args.tiles_k;
-    m0 = ((cid / args.tiles_k) * CS + static_cast<int>(crank)) * 128;
-    k0 = kt * 512;
-    nst = (args.N + 63) / 64;  // raw stages: 64 columns of n each
-  } else {
-    int t = blockIdx.x;
-    const int nt = t % args.tiles_n;
-    t /= args.tiles_n;
-    kt = t % args.tiles_k;
-    split = t / args.tiles_k;
-    n0 = nt * 64;
-    k0 = kt * 512;
-    kb_begin = split * args.kb_per;
-    nst = min(args.nkb_total, kb_begin + args.kb_per) - kb_begin;  // raw stages: 64 rows of m each
-  }
-  const int nh = (args.K - k0) > 256 ? 2 : 1;  // 256-column accumulator halves in use
-  const int entries_per_stage = (MODE == kFX) ? 2 * nh : nh;
+  const int cluster = blockIdx.x / CS;
+  const int nclusters = gridDim.x / CS;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRS; ++i) {
-      mbar_init(&s.raw_full[i], 1);
-      mbar_init(&s.raw_empty[i], 1);
-      mbar_init(&s.a_ready[i], kXThreads);
+    for (int i = 0; i < kAS; ++i) {
+      mbar_init(&s.a_full[i], kXThreads);
+      mbar_init(&s.a_empty[i], 1);
     }
     for (int i = 0; i < kRE; ++i) {
       mbar_init(&s.ring_full[i], 1);
       mbar_init(&s.ring_empty[i], CS);  // released by all CTAs of the cluster
     }
     mbar_init(&s.accum, 1);
+    mbar_init(&s.tmem_free, kXThreads);
     s.abort_flag = 0u;
-    s.raw_issued = s.raw_consumed = s.ring_issued = s.ring_consumed = 0u;
+    s.ring_issued = s.ring_consumed = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_dy);
     tma_prefetch_desc(&tm_g);
@@ -233,71 +252,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ raw producer
-    if (lane == 0) {
-      for (int i = 0; i < nst && !s.abort_flag; ++i) {
-        const int r = i % kRS;
-        if (i >= kRS && !mbar_wait(&s.raw_empty[r], ((i / kRS) - 1) & 1)) {
-          flag_timeout(s, args.status);
-          break;
-        }
-        const int c0 = MODE == kFX ? i * 64 : n0;               // n
-        const int c1 = MODE == kFX ? m0 : (kb_begin + i) * 64;  // m
-        mbar_arrive_expect_tx(&s.raw_full[r], 3 * kSlot);
-        tma_load_2d(s.raw[r][0], &tm_dy, &s.raw_full[r], c0, c1);
-        tma_load_2d(s.raw[r][1], &tm_g, &s.raw_full[r], c0, c1);
-        tma_load_2d(s.raw[r][2], &tm_fc, &s.raw_full[r], c0, c1);
-        s.raw_issued = i + 1;
-      }
-    }
-  } else if (warp == kRingWarp) {
     // ------------------------------------------------------------ operand producer
     if (lane == 0) {
-      const int total = nst * entries_per_stage;
-      for (int j = 0; j < total && !s.abort_flag; ++j) {
-        const int e = j % kRE;
-        if (j >= kRE && !mbar_wait(&s.ring_empty[e], ((j / kRE) - 1) & 1)) {
-          flag_timeout(s, args.status);
-          break;
-        }
-        const int i = j / entries_per_stage, q = j % entries_per_stage;
-        mbar_arrive_expect_tx(&s.ring_full[e], C::kEntryBytes);  // all CS slices land here
-        if (MODE == kFX) {
-          const int p = q / nh, h = q % nh;  // W_g / W_fc, k half
-          constexpr int kSliceRows = 256 / CS;
-          uint8_t* dst = s.ring[e] + crank * kSliceRows * 128;
-          const int kr = k0 + 256 * h + static_cast<int>(crank) * kSliceRows;
-          if (CS > 1)
-            tma_load_2d_mc(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr, kMask);
-          else
-            tma_load_2d(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr);
-        } else {
-          const int mrow = (kb_begin + i) * 64;
-          const int kk = k0 + 256 * q;
-          constexpr int kSliceChunks = 4 / CS;  // 64x64 blocks of the entry this CTA loads
-          const int c_begin = static_cast<int>(crank) * kSliceChunks;
-          uint8_t* dst = s.ring[e] + c_begin * 8192;
-          if (args.x3d) {
+      uint32_t gj = 0;  // ring entries issued, over all tiles
+      for (int ct = cluster; ct < args.cluster_tiles && !s.abort_flag; ct += nclusters) {
+        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+        const int total = tl.nst * tl.eps;
+        for (int j = 0; j < total && !s.abort_flag; ++j, ++gj) {
+          const int e = gj % kRE;
+          if (gj >= kRE && !mbar_wait(&s.ring_empty[e], ((gj / kRE) - 1) & 1)) {
+            flag_timeout(s, args.status);
+            break;
+          }
+          const int i = j / tl.eps, q = j % tl.eps;
+          mbar_arrive_expect_tx(&s.ring_full[e], C::kEntryBytes);  // all CS slices land here
+          if (MODE == kFX) {
+            const int p = q / tl.nh, h = q % tl.nh;  // W_g / W_fc, k half
+            constexpr int kSliceRows = 256 / CS;
+            uint8_t* dst = s.ring[e] + crank * kSliceRows * 128;
+            const int kr = tl.k0 + 256 * h + static_cast<int>(crank) * kSliceRows;
             if (CS > 1)
-              tma_load_3d_mc(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin, kMask);
+              tma_load_2d_mc(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr, kMask);
             else
-              tma_load_3d(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin);
+              tma_load_2d(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr);
           } else {
-#pragma unroll
-            for (int c = 0; c < kSliceChunks; ++c) {
+            const int mrow = (tl.kb_begin + i) * 64;
+            const int kk = tl.k0 + 256 * q;
+            constexpr int kSliceChunks = 4 / CS;  // 64x64 blocks of the entry this CTA loads
+            const int c_begin = static_cast<int>(crank) * kSliceChunks;
+            uint8_t* dst = s.ring[e] + c_begin * 8192;
+            if (args.x3d) {
               if (CS > 1)
-                tma_load_2d_mc(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow, kMask);
+                tma_load_3d_mc(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin, kMask);
               else
-                tma_load_2d(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow);
+                tma_load_3d(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin);
+            } else {
+#pragma unroll
+              for (int c = 0; c < kSliceChunks; ++c) {
+                if (CS > 1)
+                  tma_load_2d_mc(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow, kMask);
+                else
+                  tma_load_2d(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow);
+              }
             }
           }
+          s.ring_issued = gj + 1;
         }
-        s.ring_issued = j + 1;
       }
       if (CS > 1 && !s.abort_flag) {
         // the peers' last releases arrive on this CTA's barriers: see them land
         // before this CTA can leave
-        for (int j = max(0, total - kRE); j < total; ++j)
+        for (uint32_t j = gj > static_cast<uint32_t>(kRE) ? gj - kRE : 0u; j < gj; ++j)
           if (!mbar_wait(&s.ring_empty[j % kRE], (j / kRE) & 1)) {
             flag_timeout(s, args.status);
             break;
@@ -308,91 +313,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, MODE == kFW, MODE == kFW);
-      uint32_t j = 0;
+      uint32_t gi = 0, gj = 0, tt = 0;  // A stages, ring entries, tiles consumed
       bool ok = true;
-      for (int i = 0; i < nst && ok; ++i) {
-        const int r = i % kRS;
-        if (!mbar_wait(&s.a_ready[r], (i / kRS) & 1)) {
-          flag_timeout(s, args.status);
-          break;
+      for (int ct = cluster; ct < args.cluster_tiles && ok; ct += nclusters, ++tt) {
+        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+        if (tt > 0) {
+          // the previous tile's epilogue must have read the accumulator out
+          if (!mbar_wait(&s.tmem_free, (tt - 1) & 1)) {
+            flag_timeout(s, args.status);
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint32_t g_slot = smem_u32(s.raw[r][1]);
-        for (int q = 0; q < entries_per_stage; ++q, ++j) {
-          const int e = j % kRE;
-          if (!mbar_wait(&s.ring_full[e], (j / kRE) & 1)) {
+        for (int i = 0; i < tl.nst && ok; ++i, ++gi) {
+          const int a = gi % kAS;
+          if (!mbar_wait(&s.a_full[a], (gi / kAS) & 1)) {
             flag_timeout(s, args.status);
             ok = false;
             break;
           }
-          s.ring_consumed = j + 1;
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(s.ring[e]);
-          if (MODE == kFX) {
-            const int p = q / nh, h = q % nh;
-            const uint32_t a_addr = g_slot + p * kSlot;  // dg or dfc
+          const uint32_t a_slot = smem_u32(s.aop[a]);
+          for (int q = 0; q < tl.eps; ++q, ++gj) {
+            const int e = gj % kRE;
+            if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1)) {
+              flag_timeout(s, args.status);
+              ok = false;
+              break;
+            }
+            s.ring_consumed = gj + 1;
+            tc_fence_after();
+            const uint32_t b_addr = smem_u32(s.ring[e]);
+            if (MODE == kFX) {
+              const int p = q / tl.nh, h = q % tl.nh;
+              const uint32_t a_addr = a_slot + p * kHalf;  // dg or dfc
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 32 * k, 16, 1024),
-                        idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
-          } else {
-            const int h = q;
+              for (int k = 0; k < 4; ++k)
+                umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024),
+                          smem_desc(b_addr + 32 * k, 16, 1024), idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
+            } else {
+              const int h = q;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + h * 256, smem_desc(g_slot + 2048 * k, kSlot, 1024),
-                        smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                umma_bf16(tmem + h * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
+                          smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
+            }
+            if (CS > 1)
+              umma_commit_mc(&s.ring_empty[e], kMask);  // release the entry in every CTA of the cluster
+            else
+              umma_commit(&s.ring_empty[e]);
           }
-          if (CS > 1)
-            umma_commit_mc(&s.ring_empty[e], kMask);  // release the entry in every CTA of the cluster
-          else
-            umma_commit(&s.ring_empty[e]);
+          umma_commit(&s.a_empty[a]);
         }
-        umma_commit(&s.raw_empty[r]);
+        umma_commit(&s.accum);  // this tile's accumulator is complete
       }
-      umma_commit(&s.accum);
     }
   } else {
     // ------------------------------------------------------------ transform
-    const int t = threadIdx.x - 64;                // 0..255
-    constexpr int kChunks = C::kRowBytes / 16;     // 16-byte chunks per row: 8
-    constexpr int kGroups = kXThreads / kChunks;   // row groups: 32
-    const int c = t % kChunks;                     // logical chunk (8 columns)
-    const int rg = t / kChunks;
-    const bool want_dg = (MODE == kFX) && kt == 0 && args.dg_out != nullptr;
-    const bool want_db = (MODE == kFW) && kt == 0 && args.db_part != nullptr;
+    const int t = threadIdx.x - 64;  // 0..255
+    const int c = t & 7;             // 16-byte chunk of the 64-column tile (8 columns)
+    const int rg = t >> 3;           // row group 0..31; rows rg, rg + 32, ...
+    const int64_t N64 = args.N;
+    // A thread whose wait runs out stops computing ("dead") but keeps taking
+    // part in the arrivals and the named barriers.
+    bool dead = false;
+    uint32_t gi = 0, tt = 0;  // A stages, tiles produced
+    for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters, ++tt) {
+    const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+    const int m0 = tl.m0, n0 = tl.n0, k0 = tl.k0, kb_begin = tl.kb_begin, nst = tl.nst, nh = tl.nh, split = tl.split;
+    const bool want_dg = (MODE == kFX) && tl.kt == 0 && args.dg_out != nullptr;
+    const bool want_db = (MODE == kFW) && tl.kt == 0 && args.db_part != nullptr;
     float cg[8], cf[8];  // column sums (FW: over the CTA's whole M range)
 #pragma unroll
     for (int e = 0; e < 8; ++e) cg[e] = cf[e] = 0.0f;
-    // A thread whose wait runs out stops computing ("dead") but keeps taking
-    // part in the arrivals (and, at the end, the named barriers).
-    bool dead = false;
-    for (int i = 0; i < nst; ++i) {
-      const int r = i % kRS;
-      if (!dead && !mbar_wait(&s.raw_full[r], (i / kRS) & 1)) {
+
+    // global coordinates of this thread's q-th row of stage i
+    auto grow = [&](int i, int q) { return (MODE == kFX ? m0 : (kb_begin + i) * 64) + rg + 32 * q; };
+    auto gcol = [&](int i) { return (MODE == kFX ? i * 64 : n0) + c * 8; };
+    auto load = [&](int i, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
+      const int col = gcol(i);
+#pragma unroll
+      for (int q = 0; q < kRPT; ++q) {
+        const int row = grow(i, q);
+        if (i < nst && row < args.M && col < args.N) {  // tails read as zeros
+          const int64_t o = static_cast<int64_t>(row) * N64 + col;
+          bdy[q] = ldg_stream(args.dy + o);
+          bg[q] = ldg_stream(args.g + o);
+          bfc[q] = ldg_stream(args.fc + o);
+        } else {
+          bdy[q] = bg[q] = bfc[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    };
+    auto prefetch = [&](int i) {
+      if (i < nst) {
+        const int p0 = MODE == kFX ? i * 64 : n0;
+        const int p1 = MODE == kFX ? m0 : (kb_begin + i) * 64;
+        tma_prefetch_l2_2d(&tm_dy, p0, p1);
+        tma_prefetch_l2_2d(&tm_g, p0, p1);
+        tma_prefetch_l2_2d(&tm_fc, p0, p1);
+      }
+    };
+
+    auto process = [&](int i, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
+      const uint32_t gs = gi + i;  // global A-stage index
+      const int a = gs % kAS;
+      if (!dead && gs >= kAS && !mbar_wait(&s.a_empty[a], ((gs / kAS) - 1) & 1)) {
         flag_timeout(s, args.status);
         dead = true;
       }
       if (s.abort_flag) dead = true;
-      if (t == 0 && !dead) s.raw_consumed = i + 1;
       if (!dead) {
-        const uint32_t sdy = smem_u32(s.raw[r][0]);
-        const uint32_t sg = sdy + kSlot;
-        const uint32_t sf = sdy + 2 * kSlot;
+        const uint32_t sdg = smem_u32(s.aop[a]);
+        const uint32_t sdf = sdg + kHalf;
 #pragma unroll
-        for (int qq = 0; qq < kRows / kGroups; ++qq) {
-          const int row = rg + kGroups * qq;
+        for (int q = 0; q < kRPT; ++q) {
+          const int row = rg + 32 * q;  // row within the tile
           // 128-byte swizzle: the 16-byte chunk index is XORed with row & 7
-          const int phys = c ^ (row & 7);
-          const uint32_t off = row * C::kRowBytes + (phys << 4);
+          const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
           uint4 odg, odfc;
-          grad8_sum(lds128(sdy + off), lds128(sg + off), lds128(sf + off), odg, odfc, cg, cf);
-          sts128(sg + off, odg);
-          sts128(sf + off, odfc);
+          grad8_sum(bdy[q], bg[q], bfc[q], odg, odfc, cg, cf);
+          sts128(sdg + off, odg);
+          sts128(sdf + off, odfc);
           if (want_dg) {
-            const int grow = m0 + row;
-            const int gcol = i * 64 + c * 8;
-            if (grow < args.M && gcol < args.N) {
-              const int64_t o = static_cast<int64_t>(grow) * args.N + gcol;
+            const int r = grow(i, q), col = gcol(i);
+            if (r < args.M && col < args.N) {
+              const int64_t o = static_cast<int64_t>(r) * N64 + col;
               *reinterpret_cast<uint4*>(args.dg_out + o) = odg;
               *reinterpret_cast<uint4*>(args.dfc_out + o) = odfc;
             }
@@ -400,16 +446,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();  // dg, dfc written by this thread -> visible to the tensor core
       }
-      mbar_arrive(&s.a_ready[r]);
+      mbar_arrive(&s.a_full[a]);
+    };
+
+    if (t == 0)
+      for (int i = 0; i <= C::kPrefetch; ++i) prefetch(i);
+    uint4 xdy[kRPT], xg[kRPT], xfc[kRPT], ydy[kRPT], yg[kRPT], yfc[kRPT];
+    load(0, xdy, xg, xfc);
+    for (int i = 0; i < nst; i += 2) {
+      // two stages per iteration, alternating register buffers: the loads of the
+      // next stage are in flight while this stage is computed
+      if (t == 0) prefetch(i + 1 + C::kPrefetch);
+      load(i + 1, ydy, yg, yfc);
+      process(i, xdy, xg, xfc);
+      if (i + 1 >= nst) break;
+      if (t == 0) prefetch(i + 2 + C::kPrefetch);
+      load(i + 2, xdy, xg, xfc);
+      process(i + 1, ydy, yg, yfc);
     }
 
-    const bool acc_ok = mbar_wait(&s.accum, 0);
+    gi += nst;
+    const bool acc_ok = mbar_wait(&s.accum, tt & 1);
     if (!acc_ok) flag_timeout(s, args.status);
     if (want_db) {
-      // Column sums over the CTA's rows (rows beyond M are zero-filled by TMA
-      // and add 0). Lanes l, l^8, l^16, l^24 share a chunk; the 8 warps are
-      // combined through the first raw slot, idle once accum has fired (every
-      // raw stage has been consumed by then).
+      // Column sums over the CTA's rows (rows beyond M were read as zeros).
+      // Lanes l, l^8, l^16, l^24 share a chunk; the 8 warps are combined
+      // through the first A slot, idle once accum has fired.
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         cg[e] += __shfl_xor_sync(0xffffffffu, cg[e], 8);
@@ -418,25 +480,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 16);
       }
       named_sync_transform();
-      float* scratch = reinterpret_cast<float*>(s.raw[0][0]);  // [8 warps][8 chunks][16]
+      float* scratch = reinterpret_cast<float*>(s.aop[0]);  // [8 warps][8 chunks][16]
       if (lane < 8) {
-        float* p = scratch + ((warp - 2) * 8 + c) * 16;
+        float* pp = scratch + ((warp - 2) * 8 + c) * 16;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = cg[e];
-          p[8 + e] = cf[e];
+          pp[e] = cg[e];
+          pp[8 + e] = cf[e];
         }
       }
       named_sync_transform();
       if (t < 128) {
         const int which = t >> 6;  // 0: dg, 1: dfc
         const int col = t & 63;
-        const int gcol = n0 + col;
-        if (!dead && acc_ok && gcol < args.N) {
+        const int gc = n0 + col;
+        if (!dead && acc_ok && gc < args.N) {
           float v = 0.0f;
 #pragma unroll
           for (int w = 0; w < 8; ++w) v += scratch[(w * 8 + (col >> 3)) * 16 + which * 8 + (col & 7)];
-          args.db_part[static_cast<int64_t>(split) * 2 * args.N + which * args.N + gcol] = v;
+          args.db_part[static_cast<int64_t>(split) * 2 * args.N + which * args.N + gc] = v;
         }
       }
     }
@@ -455,12 +517,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         const int kcol = k0 + h * 256 + cc * 32;
         if (MODE == kFX) {
-          const int row = m0 + r;
-          if (row < args.M) {
-            uint4* dst = reinterpret_cast<uint4*>(args.dx + static_cast<int64_t>(row) * args.K + kcol);
+          // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
+          // store (rows beyond M and columns beyond K are clipped by the copy engine)
+          uint8_t* buf = s.aop[0] + (warp - 2) * 4096 + (cc & 1) * 2048;
+          if (cc >= 2) {
+            if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+            __syncwarp();
+          }
+          const uint32_t sb = smem_u32(buf) + lane * 64;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (kcol + 8 * j < args.K) dst[j] = pack8(v + 8 * j);
+          for (int j = 0; j < 4; ++j) sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), pack8(v + 8 * j));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_out, buf, kcol, m0 + q * 32);
+            bulk_commit();
           }
         } else {
           const int prob = r >> 6;  // lanes 0-63: dw_g, 64-127: dw_fc
@@ -489,13 +560,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_before();
+    mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
+    if (MODE == kFX) {
+      // the next tile's transform reuses the A slots that stage these stores
+      if (lane == 0) bulk_wait_read<0>();
+      named_sync_transform();
+    }
+    }  // tile loop
+    if (MODE == kFX && lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
   }
 
   __syncthreads();
   if (threadIdx.x == 0 && s.abort_flag) {
-    // drain: copies issued but never waited on must land before the CTA exits
-    for (uint32_t i = s.raw_consumed; i < s.raw_issued; ++i)
-      if (!mbar_wait(&s.raw_full[i % kRS], (i / kRS) & 1)) break;
+    // drain: ring copies issued but never waited on must land before the CTA exits
     for (uint32_t i = s.ring_consumed; i < s.ring_issued; ++i)
       if (!mbar_wait(&s.ring_full[i % kRE], (i / kRE) & 1)) break;
   }
@@ -514,7 +591,8 @@ constexpr size_t smem_bytes() {
 
 template <int MODE, int CS>
 cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, const CUtensorMap& b,
-                   const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const FusedArgs& args) {
+                   const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const CUtensorMap& out,
+                   FusedArgs args, bool persistent) {
   constexpr size_t smem = smem_bytes<MODE>();
   static_assert(smem <= 232448, "fused kernel shared memory");
   cudaError_t err = cudaFuncSetAttribute(fused_kernel<MODE, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -532,7 +610,15 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fused_kernel<MODE, CS>, a, b, c, d, e, args);
+  args.cluster_tiles = static_cast<int>(grid / CS);
+  if (persistent) {
+    // one resident wave of clusters, each looping over cluster tiles
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, fused_kernel<MODE, CS>, &cfg) == cudaSuccess &&
+        max_clusters > 0 && static_cast<unsigned>(max_clusters) * CS < grid)
+      cfg.gridDim = dim3(static_cast<unsigned>(max_clusters) * CS);
+  }
+  return cudaLaunchKernelEx(&cfg, fused_kernel<MODE, CS>, a, b, c, d, e, out, args);
 }
 
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -560,10 +646,12 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
                            const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
                            int64_t N, cudaStream_t stream) {
   constexpr int CS = kClusterX;
-  CUtensorMap mdy, mg, mfc, mw0, mw1;
+  CUtensorMap mdy, mg, mfc, mw0, mw1, mdx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
-  if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 128) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 128) ||
-      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128) ||
+  if (!encode_tmap_2d_bf16(&mdx, dx, K, M, static_cast<uint64_t>(K) * 2, 32, 32, 64)) return cudaErrorInvalidValue;
+  // the raw tensors are only prefetched into L2 here, one stage's box at a time
+  if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 128, 0) ||
+      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) ||
       !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256 / CS) ||
       !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256 / CS))
     return cudaErrorInvalidValue;
@@ -573,11 +661,15 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
   a.N = static_cast<int>(N);
   a.status = status_word_ptr();
   a.tiles_k = static_cast<int>((K + 511) / 512);
+  a.dy = dy;
+  a.g = g;
+  a.fc = fc;
   a.dx = dx;
   a.dg_out = dg;
   a.dfc_out = dfc;
   const int64_t mclusters = ((M + 127) / 128 + CS - 1) / CS;  // tail CTAs run on zero-filled rows
-  return launch<kFX, CS>(static_cast<unsigned>(mclusters * CS * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, a);
+  return launch<kFX, CS>(static_cast<unsigned>(mclusters * CS * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, mdx, a,
+                         true);
 }
 
 cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
@@ -606,6 +698,9 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   a.N = static_cast<int>(N);
   a.status = status_word_ptr();
   a.tiles_k = static_cast<int>((K + 511) / 512);
+  a.dy = dy;
+  a.g = g;
+  a.fc = fc;
   a.dw_g = dw_g;
   a.dw_fc = dw_fc;
   const size_t dw_part = plan.splits > 1 ? static_cast<size_t>(plan.splits) * 2 * K * N * sizeof(float) : 0;
@@ -617,7 +712,7 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   a.tiles_n = static_cast<int>(((N + 63) / 64 + CS - 1) / CS * CS);  // clusters of CS n tiles
   a.x3d = x3d;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
-  cudaError_t e = launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, a);
+  cudaError_t e = launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {
     e = launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream);

@@ -322,7 +322,10 @@ cudaError_t prepare_kernel() {
 }  // namespace
 
 static CUtensorMapSwizzle swizzle_mode(int bytes) {
-  return bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return bytes == 0    ? CU_TENSOR_MAP_SWIZZLE_NONE
+         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                       : CU_TENSOR_MAP_SWIZZLE_128B;
 }
 
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,

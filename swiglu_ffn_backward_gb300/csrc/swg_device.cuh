@@ -11,45 +11,59 @@
 namespace swg {
 
 // ---------------------------------------------------------------- numerics
-// sigma(z) and 1 - sigma(z) in fp32 without overflow: with e = exp(-|z|) in
-// (0, 1] and r = 1 / (1 + e), sigma = r for z >= 0 and e*r for z < 0; the
-// complement is the other one, so neither is formed by cancellation.
-struct Sig {
-  float s;   // sigma(z)
-  float sc;  // 1 - sigma(z)
-};
+// sigma(z) and 1 - sigma(z) in fp32, two elements at a time (packed fp32x2
+// arithmetic): e = e^-z = 2^(-z log2 e) with the ex2.approx instruction,
+// s = 1/(1 + e) with rcp.approx (about 1 ulp), 1 - s formed directly. No
+// overflow case is special: for z below about -88, e is +inf and s = 0
+// exactly, 1 - s = 1. For large positive z the difference 1 - s carries an
+// absolute error of at most half an ulp of 1, which only ever multiplies z
+// inside 1 + z (1 - s), where it is negligible against the 1.
+// Every element-wise kernel uses these helpers, so the b stage, the fused
+// GEMM producers and SwishGrad produce bit-identical values for equal inputs.
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
-
-__device__ __forceinline__ Sig sigmoid_pair(float z) {
-  const float e = __expf(-fabsf(z));
-  const float r = rcp_approx(1.0f + e);  // 1 + e in [1, 2]: no denormal or overflow cases
-  const float er = e * r;
-  Sig o;
-  o.s = z >= 0.0f ? r : er;
-  o.sc = z >= 0.0f ? er : r;
-  return o;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+struct Sig2 {
+  float2 s;   // sigma(z)
+  float2 sc;  // 1 - sigma(z)
+};
+
+__device__ __forceinline__ Sig2 sigmoid_pair2(float2 z) {
+  const float2 a = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+  const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+  const float2 d = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+  Sig2 o;
+  o.s = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+  o.sc = __ffma2_rn(o.s, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f));
+  return o;
+}
 
 // two fp32 -> packed bf16x2, round to nearest even (lo in the low half)
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// the two bf16 of a packed word, widened exactly (low half first)
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
 
-// b-stage math for one element (fp32): dg = dy*fc*s*(1+g*(1-s)), dfc = dy*g*s
-__device__ __forceinline__ void swiglu_grad_elem(float dy, float g, float fc, float& dg, float& dfc) {
-  const Sig q = sigmoid_pair(g);
-  const float dys = dy * q.s;
-  dfc = dys * g;
-  dg = dys * fc * fmaf(g, q.sc, 1.0f);
+// b-stage math for two elements (fp32): dg = dy*fc*s*(1+g*(1-s)), dfc = dy*g*s
+__device__ __forceinline__ void swiglu_grad_pair(float2 dy, float2 g, float2 fc, float2& dg, float2& dfc) {
+  const Sig2 q = sigmoid_pair2(g);
+  const float2 dys = __fmul2_rn(dy, q.s);
+  dfc = __fmul2_rn(dys, g);
+  dg = __fmul2_rn(__fmul2_rn(dys, fc), __ffma2_rn(g, q.sc, make_float2(1.0f, 1.0f)));
 }
 
 // ---------------------------------------------------------------- status word
@@ -154,6 +168,21 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// 2-D tiled store shared -> global (bulk group); elements outside the tensor are not written
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N committed bulk groups still read their shared-memory source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until every committed bulk group has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // 2-D tiled prefetch global -> L2 (no shared-memory destination, no completion)
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -17,10 +17,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// two elements: t = beta x, grad_x = grad * s * (1 + t (1 - s)), s = sigma(t)
+__device__ __forceinline__ float2 swish_grad_f2(float2 grad, float2 x, float beta) {
+  const float2 t = __fmul2_rn(make_float2(beta, beta), x);
+  const Sig2 q = sigmoid_pair2(t);
+  return __fmul2_rn(grad, __fmul2_rn(q.s, __ffma2_rn(t, q.sc, make_float2(1.0f, 1.0f))));
+}
 __device__ __forceinline__ float swish_grad_f32(float grad, float x, float beta) {
-  const float t = beta * x;
-  const Sig q = sigmoid_pair(t);
-  return grad * (q.s * fmaf(t, q.sc, 1.0f));
+  return swish_grad_f2(make_float2(grad, 0.0f), make_float2(x, 0.0f), beta).x;
 }
 
 template <typename T>
@@ -43,27 +47,26 @@ struct Elem<__nv_bfloat16> {
 
 // one 16-byte vector: 4 fp32 or 8 fp16/bf16
 __device__ __forceinline__ uint4 vec_apply(uint4 g, uint4 x, float beta, float*) {
-  uint4 o;
-  o.x = __float_as_uint(swish_grad_f32(__uint_as_float(g.x), __uint_as_float(x.x), beta));
-  o.y = __float_as_uint(swish_grad_f32(__uint_as_float(g.y), __uint_as_float(x.y), beta));
-  o.z = __float_as_uint(swish_grad_f32(__uint_as_float(g.z), __uint_as_float(x.z), beta));
-  o.w = __float_as_uint(swish_grad_f32(__uint_as_float(g.w), __uint_as_float(x.w), beta));
-  return o;
+  const float2 a = swish_grad_f2(make_float2(__uint_as_float(g.x), __uint_as_float(g.y)),
+                                 make_float2(__uint_as_float(x.x), __uint_as_float(x.y)), beta);
+  const float2 b = swish_grad_f2(make_float2(__uint_as_float(g.z), __uint_as_float(g.w)),
+                                 make_float2(__uint_as_float(x.z), __uint_as_float(x.w)), beta);
+  return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b.x), __float_as_uint(b.y));
 }
 __device__ __forceinline__ uint32_t pair_h(uint32_t g, uint32_t x, float beta) {
   const __half2 gh = *reinterpret_cast<const __half2*>(&g);
   const __half2 xh = *reinterpret_cast<const __half2*>(&x);
-  const float2 gf = __half22float2(gh);
-  const float2 xf = __half22float2(xh);
-  __half2 r = __floats2half2_rn(swish_grad_f32(gf.x, xf.x, beta), swish_grad_f32(gf.y, xf.y, beta));
-  return *reinterpret_cast<uint32_t*>(&r);
+  const float2 r = swish_grad_f2(__half22float2(gh), __half22float2(xh), beta);
+  __half2 o = __floats2half2_rn(r.x, r.y);
+  return *reinterpret_cast<uint32_t*>(&o);
 }
 __device__ __forceinline__ uint4 vec_apply(uint4 g, uint4 x, float beta, __half*) {
   return make_uint4(pair_h(g.x, x.x, beta), pair_h(g.y, x.y, beta), pair_h(g.z, x.z, beta),
                     pair_h(g.w, x.w, beta));
 }
 __device__ __forceinline__ uint32_t pair_b(uint32_t g, uint32_t x, float beta) {
-  return pack_bf16x2(swish_grad_f32(bf16lo(g), bf16lo(x), beta), swish_grad_f32(bf16hi(g), bf16hi(x), beta));
+  const float2 r = swish_grad_f2(bf16x2_to_f2(g), bf16x2_to_f2(x), beta);
+  return pack_bf16x2(r.x, r.y);
 }
 __device__ __forceinline__ uint4 vec_apply(uint4 g, uint4 x, float beta, __nv_bfloat16*) {
   return make_uint4(pair_b(g.x, x.x, beta), pair_b(g.y, x.y, beta), pair_b(g.z, x.z, beta),
