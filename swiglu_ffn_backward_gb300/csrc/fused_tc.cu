@@ -23,7 +23,9 @@
 //   Stages of 64 reduction columns. A = dg or dfc [128 m x 64 n] (K-major),
 //   B = W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries). Each dg element
 //   is computed once per 512 columns of dx (once when K <= 512); dg, dfc can
-//   also be written to HBM as optional outputs.
+//   also be written to HBM as optional outputs. Persistent: each CTA loops
+//   over its tiles, and a tile's epilogue waits until the next tile's first
+//   stages are in their A slots, so the tensor core restarts right after it.
 // fused w (FW): D = [dw_g^T ; dw_fc^T][n0:n0+64, k0:k0+512]: the A operand
 //   stacks 64 columns of dg over the same 64 columns of dfc (MN-major; the two
 //   8 KB halves of a slot are the two 64-element MN chunks, LBO = 8 KB), so one
@@ -377,25 +379,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A thread whose wait runs out stops computing ("dead") but keeps taking
     // part in the arrivals and the named barriers.
     bool dead = false;
-    uint32_t gi = 0, tt = 0;  // A stages, tiles produced
-    for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters, ++tt) {
-    const Tile tl = tile_of<MODE, CS>(ct, crank, args);
-    const int m0 = tl.m0, n0 = tl.n0, k0 = tl.k0, kb_begin = tl.kb_begin, nst = tl.nst, nh = tl.nh, split = tl.split;
-    const bool want_dg = (MODE == kFX) && tl.kt == 0 && args.dg_out != nullptr;
-    const bool want_db = (MODE == kFW) && tl.kt == 0 && args.db_part != nullptr;
-    float cg[8], cf[8];  // column sums (FW: over the CTA's whole M range)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) cg[e] = cf[e] = 0.0f;
 
-    // global coordinates of this thread's q-th row of stage i
-    auto grow = [&](int i, int q) { return (MODE == kFX ? m0 : (kb_begin + i) * 64) + rg + 32 * q; };
-    auto gcol = [&](int i) { return (MODE == kFX ? i * 64 : n0) + c * 8; };
-    auto load = [&](int i, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
-      const int col = gcol(i);
+    // stores one stage's dg, dfc (8 columns x kRPT rows of this thread) into A slot a
+    auto store_stage = [&](int a, int row0, int col, bool want_dg, const uint4 (&bdy)[kRPT],
+                           const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT], float (&cg)[8], float (&cf)[8]) {
+      const uint32_t sdg = smem_u32(s.aop[a]);
+      const uint32_t sdf = sdg + kHalf;
 #pragma unroll
       for (int q = 0; q < kRPT; ++q) {
-        const int row = grow(i, q);
-        if (i < nst && row < args.M && col < args.N) {  // tails read as zeros
+        const int row = rg + 32 * q;  // row within the tile
+        // 128-byte swizzle: the 16-byte chunk index is XORed with row & 7
+        const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
+        uint4 odg, odfc;
+        grad8_sum(bdy[q], bg[q], bfc[q], odg, odfc, cg, cf);
+        sts128(sdg + off, odg);
+        sts128(sdf + off, odfc);
+        if (want_dg) {
+          const int r = row0 + row;
+          if (r < args.M && col < args.N) {
+            const int64_t o = static_cast<int64_t>(r) * N64 + col;
+            *reinterpret_cast<uint4*>(args.dg_out + o) = odg;
+            *reinterpret_cast<uint4*>(args.dfc_out + o) = odfc;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // dg, dfc written by this thread -> visible to the tensor core
+    };
+    auto load_rows = [&](int row0, int col, bool valid, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT],
+                         uint4 (&bfc)[kRPT]) {
+#pragma unroll
+      for (int q = 0; q < kRPT; ++q) {
+        const int row = row0 + rg + 32 * q;
+        if (valid && row < args.M && col < args.N) {  // tails read as zeros
           const int64_t o = static_cast<int64_t>(row) * N64 + col;
           bdy[q] = ldg_stream(args.dy + o);
           bg[q] = ldg_stream(args.g + o);
@@ -405,169 +420,246 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    auto prefetch = [&](int i) {
-      if (i < nst) {
-        const int p0 = MODE == kFX ? i * 64 : n0;
-        const int p1 = MODE == kFX ? m0 : (kb_begin + i) * 64;
-        tma_prefetch_l2_2d(&tm_dy, p0, p1);
-        tma_prefetch_l2_2d(&tm_g, p0, p1);
-        tma_prefetch_l2_2d(&tm_fc, p0, p1);
-      }
-    };
-
-    auto process = [&](int i, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
-      const uint32_t gs = gi + i;  // global A-stage index
-      const int a = gs % kAS;
-      if (!dead && gs >= kAS && !mbar_wait(&s.a_empty[a], ((gs / kAS) - 1) & 1)) {
+    // waits for A slot a to be released by the MMAs of stage st - kAS
+    auto acquire_slot = [&](uint32_t st, int a) {
+      if (!dead && st >= kAS && !mbar_wait(&s.a_empty[a], ((st / kAS) - 1) & 1)) {
         flag_timeout(s, args.status);
         dead = true;
       }
       if (s.abort_flag) dead = true;
-      if (!dead) {
-        const uint32_t sdg = smem_u32(s.aop[a]);
-        const uint32_t sdf = sdg + kHalf;
+    };
+    uint4 xdy[kRPT], xg[kRPT], xfc[kRPT], ydy[kRPT], yg[kRPT], yfc[kRPT];
+
+    if constexpr (MODE == kFX) {
+      // The CTA's stages form one stream over its tiles: stage st is stage
+      // st % nst of the CTA's tile st / nst, and also the global A-stage index.
+      // A tile's epilogue runs after the first kAS - 1 stages of the next tile
+      // are in their A slots, so the tensor core restarts as soon as the
+      // accumulator is drained; the staging buffer of the epilogue's TMA stores
+      // is the A slot of the finished tile's last stage, free once its MMAs are.
+      const int nst = (args.N + 63) / 64;
+      const int ntiles = cluster < args.cluster_tiles ? (args.cluster_tiles - 1 - cluster) / nclusters + 1 : 0;
+      const int total = ntiles * nst;
+      const int look = nst < kAS - 1 ? nst : kAS - 1;
+      auto tile_at = [&](int tix) { return tile_of<MODE, CS>(cluster + tix * nclusters, crank, args); };
+      float ug[8], uf[8];  // column sums, unused here
 #pragma unroll
-        for (int q = 0; q < kRPT; ++q) {
-          const int row = rg + 32 * q;  // row within the tile
-          // 128-byte swizzle: the 16-byte chunk index is XORed with row & 7
-          const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
-          uint4 odg, odfc;
-          grad8_sum(bdy[q], bg[q], bfc[q], odg, odfc, cg, cf);
-          sts128(sdg + off, odg);
-          sts128(sdf + off, odfc);
-          if (want_dg) {
-            const int r = grow(i, q), col = gcol(i);
-            if (r < args.M && col < args.N) {
-              const int64_t o = static_cast<int64_t>(r) * N64 + col;
-              *reinterpret_cast<uint4*>(args.dg_out + o) = odg;
-              *reinterpret_cast<uint4*>(args.dfc_out + o) = odfc;
+      for (int e = 0; e < 8; ++e) ug[e] = uf[e] = 0.0f;
+
+      auto load = [&](int st, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
+        const bool valid = st < total;
+        const int m0 = valid ? tile_at(st / nst).m0 : 0;
+        load_rows(m0, (valid ? (st % nst) * 64 : 0) + c * 8, valid, bdy, bg, bfc);
+      };
+      auto prefetch = [&](int st) {
+        if (st < total) {
+          const int m0 = tile_at(st / nst).m0, p0 = (st % nst) * 64;
+          tma_prefetch_l2_2d(&tm_dy, p0, m0);
+          tma_prefetch_l2_2d(&tm_g, p0, m0);
+          tma_prefetch_l2_2d(&tm_fc, p0, m0);
+        }
+      };
+      auto process = [&](int st, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
+        const int a = st % kAS;
+        acquire_slot(static_cast<uint32_t>(st), a);
+        if (!dead) {
+          const Tile tl = tile_at(st / nst);
+          store_stage(a, tl.m0, (st % nst) * 64 + c * 8, tl.kt == 0 && args.dg_out != nullptr, bdy, bg, bfc, ug,
+                      uf);
+        }
+        mbar_arrive(&s.a_full[a]);
+      };
+      // tile tix's accumulator -> bf16 dx through staging buffer stg (an A slot)
+      auto epilogue = [&](int tix, int stg) {
+        const Tile tl = tile_at(tix);
+        bool acc_ok = false;
+        if (!dead && !s.abort_flag) {
+          acc_ok = mbar_wait(&s.accum, tix & 1);
+          if (!acc_ok) flag_timeout(s, args.status);
+        }
+        const int q = warp & 3;         // TMEM lane quarter this warp may read
+        const int h = (warp - 2) >> 2;  // accumulator half this warp drains
+        tc_fence_after();
+        // tcgen05.ld is warp-collective: decide for the whole warp
+        if (h < tl.nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + cc * 32, v);
+            tmem_ld_wait();
+            // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
+            // store (rows beyond M and columns beyond K are clipped by the copy engine)
+            uint8_t* buf = s.aop[stg] + (warp - 2) * 4096 + (cc & 1) * 2048;
+            if (cc >= 2) {
+              if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+              __syncwarp();
+            }
+            const uint32_t sb = smem_u32(buf) + lane * 64;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), pack8(v + 8 * j));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, buf, tl.k0 + h * 256 + cc * 32, tl.m0 + q * 32);
+              bulk_commit();
             }
           }
         }
-        fence_proxy_async_smem();  // dg, dfc written by this thread -> visible to the tensor core
-      }
-      mbar_arrive(&s.a_full[a]);
-    };
+        tc_fence_before();
+        mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
+        // the staging slot is written again by a later stage: every store has read it
+        if (lane == 0) bulk_wait_read<0>();
+        named_sync_transform();
+      };
+      auto after = [&](int st) {
+        const int tix = st / nst;
+        if (tix >= 1 && st % nst + 1 == look) epilogue(tix - 1, (tix * nst - 1) % kAS);
+      };
 
-    if (t == 0)
-      for (int i = 0; i <= C::kPrefetch; ++i) prefetch(i);
-    uint4 xdy[kRPT], xg[kRPT], xfc[kRPT], ydy[kRPT], yg[kRPT], yfc[kRPT];
-    load(0, xdy, xg, xfc);
-    for (int i = 0; i < nst; i += 2) {
-      // two stages per iteration, alternating register buffers: the loads of the
-      // next stage are in flight while this stage is computed
-      if (t == 0) prefetch(i + 1 + C::kPrefetch);
-      load(i + 1, ydy, yg, yfc);
-      process(i, xdy, xg, xfc);
-      if (i + 1 >= nst) break;
-      if (t == 0) prefetch(i + 2 + C::kPrefetch);
-      load(i + 2, xdy, xg, xfc);
-      process(i + 1, ydy, yg, yfc);
-    }
-
-    gi += nst;
-    const bool acc_ok = mbar_wait(&s.accum, tt & 1);
-    if (!acc_ok) flag_timeout(s, args.status);
-    if (want_db) {
-      // Column sums over the CTA's rows (rows beyond M were read as zeros).
-      // Lanes l, l^8, l^16, l^24 share a chunk; the 8 warps are combined
-      // through the first A slot, idle once accum has fired.
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        cg[e] += __shfl_xor_sync(0xffffffffu, cg[e], 8);
-        cg[e] += __shfl_xor_sync(0xffffffffu, cg[e], 16);
-        cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 8);
-        cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 16);
+      if (t == 0)
+        for (int p = 0; p <= C::kPrefetch; ++p) prefetch(p);
+      load(0, xdy, xg, xfc);
+      for (int st = 0; st < total; st += 2) {
+        // two stages per iteration, alternating register buffers: the loads of the
+        // next stage are in flight while this stage is computed (and while an
+        // epilogue runs)
+        if (t == 0) prefetch(st + 1 + C::kPrefetch);
+        load(st + 1, ydy, yg, yfc);
+        process(st, xdy, xg, xfc);
+        after(st);
+        if (st + 1 >= total) break;
+        if (t == 0) prefetch(st + 2 + C::kPrefetch);
+        load(st + 2, xdy, xg, xfc);
+        process(st + 1, ydy, yg, yfc);
+        after(st + 1);
       }
-      named_sync_transform();
-      float* scratch = reinterpret_cast<float*>(s.aop[0]);  // [8 warps][8 chunks][16]
-      if (lane < 8) {
-        float* pp = scratch + ((warp - 2) * 8 + c) * 16;
+      if (ntiles > 0) epilogue(ntiles - 1, (total - 1) % kAS);
+      if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
+    } else {
+      uint32_t gi = 0, tt = 0;  // A stages, tiles produced
+      for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters, ++tt) {
+        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+        const int n0 = tl.n0, k0 = tl.k0, kb_begin = tl.kb_begin, nst = tl.nst, nh = tl.nh, split = tl.split;
+        const bool want_db = tl.kt == 0 && args.db_part != nullptr;
+        float cg[8], cf[8];  // column sums over the CTA's whole M range
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pp[e] = cg[e];
-          pp[8 + e] = cf[e];
+        for (int e = 0; e < 8; ++e) cg[e] = cf[e] = 0.0f;
+
+        auto load = [&](int i, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
+          load_rows((kb_begin + i) * 64, n0 + c * 8, i < nst, bdy, bg, bfc);
+        };
+        auto prefetch = [&](int i) {
+          if (i < nst) {
+            const int p1 = (kb_begin + i) * 64;
+            tma_prefetch_l2_2d(&tm_dy, n0, p1);
+            tma_prefetch_l2_2d(&tm_g, n0, p1);
+            tma_prefetch_l2_2d(&tm_fc, n0, p1);
+          }
+        };
+        auto process = [&](int i, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
+          const uint32_t gs = gi + i;  // global A-stage index
+          const int a = gs % kAS;
+          acquire_slot(gs, a);
+          if (!dead) store_stage(a, (kb_begin + i) * 64, n0 + c * 8, false, bdy, bg, bfc, cg, cf);
+          mbar_arrive(&s.a_full[a]);
+        };
+
+        if (t == 0)
+          for (int i = 0; i <= C::kPrefetch; ++i) prefetch(i);
+        load(0, xdy, xg, xfc);
+        for (int i = 0; i < nst; i += 2) {
+          if (t == 0) prefetch(i + 1 + C::kPrefetch);
+          load(i + 1, ydy, yg, yfc);
+          process(i, xdy, xg, xfc);
+          if (i + 1 >= nst) break;
+          if (t == 0) prefetch(i + 2 + C::kPrefetch);
+          load(i + 2, xdy, xg, xfc);
+          process(i + 1, ydy, yg, yfc);
         }
-      }
-      named_sync_transform();
-      if (t < 128) {
-        const int which = t >> 6;  // 0: dg, 1: dfc
-        const int col = t & 63;
-        const int gc = n0 + col;
-        if (!dead && acc_ok && gc < args.N) {
-          float v = 0.0f;
-#pragma unroll
-          for (int w = 0; w < 8; ++w) v += scratch[(w * 8 + (col >> 3)) * 16 + which * 8 + (col & 7)];
-          args.db_part[static_cast<int64_t>(split) * 2 * args.N + which * args.N + gc] = v;
-        }
-      }
-    }
 
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    tc_fence_after();
-    const int r = q * 32 + lane;    // accumulator row (TMEM lane)
-    const int h = (warp - 2) >> 2;  // accumulator half this warp drains
-    // tcgen05.ld is warp-collective: decide for the whole warp
-    if (h < nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag && nst > 0)) {
+        gi += nst;
+        bool acc_ok = false;
+        if (!dead && !s.abort_flag) {
+          acc_ok = mbar_wait(&s.accum, tt & 1);
+          if (!acc_ok) flag_timeout(s, args.status);
+        }
+        if (want_db) {
+          // Column sums over the CTA's rows (rows beyond M were read as zeros).
+          // Lanes l, l^8, l^16, l^24 share a chunk; the 8 warps are combined
+          // through the first A slot, idle once accum has fired.
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            cg[e] += __shfl_xor_sync(0xffffffffu, cg[e], 8);
+            cg[e] += __shfl_xor_sync(0xffffffffu, cg[e], 16);
+            cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 8);
+            cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 16);
+          }
+          named_sync_transform();
+          float* scratch = reinterpret_cast<float*>(s.aop[0]);  // [8 warps][8 chunks][16]
+          if (lane < 8) {
+            float* pp = scratch + ((warp - 2) * 8 + c) * 16;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              pp[e] = cg[e];
+              pp[8 + e] = cf[e];
+            }
+          }
+          named_sync_transform();
+          if (t < 128) {
+            const int which = t >> 6;  // 0: dg, 1: dfc
+            const int col = t & 63;
+            const int gc = n0 + col;
+            if (!dead && acc_ok && gc < args.N) {
+              float v = 0.0f;
+#pragma unroll
+              for (int w = 0; w < 8; ++w) v += scratch[(w * 8 + (col >> 3)) * 16 + which * 8 + (col & 7)];
+              args.db_part[static_cast<int64_t>(split) * 2 * args.N + which * args.N + gc] = v;
+            }
+          }
+          named_sync_transform();  // the scratch is read before a later tile's stage reuses the slot
+        }
+
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        tc_fence_after();
+        const int r = q * 32 + lane;    // accumulator row (TMEM lane)
+        const int h = (warp - 2) >> 2;  // accumulator half this warp drains
+        // tcgen05.ld is warp-collective: decide for the whole warp
+        if (h < nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag && nst > 0)) {
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + cc * 32, v);
-        tmem_ld_wait();
-        const int kcol = k0 + h * 256 + cc * 32;
-        if (MODE == kFX) {
-          // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
-          // store (rows beyond M and columns beyond K are clipped by the copy engine)
-          uint8_t* buf = s.aop[0] + (warp - 2) * 4096 + (cc & 1) * 2048;
-          if (cc >= 2) {
-            if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
-            __syncwarp();
-          }
-          const uint32_t sb = smem_u32(buf) + lane * 64;
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + cc * 32, v);
+            tmem_ld_wait();
+            const int kcol = k0 + h * 256 + cc * 32;
+            const int prob = r >> 6;  // lanes 0-63: dw_g, 64-127: dw_fc
+            const int n = n0 + (r & 63);
+            if (n < args.N) {
+              if (args.splits == 1) {
+                uint16_t* dst = (prob ? args.dw_fc : args.dw_g) + n;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), pack8(v + 8 * j));
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_out, buf, kcol, m0 + q * 32);
-            bulk_commit();
-          }
-        } else {
-          const int prob = r >> 6;  // lanes 0-63: dw_g, 64-127: dw_fc
-          const int n = n0 + (r & 63);
-          if (n < args.N) {
-            if (args.splits == 1) {
-              uint16_t* dst = (prob ? args.dw_fc : args.dw_g) + n;
-#pragma unroll 8
-              for (int e = 0; e < 32; ++e) {
-                const int k = kcol + e;
-                if (k < args.K) {
-                  const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
-                  dst[static_cast<int64_t>(k) * args.N] = *reinterpret_cast<const uint16_t*>(&b);
+                for (int e = 0; e < 32; ++e) {
+                  const int k = kcol + e;
+                  if (k < args.K) {
+                    const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
+                    dst[static_cast<int64_t>(k) * args.N] = *reinterpret_cast<const uint16_t*>(&b);
+                  }
+                }
+              } else {
+                float* dst = args.ws + static_cast<int64_t>(split * 2 + prob) * args.K * args.N + n;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const int k = kcol + e;
+                  if (k < args.K) dst[static_cast<int64_t>(k) * args.N] = __uint_as_float(v[e]);
                 }
               }
-            } else {
-              float* dst = args.ws + static_cast<int64_t>(split * 2 + prob) * args.K * args.N + n;
-#pragma unroll 8
-              for (int e = 0; e < 32; ++e) {
-                const int k = kcol + e;
-                if (k < args.K) dst[static_cast<int64_t>(k) * args.N] = __uint_as_float(v[e]);
-              }
             }
           }
         }
-      }
+        tc_fence_before();
+        mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
+      }  // tile loop
     }
-    tc_fence_before();
-    mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
-    if (MODE == kFX) {
-      // the next tile's transform reuses the A slots that stage these stores
-      if (lane == 0) bulk_wait_read<0>();
-      named_sync_transform();
-    }
-    }  // tile loop
-    if (MODE == kFX && lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
   }
 
   __syncthreads();
