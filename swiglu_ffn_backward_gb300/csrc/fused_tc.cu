@@ -56,7 +56,7 @@ enum FusedMode : int { kFX = 0, kFW = 1 };
 
 constexpr int kThreads = 320;
 constexpr int kXThreads = 256;  // transform / epilogue threads (warps 2-9)
-constexpr int kClusterX = 2;    // CTAs sharing each W chunk in the fused x kernel
+constexpr int kClusterX = 4;    // CTAs sharing each W chunk in the fused x kernel (measured: 3% over 2)
 constexpr int kClusterW = 4;    // CTAs sharing each x chunk in the fused w kernel
 constexpr uint32_t kTmemCols = 512;
 
