@@ -304,6 +304,28 @@ def run_ours(args, rank, world):
     sw_gbs = 3.0 * SWISH_N * 2 / (sw_ms * 1e-3) / 1e9
     del sets
 
+    # accumulate mode: the public whole-backward call (fused chain, dg/dfc not
+    # returned) with and without SWG_ACCUMULATE, device-resident inputs
+    acc_outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
+    acc_ws = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 1), 16), dtype=torch.uint8, device=dev)
+
+    def acc_call(acc):
+        swg.swiglu_bwd(**inp, fused=True, return_dg=False, out=acc_outs, workspace=acc_ws, accumulate=acc)
+
+    acc_ms = {}
+    for acc in (False, True):
+        for _ in range(3):
+            acc_call(acc)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(20):
+            acc_call(acc)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        acc_ms["accumulate" if acc else "overwrite"] = round(a0.elapsed_time(a1) / 20, 4)
+    swg.swg_check()
+
     # e2e: host buffers in pinned memory, H2D of every input and D2H of the
     # results inside the timed region, through the public swiglu_bwd call
     host_in = {k: v.cpu().pin_memory() for k, v in inp.items()}
@@ -358,6 +380,7 @@ def run_ours(args, rank, world):
                        "stages": describe(per_other)},
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
                        "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
+        "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "call": f"swiglu_bwd ({args.path}, dg/dfc not returned)"},
         "gpu_launches": launches[args.path] * args.steps,

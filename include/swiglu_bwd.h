@@ -73,6 +73,15 @@ typedef enum { SWG_F32 = 0, SWG_F16 = 1, SWG_BF16 = 2 } swg_dtype;
 #define SWG_UNFUSED 0u /* b stage, then the w and x GEMMs on the stored dg, dfc */
 #define SWG_FUSED 1u   /* the GEMMs recompute dg, dfc from dy, g, fc in their
                           operand producer; dg, dfc never round-trip HBM */
+/* Accumulate mode ([P1] "Kernel signatures": the pages' b and w kernels add
+ * their db and dw into outputs the caller has zeroed, so that several
+ * micro-batches can be summed). With SWG_ACCUMULATE, db_g, db_fc, dw_g and
+ * dw_fc are read and replaced by bf16(old + this call's sum): the fp32 (db:
+ * fp64) sum and the old value are added before the single rounding. dx, dg and
+ * dfc are still overwritten. With M == 0 the four outputs are left unchanged.
+ * Without the flag every output is overwritten (the same result as the pages'
+ * zero-then-accumulate on zeroed outputs). */
+#define SWG_ACCUMULATE 2u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* swg_status_string(swg_status s);
@@ -164,6 +173,7 @@ swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, cons
 
 /* ---- whole backward ----------------------------------------------------------
  * [P1] "Kernel overview and call chain": b, then w and x on b's dg, dfc.
+ * flags: SWG_UNFUSED or SWG_FUSED, optionally | SWG_ACCUMULATE.
  * dg, dfc are optional outputs: pass NULL to skip them. With SWG_UNFUSED and
  * NULL dg/dfc, the workspace holds them (4*M*N bytes more). With SWG_FUSED the
  * call runs swiglu_bwd_x_fused then swiglu_bwd_w_fused: the w and x GEMMs

@@ -7,6 +7,7 @@ include/swiglu_bwd.h; this package is the thin Python binding over it.
 from ._binding import (  # noqa: F401
     EXPORTS,
     LIB_PATH,
+    SWG_ACCUMULATE,
     SWG_FUSED,
     SWG_UNFUSED,
     SwgError,

@@ -32,6 +32,7 @@ _DTYPE = {torch.float32: SWG_F32, torch.float16: SWG_F16, torch.bfloat16: SWG_BF
 # flags
 SWG_UNFUSED = 0
 SWG_FUSED = 1
+SWG_ACCUMULATE = 2
 SWG_WS_DG_GIVEN = 0x100
 
 EXPORTS = (
@@ -241,9 +242,11 @@ def swiglu_bwd_x(dg, dfc, w_g, w_fc, dx=None, stream=None):
 
 
 def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = True,
-               out: dict | None = None, workspace=None, stream=None) -> dict:
+               out: dict | None = None, workspace=None, stream=None, accumulate: bool = False) -> dict:
     """The whole backward. Returns a dict with dx, dw_g, dw_fc, db_g, db_fc
-    (and dg, dfc when return_dg). `out` may supply any of those tensors."""
+    (and dg, dfc when return_dg). `out` may supply any of those tensors.
+    accumulate=True adds this call's db and dw into out's db_g, db_fc, dw_g,
+    dw_fc (which must then be given) instead of overwriting them."""
     x, w_g, w_fc, dy, g, fc = (_dev_bf16(t, n) for t, n in (
         (x, "x"), (w_g, "w_g"), (w_fc, "w_fc"), (dy, "dy"), (g, "g"), (fc, "fc")))
     M, K = x.shape
@@ -253,13 +256,15 @@ def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = T
         if tuple(t.shape) != shp:
             raise ValueError(f"{n} must have shape {shp}, got {tuple(t.shape)}")
     out = dict(out or {})
+    if accumulate and any(out.get(k) is None for k in ("dw_g", "dw_fc", "db_g", "db_fc")):
+        raise ValueError("accumulate=True needs dw_g, dw_fc, db_g and db_fc in `out`")
     shapes = dict(dx=(M, K), dw_g=(K, N), dw_fc=(K, N), db_g=(1, N), db_fc=(1, N))
     if return_dg:
         shapes.update(dg=(M, N), dfc=(M, N))
     for k, shp in shapes.items():
         if out.get(k) is None:
             out[k] = torch.empty(shp, dtype=torch.bfloat16, device=x.device)
-    flags = SWG_FUSED if fused else SWG_UNFUSED
+    flags = (SWG_FUSED if fused else SWG_UNFUSED) | (SWG_ACCUMULATE if accumulate else 0)
     ws_flags = flags | (SWG_WS_DG_GIVEN if return_dg else 0)
     ws = _workspace(lib.swiglu_bwd_workspace_size(M, K, N, ws_flags), x.device, workspace)
     _check(lib.swiglu_bwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dy.data_ptr(), g.data_ptr(),

@@ -303,7 +303,8 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
                       const void* fc, void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc, void* db_g,
                       void* db_fc, int64_t M, int64_t K, int64_t N, unsigned flags, void* workspace,
                       size_t workspace_bytes, swg_stream_t stream) {
-  if ((flags & ~(SWG_FUSED | SWG_WS_DG_GIVEN)) != 0) return SWG_ERR_PARAM_INVALID;
+  if ((flags & ~(SWG_FUSED | SWG_ACCUMULATE | SWG_WS_DG_GIVEN)) != 0) return SWG_ERR_PARAM_INVALID;
+  const bool acc = (flags & SWG_ACCUMULATE) != 0;
   swg_status st = check_shape(M, K, N);
   if (st != SWG_OK) return st;
   if (K == 0 || N == 0) return SWG_OK;
@@ -325,6 +326,7 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
   if (st != SWG_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M == 0) {
+    if (acc) return SWG_OK;  // a sum over no rows adds nothing
     st = zero_bf16(dw_g, K * N, s);
     if (st == SWG_OK) st = zero_bf16(dw_fc, K * N, s);
     if (st == SWG_OK) st = zero_bf16(db_g, N, s);
@@ -349,7 +351,8 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
     e = swg::launch_fused_w(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
                             static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
                             static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
-                            static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, wp, fplan, s);
+                            static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, wp, fplan, s,
+                            acc);
     return cuda_status(e);
   }
   uint16_t* dgp = static_cast<uint16_t*>(dg);
@@ -367,10 +370,10 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
 
   cudaError_t e = swg::launch_b_stage(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g),
                                       static_cast<const uint16_t*>(fc), dgp, dfcp, static_cast<uint16_t*>(db_g),
-                                      static_cast<uint16_t*>(db_fc), M, N, bws, s);
+                                      static_cast<uint16_t*>(db_fc), M, N, bws, s, acc);
   if (e != cudaSuccess) return SWG_ERR_CUDA;
   e = swg::launch_w_gemm(static_cast<const uint16_t*>(x), dgp, dfcp, static_cast<uint16_t*>(dw_g),
-                         static_cast<uint16_t*>(dw_fc), M, K, N, wws, plan, s);
+                         static_cast<uint16_t*>(dw_fc), M, K, N, wws, plan, s, acc);
   if (e != cudaSuccess) return SWG_ERR_CUDA;
   e = swg::launch_x_gemm(dgp, dfcp, static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc),
                          static_cast<uint16_t*>(dx), M, K, N, s);

@@ -137,12 +137,13 @@ __global__ void __launch_bounds__(kThreads) b_stage_kernel(const uint4* __restri
   }
 }
 
-// db[j] = sum_c partials[c][j], j over the 2N columns (dg's then dfc's).
+// db[j] = sum_c partials[c][j], j over the 2N columns (dg's then dfc's); with
+// accumulate, the existing db value joins the fp64 sum before the one rounding.
 // Block: 32 columns x 32 chunk lanes; lane ty sums chunks ty, ty+32, ... in
 // order, then ty 0..31 are added in order: a fixed summation tree.
 __global__ void __launch_bounds__(1024) db_reduce_kernel(const float* __restrict__ partials, int64_t chunks,
                                                          int64_t N, uint16_t* __restrict__ db_g,
-                                                         uint16_t* __restrict__ db_fc) {
+                                                         uint16_t* __restrict__ db_fc, int accumulate) {
   __shared__ double acc[32][33];
   const int tx = threadIdx.x & 31;
   const int ty = threadIdx.x >> 5;
@@ -157,12 +158,10 @@ __global__ void __launch_bounds__(1024) db_reduce_kernel(const float* __restrict
   if (ty == 0 && j < two_n) {
     double t = 0.0;
     for (int k = 0; k < 32; ++k) t += acc[k][tx];
+    uint16_t* dst = j < N ? db_g + j : db_fc + (j - N);
+    if (accumulate) t += static_cast<double>(__uint_as_float(static_cast<uint32_t>(*dst) << 16));
     const __nv_bfloat16 b = __double2bfloat16(t);
-    const uint16_t bits = *reinterpret_cast<const uint16_t*>(&b);
-    if (j < N)
-      db_g[j] = bits;
-    else
-      db_fc[j - N] = bits;
+    *dst = *reinterpret_cast<const uint16_t*>(&b);
   }
 }
 
@@ -190,14 +189,16 @@ size_t b_workspace_bytes(int64_t M, int64_t N) {
 }
 
 cudaError_t launch_db_reduce(const float* partials, int64_t chunks, int64_t N, uint16_t* db_g, uint16_t* db_fc,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool accumulate) {
   const int64_t blocks = (2 * N + 31) / 32;
-  db_reduce_kernel<<<static_cast<unsigned>(blocks), 1024, 0, stream>>>(partials, chunks, N, db_g, db_fc);
+  db_reduce_kernel<<<static_cast<unsigned>(blocks), 1024, 0, stream>>>(partials, chunks, N, db_g, db_fc,
+                                                                       accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_b_stage(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, uint16_t* dg, uint16_t* dfc,
-                           uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t N, void* ws, cudaStream_t stream) {
+                           uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t N, void* ws, cudaStream_t stream,
+                           bool accumulate) {
   const BPlan p = b_plan(M, N);
   float* partials = static_cast<float*>(ws);
   dim3 grid(static_cast<unsigned>((N + kCols - 1) / kCols), static_cast<unsigned>(p.chunks));
@@ -212,7 +213,7 @@ cudaError_t launch_b_stage(const uint16_t* dy, const uint16_t* g, const uint16_t
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_db_reduce(partials, p.chunks, N, db_g, db_fc, stream);
+  return launch_db_reduce(partials, p.chunks, N, db_g, db_fc, stream, accumulate);
 }
 
 }  // namespace swg

@@ -115,6 +115,7 @@ struct FusedArgs {
   int splits, kb_per, nkb_total, tiles_n;
   int x3d;  // x entries come from one 3-D box (else 2-D boxes)
   int cluster_tiles;  // work items of CS CTAs; cluster c takes c, c + nclusters, ...
+  int accumulate;     // FW: dw, db += this call's sums (one rounding of old + new)
   int mtiles;         // FX: 128-row tiles of M
 };
 
@@ -641,8 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                   const int k = kcol + e;
                   if (k < args.K) {
-                    const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
-                    dst[static_cast<int64_t>(k) * args.N] = *reinterpret_cast<const uint16_t*>(&b);
+                    uint16_t* d = dst + static_cast<int64_t>(k) * args.N;
+                    float val = __uint_as_float(v[e]);
+                    if (args.accumulate) val += __uint_as_float(static_cast<uint32_t>(*d) << 16);
+                    const __nv_bfloat16 b = __float2bfloat16_rn(val);
+                    *d = *reinterpret_cast<const uint16_t*>(&b);
                   }
                 }
               } else {
@@ -766,7 +770,7 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
 
 cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                            uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
-                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream) {
+                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
   CUtensorMap mdy, mg, mfc, mx2, mx3;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 64) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 64) ||
@@ -803,14 +807,15 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   a.nkb_total = static_cast<int>((M + 63) / 64);
   a.tiles_n = static_cast<int>(((N + 63) / 64 + CS - 1) / CS * CS);  // clusters of CS n tiles
   a.x3d = x3d;
+  a.accumulate = accumulate ? 1 : 0;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
   cudaError_t e = launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {
-    e = launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream);
+    e = launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
     if (e != cudaSuccess) return e;
   }
-  return launch_db_reduce(a.db_part, plan.splits, N, db_g, db_fc, stream);
+  return launch_db_reduce(a.db_part, plan.splits, N, db_g, db_fc, stream, accumulate);
 }
 
 }  // namespace swg

@@ -77,6 +77,7 @@ struct GemmArgs {
   float* ws;
   int splits, kb_per, nkb_total;
   int tiles_kw, tiles_nw;  // dw tile grid per problem
+  int accumulate;          // dw += this call's sums (one rounding of old + new)
 };
 
 __device__ __forceinline__ void flag_timeout(Smem& s) {
@@ -234,11 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 if (col + 8 * j < args.N) {
-                  dst[j] =
-                      make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                                 pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                 pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                 pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                  float f[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[8 * j + e]);
+                  if (args.accumulate) {
+                    const uint4 o = dst[j];
+                    dst[j] = make_uint4(add_pack_bf16x2(f[0], f[1], o.x), add_pack_bf16x2(f[2], f[3], o.y),
+                                        add_pack_bf16x2(f[4], f[5], o.z), add_pack_bf16x2(f[6], f[7], o.w));
+                  } else {
+                    dst[j] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                        pack_bf16x2(f[6], f[7]));
+                  }
                 }
               }
             } else {
@@ -271,10 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// dw[p][k][n] = sum_s ws[s][p][k][n] (fixed order), rounded once to bf16.
+// dw[p][k][n] = sum_s ws[s][p][k][n] (fixed order), rounded once to bf16; with
+// accumulate, the existing dw value is added to the fp32 sum before that rounding.
 __global__ void __launch_bounds__(256) w_split_reduce_kernel(const float4* __restrict__ ws, int splits,
                                                              int64_t per_prob4, uint2* __restrict__ dw_g,
-                                                             uint2* __restrict__ dw_fc) {
+                                                             uint2* __restrict__ dw_fc, int accumulate) {
   const int64_t total4 = 2 * per_prob4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -286,11 +294,13 @@ __global__ void __launch_bounds__(256) w_split_reduce_kernel(const float4* __res
       acc.z += v.z;
       acc.w += v.w;
     }
-    const uint2 o = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    if (i < per_prob4)
-      dw_g[i] = o;
-    else
-      dw_fc[i - per_prob4] = o;
+    uint2* dst = i < per_prob4 ? dw_g + i : dw_fc + (i - per_prob4);
+    if (accumulate) {
+      const uint2 old = *dst;
+      *dst = make_uint2(add_pack_bf16x2(acc.x, acc.y, old.x), add_pack_bf16x2(acc.z, acc.w, old.y));
+    } else {
+      *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
   }
 }
 
@@ -400,7 +410,7 @@ cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_
 
 cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
                           uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool accumulate) {
   CUtensorMap a0, b0, b1;
   if (!encode_tmap_2d_bf16(&a0, x, K, M, static_cast<uint64_t>(K) * 2, 64, BK) ||
       !encode_tmap_2d_bf16(&b0, dg, N, M, static_cast<uint64_t>(N) * 2, 64, BK) ||
@@ -418,23 +428,24 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
   a.nkb_total = static_cast<int>((M + BK - 1) / BK);
   a.tiles_kw = static_cast<int>((K + BM - 1) / BM);
   a.tiles_nw = static_cast<int>((N + BN - 1) / BN);
+  a.accumulate = accumulate ? 1 : 0;
   const int64_t ctas = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
   cudaError_t e = prepare_kernel<kModeW>();
   if (e != cudaSuccess) return e;
   tc_gemm_kernel<kModeW><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(a0, a0, b0, b1, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.splits == 1) return e;
-  return launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream);
+  return launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
 }
 
 cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
-                                  uint16_t* dw_fc, cudaStream_t stream) {
+                                  uint16_t* dw_fc, cudaStream_t stream, bool accumulate) {
   const int64_t per_prob4 = K * N / 4;
   int64_t blocks = (2 * per_prob4 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   w_split_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       reinterpret_cast<const float4*>(ws), static_cast<int>(splits), per_prob4, reinterpret_cast<uint2*>(dw_g),
-      reinterpret_cast<uint2*>(dw_fc));
+      reinterpret_cast<uint2*>(dw_fc), accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,12 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
+// accumulate mode: (fp32 a, b) + the two bf16 of an existing output word, rounded once
+__device__ __forceinline__ uint32_t add_pack_bf16x2(float a, float b, uint32_t old) {
+  const float2 o = bf16x2_to_f2(old);
+  return pack_bf16x2(a + o.x, b + o.y);
+}
+
 // b-stage math for two elements (fp32): dg = dy*fc*s*(1+g*(1-s)), dfc = dy*g*s
 __device__ __forceinline__ void swiglu_grad_pair(float2 dy, float2 g, float2 fc, float2& dg, float2& dfc) {
   const Sig2 q = sigmoid_pair2(g);

@@ -21,11 +21,13 @@ struct BPlan {
 BPlan b_plan(int64_t M, int64_t N);
 size_t b_workspace_bytes(int64_t M, int64_t N);
 // dg/dfc may be null (then only the column sums are produced)
+// accumulate: db_g, db_fc += the column sums (one rounding of old + new); default: overwrite
 cudaError_t launch_b_stage(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, uint16_t* dg, uint16_t* dfc,
-                           uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t N, void* ws, cudaStream_t stream);
+                           uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t N, void* ws, cudaStream_t stream,
+                           bool accumulate = false);
 // db from fp32 partials [chunks][2N] -> bf16 db_g, db_fc (fixed order)
 cudaError_t launch_db_reduce(const float* partials, int64_t chunks, int64_t N, uint16_t* db_g, uint16_t* db_fc,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool accumulate = false);
 // 3-D tensor-map encoding (dims/strides innermost first; strides[i] is the byte stride of dim i+1)
 bool encode_tmap_3d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                          const uint32_t box[3], int swizzle_bytes);
@@ -43,7 +45,7 @@ cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_
                           uint16_t* dx, int64_t M, int64_t K, int64_t N, cudaStream_t stream);
 cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
                           uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool accumulate = false);
 
 // module status word (timeouts)
 cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream);
@@ -64,9 +66,9 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
 // dw and db from x, dy, g, fc; ws holds the split-M dw partials, then the db partials
 cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                            uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
-                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream);
+                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate = false);
 cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
-                                  uint16_t* dw_fc, cudaStream_t stream);
+                                  uint16_t* dw_fc, cudaStream_t stream, bool accumulate = false);
 
 // tensor-map encoding (driver entry point resolved once)
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
