@@ -326,6 +326,33 @@ def run_ours(args, rank, world):
         acc_ms["accumulate" if acc else "overwrite"] = round(a0.elapsed_time(a1) / 20, 4)
     swg.swg_check()
 
+    # forward (g, fc, y from x, W, b) at the same shape: one launch
+    from synth import swiglu_fwd_biases
+    fb_g, fb_fc = swiglu_fwd_biases(shape, device=dev)
+    fout = {k: torch.empty((M, N), **bf) for k in ("g", "fc", "y")}
+
+    def fwd_call():
+        swg.swiglu_fwd(inp["x"], inp["w_g"], inp["w_fc"], fb_g, fb_fc, out=fout)
+
+    for _ in range(3):
+        fwd_call()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(30):
+        fwd_call()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    swg.swg_check()
+    fwd_ms = f0.elapsed_time(f1) / 30
+    fwd_flop = 4.0 * M * K * N
+    fwd_bytes = 2.0 * M * K + 4.0 * K * N + 4.0 * N + 6.0 * M * N
+    fwd_roof = max(fwd_flop / (pk["bf16"] * 1e12), fwd_bytes / (pk["hbm"] * 1e9)) * 1e3
+    fwd = {"ms": round(fwd_ms, 4), "tflops": round(fwd_flop / (fwd_ms * 1e-3) / 1e12, 1),
+           "gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1), "roofline_ms": round(fwd_roof, 4),
+           "pct_roofline": round(fwd_roof / fwd_ms, 4)}
+    del fout
+
     # e2e: host buffers in pinned memory, H2D of every input and D2H of the
     # results inside the timed region, through the public swiglu_bwd call
     host_in = {k: v.cpu().pin_memory() for k, v in inp.items()}
@@ -381,6 +408,7 @@ def run_ours(args, rank, world):
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
                        "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
         "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
+        "swiglu_fwd": fwd,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "call": f"swiglu_bwd ({args.path}, dg/dfc not returned)"},
         "gpu_launches": launches[args.path] * args.steps,

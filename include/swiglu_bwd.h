@@ -171,6 +171,21 @@ swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, cons
                               int64_t M, int64_t K, int64_t N,
                               void* workspace, size_t workspace_bytes, swg_stream_t stream);
 
+/* ---- forward ----------------------------------------------------------------
+ * [P1] "Operator background" (the forward whose outputs the backward takes):
+ *   g  = x W_g + b_g,   fc = x W_fc + b_fc      (g, fc [M,N])
+ *   y  = SiLU(g) * fc = g * sigma(g) * fc        (y [M,N])
+ * x [M,K], w_g/w_fc [K,N], b_g/b_fc [N] (NULL: no bias), all bf16 row-major.
+ * One tcgen05 GEMM launch (fp32 accumulation) computes both products; g, fc
+ * are formed in fp32 with the bias and y from those fp32 values; each output
+ * is rounded once to bf16 (round to nearest even). K must be positive
+ * (K == 0: SWG_ERR_UNSUPPORTED); M == 0 or N == 0: nothing is launched.
+ * Outputs must not overlap the inputs or each other (SWG_ERR_PARAM_INVALID);
+ * no workspace. */
+swg_status swiglu_fwd(const void* x, const void* w_g, const void* w_fc,
+                      const void* b_g, const void* b_fc, void* g, void* fc, void* y,
+                      int64_t M, int64_t K, int64_t N, swg_stream_t stream);
+
 /* ---- whole backward ----------------------------------------------------------
  * [P1] "Kernel overview and call chain": b, then w and x on b's dg, dfc.
  * flags: SWG_UNFUSED or SWG_FUSED, optionally | SWG_ACCUMULATE.

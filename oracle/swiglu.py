@@ -59,10 +59,11 @@ def silu_grad(z) -> np.ndarray:
 
 
 def swiglu_fwd(x, w_g, w_fc, b_g=None, b_fc=None):
-    """Forward of the FFN gate ("Operator background"); returns (g, fc, y).
+    """Forward of the FFN gate ("Operator background"); returns (g, fc, y):
+    g = x W_g + b_g, fc = x W_fc + b_fc, y = SiLU(g) * fc, in fp64.
 
-    Used only by the pins (finite differences of the forward), never as an
-    input producer for parity.
+    The reference for the forward kernel's parity tests; never an input
+    producer for the backward's parity tests (those draw g, fc directly).
     """
     x = np.asarray(x, np.float64)
     g = x @ np.asarray(w_g, np.float64)

@@ -24,5 +24,6 @@ from ._binding import (  # noqa: F401
     swiglu_bwd_w_fused_workspace_size,
     swiglu_bwd_x,
     swiglu_bwd_x_fused,
+    swiglu_fwd,
     swish_grad,
 )

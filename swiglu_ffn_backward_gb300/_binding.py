@@ -45,6 +45,7 @@ EXPORTS = (
     "swiglu_bwd_b_noalloc",
     "swiglu_bwd_x_fused",
     "swiglu_bwd_w_fused_workspace_size", "swiglu_bwd_w_fused",
+    "swiglu_fwd",
 )
 
 
@@ -76,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_bwd_w.restype = st
     lib.swiglu_bwd_x.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     lib.swiglu_bwd_x.restype = st
+    lib.swiglu_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, P]
+    lib.swiglu_fwd.restype = st
     lib.swiglu_bwd_workspace_size.argtypes = [I64, I64, I64, U]
     lib.swiglu_bwd_workspace_size.restype = SZ
     lib.swiglu_bwd.argtypes = [P] * 13 + [I64, I64, I64, U, P, SZ, P]
@@ -239,6 +242,32 @@ def swiglu_bwd_x(dg, dfc, w_g, w_fc, dx=None, stream=None):
     _check(lib.swiglu_bwd_x(dg.data_ptr(), dfc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dx.data_ptr(),
                             M, K, N, _stream(stream)), "swiglu_bwd_x")
     return dx
+
+
+def swiglu_fwd(x, w_g, w_fc, b_g=None, b_fc=None, out: dict | None = None, stream=None) -> dict:
+    """Forward: returns dict g = x W_g + b_g, fc = x W_fc + b_fc, y = SiLU(g) * fc
+    (all [M, N] bf16); b_g, b_fc ([N] or [1, N]) may be None. `out` may supply
+    any of g, fc, y."""
+    x, w_g, w_fc = (_dev_bf16(t, n) for t, n in ((x, "x"), (w_g, "w_g"), (w_fc, "w_fc")))
+    M, K = x.shape
+    N = w_g.shape[1]
+    if w_g.shape != (K, N) or w_fc.shape != (K, N):
+        raise ValueError("shape mismatch: x [M, K]; w_g, w_fc [K, N]")
+    biases = []
+    for b, n in ((b_g, "b_g"), (b_fc, "b_fc")):
+        if b is not None:
+            b = _dev_bf16(b, n)
+            if b.numel() != N:
+                raise ValueError(f"{n} must have N = {N} elements")
+        biases.append(b)
+    out = dict(out or {})
+    for k in ("g", "fc", "y"):
+        if out.get(k) is None:
+            out[k] = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib.swiglu_fwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), _ptr(biases[0]), _ptr(biases[1]),
+                          out["g"].data_ptr(), out["fc"].data_ptr(), out["y"].data_ptr(), M, K, N,
+                          _stream(stream)), "swiglu_fwd")
+    return out
 
 
 def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = True,

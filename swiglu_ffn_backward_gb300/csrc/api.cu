@@ -220,6 +220,31 @@ swg_status swiglu_bwd_x(const void* dg, const void* dfc, const void* w_g, const 
                                         static_cast<uint16_t*>(dx), M, K, N, s));
 }
 
+// ---------------------------------------------------------------- forward
+swg_status swiglu_fwd(const void* x, const void* w_g, const void* w_fc, const void* b_g, const void* b_fc, void* g,
+                      void* fc, void* y, int64_t M, int64_t K, int64_t N, swg_stream_t stream) {
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (K == 0) return SWG_ERR_UNSUPPORTED;  // the products need a reduction of positive length
+  if (M == 0 || N == 0) return SWG_OK;
+  if (!x || !w_g || !w_fc || !g || !fc || !y) return SWG_ERR_NULLPTR;
+  const void* all[] = {x, w_g, w_fc, b_g, b_fc, g, fc, y};  // null biases count as aligned
+  for (const void* p : all)
+    if (!aligned16(p)) return SWG_ERR_UNSUPPORTED;
+  const int64_t mn = M * N * 2, kn = K * N * 2;
+  const Range outs[] = {rng(g, mn), rng(fc, mn), rng(y, mn)};
+  const Range ins[] = {rng(x, M * K * 2), rng(w_g, kn), rng(w_fc, kn), rng(b_g, b_g ? N * 2 : 0),
+                       rng(b_fc, b_fc ? N * 2 : 0)};
+  if (any_overlap(outs, 3, ins, 5)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(swg::launch_fwd_gemm(
+      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc),
+      static_cast<const uint16_t*>(b_g), static_cast<const uint16_t*>(b_fc), static_cast<uint16_t*>(g),
+      static_cast<uint16_t*>(fc), static_cast<uint16_t*>(y), M, K, N, s));
+}
+
 // ---------------------------------------------------------------- fused stages
 swg_status swiglu_bwd_x_fused(const void* dy, const void* g, const void* fc, const void* w_g, const void* w_fc,
                               void* dx, void* dg, void* dfc, int64_t M, int64_t K, int64_t N, swg_stream_t stream) {

@@ -1,0 +1,300 @@
+// Forward of the SwiGLU FFN gate, the producer of the backward's inputs:
+//   g = x W_g + b_g,  fc = x W_fc + b_fc,  y = SiLU(g) * fc = g * sigma(g) * fc
+// Source: "PyPTO-Gym in practice: the fused SwiGLU backward operator",
+// "Operator background" (the forward the backward kernels differentiate).
+// bf16 operands, fp32 accumulation in TMEM; g and fc are formed in fp32 with
+// the bias, y from those fp32 values, and each output is rounded once to bf16.
+//
+// One persistent tcgen05 GEMM, one CTA per SM, six warps:
+//   warp 0 lane 0   TMA producer: for every 64-wide block of K, the x tile
+//                   [128 m x 64 k] (K-major) and the W_g, W_fc tiles
+//                   [64 k x 128 n] (MN-major, two 64x64 boxes each) into a
+//                   4-deep ring, running across the CTA's tiles
+//   warp 1          TMEM allocation (512 columns = two accumulator buffers,
+//                   each g [128 x 128] | fc [128 x 128]); lane 0 issues
+//                   tcgen05.mma (M=128, N=128, K=16): each x step feeds both
+//                   products
+//   warps 2-5       epilogue: drain the finished buffer while the tensor core
+//                   fills the other one: bias, SiLU, and per 32x32 block one
+//                   TMA store per output from a 64-byte-swizzled staging
+//                   buffer (the copy engine clips rows beyond M and columns
+//                   beyond N)
+// The CTA loops over output tiles [128 rows x 128 columns]; with K = 512 a
+// tile holds only eight K blocks, so the double-buffered accumulator is what
+// keeps the tensor core busy across tile boundaries.
+//
+// Every mbarrier wait is bounded; a timeout sets the module status word,
+// stops issuing, drains the CTA's own TMA copies, frees TMEM and returns.
+#include "swg_device.cuh"
+#include "swg_launch.h"
+
+namespace swg {
+namespace {
+
+constexpr int BM = 128;   // rows of a tile
+constexpr int BN = 128;   // columns of n per product in a tile
+constexpr int BK = 64;    // reduction block
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = 2 * BN * BK * 2;   // W_g | W_fc, 32 KB
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 512;        // two buffers of [g | fc]
+
+struct __align__(1024) FwdSmem {
+  uint8_t a[STAGES][A_BYTES];
+  uint8_t b[STAGES][B_BYTES];
+  uint8_t stage[kEpiThreads / 32][3][2048];  // per epilogue warp: g, fc, y blocks [32 rows x 32 columns]
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];   // the tile's MMAs into this buffer are done
+  uint64_t tmem_empty[2];  // the epilogue has read this buffer out
+  uint32_t tmem_base;
+  volatile uint32_t abort_flag;
+  volatile uint32_t issued, consumed;
+};
+
+struct FwdArgs {
+  int M, K, N;
+  uint32_t* status;
+  const uint16_t* bias[2]; // b_g, b_fc [N] or null
+  int tiles, tiles_n, nkb;
+};
+
+__device__ __forceinline__ void fwd_timeout(FwdSmem& s, uint32_t* status) {
+  if (status != nullptr) atomicOr(status, kStatusTimeout);
+  s.abort_flag = 1u;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
+               const __grid_constant__ CUtensorMap tm_wfc, const __grid_constant__ CUtensorMap tm_g,
+               const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_y,
+               const FwdArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& s = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tmem_full[i], 1);
+      mbar_init(&s.tmem_empty[i], kEpiThreads);
+    }
+    s.abort_flag = 0u;
+    s.issued = s.consumed = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_wg);
+    tma_prefetch_desc(&tm_wfc);
+    tma_prefetch_desc(&tm_g);
+    tma_prefetch_desc(&tm_fc);
+    tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t gj = 0;
+      for (int t = blockIdx.x; t < args.tiles && !s.abort_flag; t += gridDim.x) {
+        const int n0 = (t % args.tiles_n) * BN, m0 = (t / args.tiles_n) * BM;
+        for (int kb = 0; kb < args.nkb && !s.abort_flag; ++kb, ++gj) {
+          const int st = gj % STAGES;
+          if (gj >= STAGES && !mbar_wait(&s.empty[st], ((gj / STAGES) - 1) & 1)) {
+            fwd_timeout(s, args.status);
+            break;
+          }
+          mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+          const int kr = kb * BK;
+          tma_load_2d(s.a[st], &tm_x, &s.full[st], kr, m0);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            tma_load_2d(s.b[st] + j * 8192, &tm_wg, &s.full[st], n0 + 64 * j, kr);
+            tma_load_2d(s.b[st] + 16384 + j * 8192, &tm_wfc, &s.full[st], n0 + 64 * j, kr);
+          }
+          s.issued = gj + 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);  // A K-major, B MN-major
+      uint32_t gj = 0, it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++it) {
+        const uint32_t buf = it & 1;
+        if (it >= 2) {
+          // the epilogue has read this buffer's previous tile out
+          if (!mbar_wait(&s.tmem_empty[buf], ((it >> 1) - 1) & 1)) {
+            fwd_timeout(s, args.status);
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t d = tmem + buf * 256;  // g at d, fc at d + 128
+        for (int kb = 0; kb < args.nkb; ++kb, ++gj) {
+          const int st = gj % STAGES;
+          if (!mbar_wait(&s.full[st], (gj / STAGES) & 1)) {
+            fwd_timeout(s, args.status);
+            ok = false;
+            break;
+          }
+          s.consumed = gj + 1;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(s.a[st]);
+          const uint32_t b_addr = smem_u32(s.b[st]);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024);
+            umma_bf16(d, ad, smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, acc);
+            umma_bf16(d + BN, ad, smem_desc(b_addr + 16384 + 2048 * k, 8192, 1024), idesc, acc);
+          }
+          umma_commit(&s.empty[st]);
+        }
+        if (ok) umma_commit(&s.tmem_full[buf]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    bool dead = false, staged = false;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++it) {
+      const uint32_t buf = it & 1;
+      const int n0 = (t % args.tiles_n) * BN, m0 = (t / args.tiles_n) * BM;
+      bool ready = false;
+      if (!dead && !s.abort_flag) {
+        ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1);
+        if (!ready) {
+          fwd_timeout(s, args.status);
+          dead = true;
+        }
+      }
+      tc_fence_after();
+      // tcgen05.ld is warp-collective: decide for the whole warp
+      if (__all_sync(0xffffffffu, ready && !s.abort_flag)) {
+        const uint32_t d = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
+        const uint32_t stg = smem_u32(s.stage[warp - 2][0]);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t vg[32], vf[32];
+          tmem_ld_32x32b_x32(d + c * 32, vg);
+          tmem_ld_32x32b_x32(d + BN + c * 32, vf);
+          tmem_ld_wait();
+          const int col = n0 + c * 32;
+          if (staged) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous stores have read the staging buffers
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 bgv = make_uint4(0u, 0u, 0u, 0u), bfv = make_uint4(0u, 0u, 0u, 0u);
+            if (col + 8 * j < args.N) {  // columns beyond N: zeros, clipped by the store
+              if (args.bias[0] != nullptr) bgv = __ldg(reinterpret_cast<const uint4*>(args.bias[0] + col + 8 * j));
+              if (args.bias[1] != nullptr) bfv = __ldg(reinterpret_cast<const uint4*>(args.bias[1] + col + 8 * j));
+            }
+            const uint32_t bgw[4] = {bgv.x, bgv.y, bgv.z, bgv.w};
+            const uint32_t bfw[4] = {bfv.x, bfv.y, bfv.z, bfv.w};
+            uint32_t og[4], of[4], oy[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = 8 * j + 2 * e;
+              const float2 g2 = __fadd2_rn(make_float2(__uint_as_float(vg[i0]), __uint_as_float(vg[i0 + 1])),
+                                           bf16x2_to_f2(bgw[e]));
+              const float2 f2 = __fadd2_rn(make_float2(__uint_as_float(vf[i0]), __uint_as_float(vf[i0 + 1])),
+                                           bf16x2_to_f2(bfw[e]));
+              const Sig2 sg = sigmoid_pair2(g2);
+              const float2 y2 = __fmul2_rn(__fmul2_rn(g2, sg.s), f2);
+              og[e] = pack_bf16x2(g2.x, g2.y);
+              of[e] = pack_bf16x2(f2.x, f2.y);
+              oy[e] = pack_bf16x2(y2.x, y2.y);
+            }
+            // this lane's row of each 32x32 block, 64-byte swizzle: 16-byte chunk j ^ ((row >> 1) & 3)
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            sts128(stg + off, make_uint4(og[0], og[1], og[2], og[3]));
+            sts128(stg + 2048 + off, make_uint4(of[0], of[1], of[2], of[3]));
+            sts128(stg + 4096 + off, make_uint4(oy[0], oy[1], oy[2], oy[3]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_g, s.stage[warp - 2][0], col, m0 + q * 32);
+            tma_store_2d(&tm_fc, s.stage[warp - 2][1], col, m0 + q * 32);
+            tma_store_2d(&tm_y, s.stage[warp - 2][2], col, m0 + q * 32);
+            bulk_commit();
+          }
+          staged = true;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.tmem_empty[buf]);  // this thread has read its rows of the buffer
+    }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && s.abort_flag) {
+    // drain: copies issued but never consumed must land before the CTA exits
+    for (uint32_t i = s.consumed; i < s.issued; ++i)
+      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16_t* w_fc, const uint16_t* b_g,
+                            const uint16_t* b_fc, uint16_t* g, uint16_t* fc, uint16_t* y, int64_t M, int64_t K,
+                            int64_t N, cudaStream_t stream) {
+  CUtensorMap mx, mwg, mwfc, mg, mfc, my;
+  const uint64_t rs = static_cast<uint64_t>(N) * 2;
+  if (!encode_tmap_2d_bf16(&mx, x, K, M, static_cast<uint64_t>(K) * 2, BK, BM) ||
+      !encode_tmap_2d_bf16(&mwg, w_g, N, K, rs, 64, BK) || !encode_tmap_2d_bf16(&mwfc, w_fc, N, K, rs, 64, BK) ||
+      !encode_tmap_2d_bf16(&mg, g, N, M, rs, 32, 32, 64) || !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 32, 32, 64) ||
+      !encode_tmap_2d_bf16(&my, y, N, M, rs, 32, 32, 64))
+    return cudaErrorInvalidValue;
+  FwdArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.status = status_word_ptr();
+  a.bias[0] = b_g;
+  a.bias[1] = b_fc;
+  a.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  a.tiles = static_cast<int>(((M + BM - 1) / BM) * a.tiles_n);
+  a.nkb = static_cast<int>((K + BK - 1) / BK);
+  constexpr size_t smem = sizeof(FwdSmem) + 1024;
+  static_assert(smem <= 232448, "forward kernel shared memory");
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int grid = device_sm_count();
+  if (grid > a.tiles) grid = a.tiles;
+  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mx, mwg, mwfc, mg, mfc, my, a);
+  return cudaGetLastError();
+}
+
+}  // namespace swg

@@ -43,6 +43,11 @@ int device_sm_count();
 
 cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_t* w_g, const uint16_t* w_fc,
                           uint16_t* dx, int64_t M, int64_t K, int64_t N, cudaStream_t stream);
+// forward: g = x W_g + b_g, fc = x W_fc + b_fc, y = SiLU(g) fc (b_g, b_fc may be null);
+// persistent tcgen05 GEMM (fwd_tc.cu)
+cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16_t* w_fc, const uint16_t* b_g,
+                            const uint16_t* b_fc, uint16_t* g, uint16_t* fc, uint16_t* y, int64_t M, int64_t K,
+                            int64_t N, cudaStream_t stream);
 cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
                           uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
                           cudaStream_t stream, bool accumulate = false);

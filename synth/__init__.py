@@ -10,6 +10,7 @@ from .workloads import (  # noqa: F401
     SWIGLU_CONFIGS,
     SWISH_CONFIG,
     SwigluShape,
+    swiglu_fwd_biases,
     swiglu_inputs,
     swish_inputs,
 )

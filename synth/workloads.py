@@ -90,6 +90,21 @@ def swiglu_inputs(shape: SwigluShape, device: str | torch.device = "cpu",
     return out
 
 
+def swiglu_fwd_biases(shape: SwigluShape, device: str | torch.device = "cpu",
+                      seed: int | None = None) -> tuple:
+    """Draw the forward's biases (b_g, b_fc) [N] bf16, with the standard deviation
+    of x W (the x scale: each product sums K terms of variance x^2 / K), from a
+    generator seeded with the workload's seed + 1000 (independent of
+    swiglu_inputs' draws)."""
+    N = shape.N
+    std = _scales(shape)["x"]
+    gen = torch.Generator(device=device)
+    gen.manual_seed((shape.seed if seed is None else seed) + 1000)
+    b = [torch.randn(N, generator=gen, device=device, dtype=torch.float32).mul_(std).to(torch.bfloat16)
+         for _ in range(2)]
+    return b[0], b[1]
+
+
 def swish_inputs(n: int, dtype: torch.dtype, device: str | torch.device = "cpu",
                  seed: int = 1) -> tuple:
     """Draw (grad, x) for SwishGrad: x ~ randn*4 (std 4), grad ~ randn."""

@@ -24,7 +24,8 @@ MAX_REL = 2.0 ** -6
 L2_REL = 2.0 ** -8
 
 ATOL = dict(dg=ATOL_ELEM, dfc=ATOL_ELEM, grad_x=ATOL_ELEM,
-            db_g=ATOL_RED, db_fc=ATOL_RED, dw_g=ATOL_RED, dw_fc=ATOL_RED, dx=ATOL_RED)
+            db_g=ATOL_RED, db_fc=ATOL_RED, dw_g=ATOL_RED, dw_fc=ATOL_RED, dx=ATOL_RED,
+            g=ATOL_RED, fc=ATOL_RED, y=ATOL_RED)  # forward: GEMM outputs, like dw and dx
 
 
 def to_f64(t) -> np.ndarray:

@@ -330,10 +330,55 @@ def pin_bf16_rounding():
     assert np.array_equal(rt, allbits[finite])
 
 
+# --------------------------------------------------------------------------- forward
+
+def pin_forward_bruteforce():
+    """g, fc by explicit loops with the bias, y = g * sigma(g) * fc per element
+    with the textbook sigmoid 1 / (1 + e^-g) (finite for these inputs)."""
+    rng = _rng(41)
+    M, K, N = 3, 4, 5
+    x, w_g, w_fc = rng.standard_normal((M, K)), rng.standard_normal((K, N)), rng.standard_normal((K, N))
+    b_g, b_fc = rng.standard_normal(N), rng.standard_normal(N)
+    g, fc, y = osw.swiglu_fwd(x, w_g, w_fc, b_g, b_fc)
+    for i in range(M):
+        for j in range(N):
+            gij = b_g[j] + sum(x[i, k] * w_g[k, j] for k in range(K))
+            fij = b_fc[j] + sum(x[i, k] * w_fc[k, j] for k in range(K))
+            yij = gij / (1.0 + math.exp(-gij)) * fij
+            assert abs(g[i, j] - gij) < 1e-13 and abs(fc[i, j] - fij) < 1e-13
+            assert abs(y[i, j] - yij) < 1e-13 * max(1.0, abs(yij))
+
+
+def pin_forward_torch():
+    import torch
+    rng = _rng(43)
+    M, K, N = 9, 7, 11
+    x, w_g, w_fc = rng.standard_normal((M, K)), rng.standard_normal((K, N)), rng.standard_normal((K, N))
+    b_g, b_fc = rng.standard_normal(N), rng.standard_normal(N)
+    t = lambda a: torch.tensor(a, dtype=torch.float64)  # noqa: E731
+    ref = torch.nn.functional.silu(t(x) @ t(w_g) + t(b_g)) * (t(x) @ t(w_fc) + t(b_fc))
+    _, _, y = osw.swiglu_fwd(x, w_g, w_fc, b_g, b_fc)
+    assert np.max(np.abs(y - ref.numpy())) < 1e-12
+
+
+def pin_forward_closed_forms():
+    """With K = 1 and x = 1 the gate takes chosen values: sigma(0) = 1/2,
+    sigma(ln 3) = 3/4, sigma(-ln 3) = 1/4, so y = g * sigma(g) * fc is known exactly."""
+    l3 = math.log(3.0)
+    x = np.array([[1.0]])
+    w_g = np.array([[0.0, l3, -l3]])
+    w_fc = np.array([[2.0, 2.0, 2.0]])
+    g, fc, y = osw.swiglu_fwd(x, w_g, w_fc, None, np.array([0.0, 1.0, -1.0]))
+    assert np.allclose(g, [[0.0, l3, -l3]], rtol=0, atol=1e-15)
+    assert np.allclose(fc, [[2.0, 3.0, 1.0]], rtol=0, atol=1e-15)
+    assert np.allclose(y, [[0.0, l3 * 0.75 * 3.0, -l3 * 0.25 * 1.0]], rtol=1e-15, atol=1e-15)
+
+
 ALL_PINS = [
     pin_sigmoid_closed_forms, pin_sigmoid_matches_scipy, pin_sigmoid_derivative,
     pin_silu_grad_fd, pin_silu_grad_symbolic, pin_b_stage_symbolic, pin_b_stage_fd,
     pin_db_is_column_sum, pin_gemm_bruteforce, pin_full_chain_fd, pin_torch_autograd,
     pin_linearity_in_dy, pin_sampled_matches_full, pin_swish_special_cases,
     pin_swish_alternative_form, pin_swish_fd, pin_swish_cann_sample, pin_bf16_rounding,
+    pin_forward_bruteforce, pin_forward_torch, pin_forward_closed_forms,
 ]

@@ -79,6 +79,19 @@ def _swish_beta_not_f32(grad, x, scale=1.0):
     return np.asarray(grad, np.float64) * (s * (1.0 + t * (1.0 - s)))
 
 
+def _fwd_drops_bias_g(x, w_g, w_fc, b_g=None, b_fc=None):
+    return osw.__dict__["_orig_fwd"](x, w_g, w_fc, None, b_fc)
+
+
+def _fwd_sigmoid_not_silu(x, w_g, w_fc, b_g=None, b_fc=None):
+    g, fc, _ = osw.__dict__["_orig_fwd"](x, w_g, w_fc, b_g, b_fc)
+    return g, fc, osw.sigmoid(g) * fc
+
+
+def _fwd_weights_swapped(x, w_g, w_fc, b_g=None, b_fc=None):
+    return osw.__dict__["_orig_fwd"](x, w_fc, w_g, b_g, b_fc)
+
+
 def _bf16_truncate(x):
     v = np.asarray(x, np.float64).astype(np.float32)
     return ((v.view(np.uint32) >> 16) << 16).view(np.float32).astype(np.float64)
@@ -96,12 +109,16 @@ MUTANTS = {
     "swish_beta_missing_in_bracket": [(osh, "swish_grad", _swish_no_beta_inside)],
     "swish_beta_not_rounded_to_f32": [(osh, "swish_grad", _swish_beta_not_f32)],
     "bf16_truncates": [(onum, "f64_to_bf16_value", _bf16_truncate)],
+    "fwd_drops_bias_g": [(osw, "swiglu_fwd", _fwd_drops_bias_g)],
+    "fwd_sigmoid_not_silu": [(osw, "swiglu_fwd", _fwd_sigmoid_not_silu)],
+    "fwd_weights_swapped": [(osw, "swiglu_fwd", _fwd_weights_swapped)],
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_planted_mistake_is_caught(name, monkeypatch):
     monkeypatch.setitem(osw.__dict__, "_orig_b", osw.swiglu_bwd_b)
+    monkeypatch.setitem(osw.__dict__, "_orig_fwd", osw.swiglu_fwd)
     for mod, attr, fn in MUTANTS[name]:
         monkeypatch.setattr(mod, attr, fn)
     caught = []
