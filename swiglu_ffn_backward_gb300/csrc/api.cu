@@ -347,11 +347,11 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
                         rng(dg, dg ? mn : 0), rng(dfc, dfc ? mn : 0)};
   const Range ins[] = {rng(x, M * K * 2), rng(w_g, kn), rng(w_fc, kn), rng(dy, mn), rng(g, mn), rng(fc, mn)};
   if (any_overlap(outs, 7, ins, 6)) return SWG_ERR_PARAM_INVALID;
+  if (M == 0 && acc) return SWG_OK;  // a sum over no rows adds nothing: no work at all
   st = check_device();
   if (st != SWG_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M == 0) {
-    if (acc) return SWG_OK;  // a sum over no rows adds nothing
     st = zero_bf16(dw_g, K * N, s);
     if (st == SWG_OK) st = zero_bf16(dw_fc, K * N, s);
     if (st == SWG_OK) st = zero_bf16(db_g, N, s);

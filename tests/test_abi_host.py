@@ -131,3 +131,38 @@ def test_python_binding_requires_cuda_tensors(swg):
         swg.swiglu_bwd_b(t, t, t)
     with pytest.raises(TypeError):
         swg.swish_grad(t, t, 1.0)
+
+
+def test_forward_argument_checks(swg):
+    lib, b = _lib(swg)
+    p = [FAKE + i * 2**26 for i in range(8)]  # x, w_g, w_fc, b_g, b_fc, g, fc, y
+    assert lib.swiglu_fwd(None, *p[1:], 16, 8, 8, None) == b.SWG_ERR_NULLPTR
+    assert lib.swiglu_fwd(*p[:7], None, 16, 8, 8, None) == b.SWG_ERR_NULLPTR
+    assert lib.swiglu_fwd(*p, -1, 8, 8, None) == b.SWG_ERR_PARAM_INVALID
+    assert lib.swiglu_fwd(*p, 16, 12, 8, None) == b.SWG_ERR_UNSUPPORTED   # K not a multiple of 8
+    assert lib.swiglu_fwd(*p, 16, 0, 8, None) == b.SWG_ERR_UNSUPPORTED    # no reduction to run
+    q = list(p)
+    q[3] += 2  # misaligned bias
+    assert lib.swiglu_fwd(*q, 16, 8, 8, None) == b.SWG_ERR_UNSUPPORTED
+    q = list(p)
+    q[7] = q[6] + 16  # y overlaps fc
+    assert lib.swiglu_fwd(*q, 16, 8, 8, None) == b.SWG_ERR_PARAM_INVALID
+    # empty M: nothing to do, even with NULL buffers
+    assert lib.swiglu_fwd(None, p[1], p[2], None, None, None, None, None, 0, 8, 8, None) == b.SWG_OK
+
+
+def test_accumulate_flag_is_accepted_and_empty_M_needs_no_device(swg):
+    lib, b = _lib(swg)
+    base = [FAKE + i * 2**26 for i in range(13)]
+    base[0] = base[3] = base[4] = base[5] = base[8] = None  # x, dy, g, fc, dx are empty at M = 0
+    base[6] = base[7] = None  # no dg, dfc
+    # M = 0 with SWG_ACCUMULATE returns before touching the device (no GPU here)
+    assert lib.swiglu_bwd(*base, 0, 8, 8, b.SWG_ACCUMULATE, None, 0, None) == b.SWG_OK
+    assert lib.swiglu_bwd(*base, 0, 8, 8, b.SWG_ACCUMULATE | b.SWG_FUSED, None, 0, None) == b.SWG_OK
+
+
+def test_forward_binding_checks_shapes(swg):
+    import torch
+    t = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        swg.swiglu_fwd(t, t, t)
