@@ -302,6 +302,22 @@ def run_ours(args, rank, world):
     sw_t = [sw_ev[i].elapsed_time(sw_ev[i + 1]) for i in range(sw_n)]
     sw_ms = statistics.median(sw_t)
     sw_gbs = 3.0 * SWISH_N * 2 / (sw_ms * 1e-3) / 1e9
+    # the sibling activation gradients through the same streaming kernels, same timing
+    act = {}
+    for name in ("gelu", "hardswish"):
+        for i in range(sw_warm):
+            g_, x_, o_ = sets[i % 6]
+            swg.act_grad(g_, x_, name, grad_x=o_)
+        for i in range(sw_n):
+            g_, x_, o_ = sets[(sw_warm + i) % 6]
+            sw_ev[i].record(stream)
+            swg.act_grad(g_, x_, name, grad_x=o_)
+        sw_ev[sw_n].record(stream)
+        torch.cuda.synchronize()
+        a_ms = statistics.median([sw_ev[i].elapsed_time(sw_ev[i + 1]) for i in range(sw_n)])
+        a_gbs = 3.0 * SWISH_N * 2 / (a_ms * 1e-3) / 1e9
+        act[name] = {"ms": round(a_ms, 5), "gbs": round(a_gbs, 1), "frac_hbm": round(a_gbs / pk["hbm"], 4)}
+    swg.swg_check()
     del sets
 
     # accumulate mode: the public whole-backward call (fused chain, dg/dfc not
@@ -407,6 +423,7 @@ def run_ours(args, rank, world):
                        "stages": describe(per_other)},
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
                        "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
+        "act_grad": {"n": SWISH_N, "dtype": "bf16", **act},
         "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
         "swiglu_fwd": fwd,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

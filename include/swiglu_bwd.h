@@ -69,6 +69,9 @@ typedef enum {
 
 typedef enum { SWG_F32 = 0, SWG_F16 = 1, SWG_BF16 = 2 } swg_dtype;
 
+/* activations whose gradient act_grad computes */
+typedef enum { SWG_ACT_SILU = 0, SWG_ACT_GELU = 1, SWG_ACT_HARDSWISH = 2 } swg_act;
+
 /* flags for swiglu_bwd */
 #define SWG_UNFUSED 0u /* b stage, then the w and x GEMMs on the stored dg, dfc */
 #define SWG_FUSED 1u   /* the GEMMs recompute dg, dfc from dy, g, fc in their
@@ -215,6 +218,23 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc,
  * No workspace ([P2]'s workspace query returns 0 for this op as well). */
 swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x,
                       int64_t n, swg_dtype dtype, swg_stream_t stream);
+
+/* ---- sibling activation gradients -------------------------------------------
+ * The Ascend C backward blog post names GELU and HardSwish as the next
+ * activations to give a hand-written backward, and SiluGrad as SwishGrad's
+ * sibling; the pages give no formula for them, so the standard definitions
+ * are used: grad_x = grad * f'(x), fp32 math, fp16/bf16 rounded once (RNE).
+ *   SWG_ACT_SILU:      f(x) = x sigma(x) -- identical to swish_grad with
+ *                      scale 1.0, bit for bit
+ *   SWG_ACT_GELU:      f(x) = x Phi(x) (exact, erf form);
+ *                      f'(x) = Phi(x) + x phi(x)
+ *   SWG_ACT_HARDSWISH: f(x) = x min(max(x + 3, 0), 6) / 6;
+ *                      f'(x) = 0 (x <= -3), x/3 + 1/2 (-3 < x < 3), 1 (x >= 3),
+ *                      the kinks as in PyTorch's autograd
+ * Same arguments, layout, aliasing and error rules as swish_grad (an unknown
+ * act is SWG_ERR_PARAM_INVALID). */
+swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x,
+                    int64_t n, swg_dtype dtype, swg_stream_t stream);
 
 #ifdef __cplusplus
 }

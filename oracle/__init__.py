@@ -9,12 +9,15 @@ It restates, in plain numpy float64, what two pages define:
 * "PyPTO-Gym in practice: the fused SwiGLU backward operator"
   (hnwysp.cn/news/34787), section "Algorithm overview and formulas",
   items 1-4 (dg, dfc, db_g, db_fc, dw_g, dw_fc, dx), plus the forward in its
-  "Operator background" section, used only by the pins.
+  "Operator background" section (g, fc, y).
 * "SwishGrad in CANN ops-nn: principle, implementation and the
   aclnnSwishBackward guide" (bhfrc.com/news/37500), section 1.2
   "Computation formula" (grad_x = grad * sigma(beta x) * (1 + beta x (1 -
   sigma(beta x)))), section 2.4 (fp16/bf16 widened to fp32, results narrowed
   with round-to-nearest-even), section 3.5 (beta defaults to 1.0).
+* The sibling activation gradients (SiLU, GELU, HardSwish) that the Ascend C
+  backward blog post and the SwishGrad page name, with their standard
+  definitions (the pages print no formula for them): `activations.py`.
 
 Library primitives used as steps: numpy.exp, numpy matmul, numpy.sum.
 Parity status: every function here is pinned by the `-m "not gpu"` tests
@@ -40,3 +43,4 @@ from .swiglu import (  # noqa: F401
     swiglu_fwd,
 )
 from .swish import swish_fwd, swish_grad  # noqa: F401
+from .activations import act_grad, gelu_grad, hardswish_grad, silu_act_grad  # noqa: F401

@@ -6,6 +6,7 @@ include/swiglu_bwd.h; this package is the thin Python binding over it.
 
 from ._binding import (  # noqa: F401
     EXPORTS,
+    act_grad,
     LIB_PATH,
     SWG_ACCUMULATE,
     SWG_FUSED,

@@ -46,6 +46,7 @@ EXPORTS = (
     "swiglu_bwd_x_fused",
     "swiglu_bwd_w_fused_workspace_size", "swiglu_bwd_w_fused",
     "swiglu_fwd",
+    "act_grad",
 )
 
 
@@ -79,6 +80,8 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_bwd_x.restype = st
     lib.swiglu_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, P]
     lib.swiglu_fwd.restype = st
+    lib.act_grad.argtypes = [P, P, ctypes.c_int, P, I64, ctypes.c_int, P]
+    lib.act_grad.restype = st
     lib.swiglu_bwd_workspace_size.argtypes = [I64, I64, I64, U]
     lib.swiglu_bwd_workspace_size.restype = SZ
     lib.swiglu_bwd.argtypes = [P] * 13 + [I64, I64, I64, U, P, SZ, P]
@@ -318,6 +321,28 @@ def swish_grad(grad, x, scale=None, grad_x=None, stream=None):
     sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
     _check(lib.swish_grad(grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
                           _DTYPE[grad.dtype], _stream(stream)), "swish_grad")
+    return grad_x
+
+
+SWG_ACT = {"silu": 0, "gelu": 1, "hardswish": 2}
+
+
+def act_grad(grad, x, act: str, grad_x=None, stream=None):
+    """Activation gradient grad * f'(x) for act in "silu", "gelu", "hardswish"
+    (fp32/fp16/bf16, any shape, treated as 1-D)."""
+    if act not in SWG_ACT:
+        raise ValueError(f"act must be one of {sorted(SWG_ACT)}")
+    if not (isinstance(grad, torch.Tensor) and isinstance(x, torch.Tensor) and grad.is_cuda and x.is_cuda):
+        raise TypeError("grad and x must be CUDA tensors")
+    if grad.dtype != x.dtype or grad.shape != x.shape:
+        raise ValueError("grad and x must have the same dtype and shape")
+    if grad.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {grad.dtype}")
+    grad, x = grad.contiguous(), x.contiguous()
+    if grad_x is None:
+        grad_x = torch.empty_like(grad)
+    _check(lib.act_grad(grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
+                        _DTYPE[grad.dtype], _stream(stream)), "act_grad")
     return grad_x
 
 

@@ -102,8 +102,8 @@ swg_status swg_check(swg_stream_t stream) {
 }
 
 // ---------------------------------------------------------------- SwishGrad
-swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x, int64_t n,
-                      swg_dtype dtype, swg_stream_t stream) {
+// shared argument checks of the element-wise gradients (swish_grad, act_grad)
+swg_status check_elementwise(const void* grad, const void* x, void* grad_x, int64_t n, swg_dtype dtype) {
   if (n < 0 || (dtype != SWG_F32 && dtype != SWG_F16 && dtype != SWG_BF16)) return SWG_ERR_PARAM_INVALID;
   if (n == 0) return SWG_OK;  // empty tensors may carry NULL data pointers
   if (grad == nullptr || x == nullptr || grad_x == nullptr) return SWG_ERR_NULLPTR;
@@ -115,7 +115,25 @@ swg_status swish_grad(const void* grad, const void* x, const float* scale, void*
   // grad_x may alias grad or x exactly, but must not partially overlap either
   const Range o = rng(grad_x, n * es), a = rng(grad, n * es), b = rng(x, n * es);
   if ((overlap(o, a) && o.lo != a.lo) || (overlap(o, b) && o.lo != b.lo)) return SWG_ERR_PARAM_INVALID;
-  swg_status st = check_device();
+  return SWG_OK;
+}
+
+swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x, int64_t n, swg_dtype dtype,
+                    swg_stream_t stream) {
+  if (act != SWG_ACT_SILU && act != SWG_ACT_GELU && act != SWG_ACT_HARDSWISH) return SWG_ERR_PARAM_INVALID;
+  swg_status st = check_elementwise(grad, x, grad_x, n, dtype);
+  if (st != SWG_OK || n == 0) return st;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  return cuda_status(swg::launch_act_grad(grad, x, static_cast<int>(act), grad_x, n, static_cast<int>(dtype),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x, int64_t n,
+                      swg_dtype dtype, swg_stream_t stream) {
+  swg_status st = check_elementwise(grad, x, grad_x, n, dtype);
+  if (st != SWG_OK || n == 0) return st;
+  st = check_device();
   if (st != SWG_OK) return st;
   const float beta = scale != nullptr ? *scale : 1.0f;
   return cuda_status(swg::launch_swish_grad(grad, x, beta, grad_x, n, static_cast<int>(dtype),

@@ -12,6 +12,9 @@ namespace swg {
 // ---- SwishGrad: dtype 0 = f32, 1 = f16, 2 = bf16
 cudaError_t launch_swish_grad(const void* grad, const void* x, float beta, void* grad_x, int64_t n, int dtype,
                               cudaStream_t stream);
+// activation gradients grad * f'(x): act 0 = SiLU (SwishGrad with beta 1), 1 = GELU (exact), 2 = HardSwish
+cudaError_t launch_act_grad(const void* grad, const void* x, int act, void* grad_x, int64_t n, int dtype,
+                            cudaStream_t stream);
 
 // ---- b stage
 struct BPlan {

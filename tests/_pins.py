@@ -17,6 +17,7 @@ import os
 
 import numpy as np
 
+import oracle.activations as oact
 import oracle.numerics as onum
 import oracle.swiglu as osw
 import oracle.swish as osh
@@ -374,6 +375,49 @@ def pin_forward_closed_forms():
     assert np.allclose(y, [[0.0, l3 * 0.75 * 3.0, -l3 * 0.25 * 1.0]], rtol=1e-15, atol=1e-15)
 
 
+# --------------------------------------------------------------------------- sibling activations
+
+def _gelu_local(z):
+    return z * 0.5 * (1.0 + math.erf(z / math.sqrt(2.0)))
+
+
+def _hardswish_local(z):
+    return z * min(max(z + 3.0, 0.0), 6.0) / 6.0
+
+
+def pin_gelu_grad_fd():
+    z = np.concatenate([np.linspace(-8, 8, 161), _rng(51).standard_normal(200) * 3])
+    h = 1e-6
+    fd = np.array([(_gelu_local(v + h) - _gelu_local(v - h)) / (2 * h) for v in z])
+    assert np.max(np.abs(oact.gelu_grad(np.ones_like(z), z) - fd)) < 1e-8
+
+
+def pin_gelu_grad_torch_and_special_values():
+    import torch
+    z = np.concatenate([np.linspace(-10, 10, 201), _rng(53).standard_normal(300) * 4])
+    t = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.gelu(t, approximate="none").sum().backward()
+    assert np.max(np.abs(oact.gelu_grad(np.ones_like(z), z) - t.grad.numpy())) < 1e-14
+    g = oact.gelu_grad(np.array([2.0, 2.0, 2.0]), np.array([0.0, 40.0, -40.0]))
+    assert g[0] == 1.0 and g[1] == 2.0 and g[2] == 0.0  # GELU'(0) = 1/2; saturation
+
+
+def pin_hardswish_grad():
+    import torch
+    z = np.concatenate([np.linspace(-5, 5, 1001), [-3.0, 3.0, -4.0, 4.0, 0.0], _rng(55).standard_normal(300) * 3])
+    t = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.hardswish(t).sum().backward()
+    got = oact.hardswish_grad(np.ones_like(z), z)
+    assert np.max(np.abs(got - t.grad.numpy())) < 1e-15
+    # finite differences away from the kinks; slope 1/3 in the middle; flat outside
+    h = 1e-6
+    w = z[(np.abs(z + 3) > 1e-3) & (np.abs(z - 3) > 1e-3)]
+    fd = np.array([(_hardswish_local(v + h) - _hardswish_local(v - h)) / (2 * h) for v in w])
+    assert np.max(np.abs(oact.hardswish_grad(np.ones_like(w), w) - fd)) < 1e-8
+    v = oact.hardswish_grad(np.ones(5), np.array([-4.0, -3.0, 0.0, 3.0, 4.0]))
+    assert list(v) == [0.0, 0.0, 0.5, 1.0, 1.0]
+
+
 ALL_PINS = [
     pin_sigmoid_closed_forms, pin_sigmoid_matches_scipy, pin_sigmoid_derivative,
     pin_silu_grad_fd, pin_silu_grad_symbolic, pin_b_stage_symbolic, pin_b_stage_fd,
@@ -381,4 +425,5 @@ ALL_PINS = [
     pin_linearity_in_dy, pin_sampled_matches_full, pin_swish_special_cases,
     pin_swish_alternative_form, pin_swish_fd, pin_swish_cann_sample, pin_bf16_rounding,
     pin_forward_bruteforce, pin_forward_torch, pin_forward_closed_forms,
+    pin_gelu_grad_fd, pin_gelu_grad_torch_and_special_values, pin_hardswish_grad,
 ]

@@ -166,3 +166,11 @@ def test_forward_binding_checks_shapes(swg):
     t = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         swg.swiglu_fwd(t, t, t)
+
+
+def test_act_grad_argument_checks(swg):
+    lib, b = _lib(swg)
+    assert lib.act_grad(FAKE, FAKE + 4096, 7, FAKE + 8192, 10, b.SWG_F32, None) == b.SWG_ERR_PARAM_INVALID
+    assert lib.act_grad(FAKE, None, 1, FAKE + 8192, 10, b.SWG_F32, None) == b.SWG_ERR_NULLPTR
+    assert lib.act_grad(FAKE, FAKE + 4096, 1, FAKE + 16, 100, b.SWG_F32, None) == b.SWG_ERR_PARAM_INVALID
+    assert lib.act_grad(None, None, 2, None, 0, b.SWG_BF16, None) == b.SWG_OK  # empty

@@ -7,6 +7,7 @@ and checks that at least one pin catches each of them.
 import numpy as np
 import pytest
 
+import oracle.activations as oact
 import oracle.numerics as onum
 import oracle.swiglu as osw
 import oracle.swish as osh
@@ -92,6 +93,22 @@ def _fwd_weights_swapped(x, w_g, w_fc, b_g=None, b_fc=None):
     return osw.__dict__["_orig_fwd"](x, w_fc, w_g, b_g, b_fc)
 
 
+def _gelu_drops_x_phi(grad, x):
+    from scipy.special import erf
+    x = np.asarray(x, np.float64)
+    return np.asarray(grad, np.float64) * 0.5 * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def _hardswish_slope_sixth(grad, x):
+    x = np.asarray(x, np.float64)
+    return np.asarray(grad, np.float64) * np.where(x <= -3.0, 0.0, np.where(x < 3.0, x / 6.0 + 0.5, 1.0))
+
+
+def _hardswish_kinks_closed(grad, x):
+    x = np.asarray(x, np.float64)
+    return np.asarray(grad, np.float64) * np.where(x < -3.0, 0.0, np.where(x <= 3.0, x / 3.0 + 0.5, 1.0))
+
+
 def _bf16_truncate(x):
     v = np.asarray(x, np.float64).astype(np.float32)
     return ((v.view(np.uint32) >> 16) << 16).view(np.float32).astype(np.float64)
@@ -112,6 +129,9 @@ MUTANTS = {
     "fwd_drops_bias_g": [(osw, "swiglu_fwd", _fwd_drops_bias_g)],
     "fwd_sigmoid_not_silu": [(osw, "swiglu_fwd", _fwd_sigmoid_not_silu)],
     "fwd_weights_swapped": [(osw, "swiglu_fwd", _fwd_weights_swapped)],
+    "gelu_drops_x_phi": [(oact, "gelu_grad", _gelu_drops_x_phi)],
+    "hardswish_slope_one_sixth": [(oact, "hardswish_grad", _hardswish_slope_sixth)],
+    "hardswish_kinks_closed": [(oact, "hardswish_grad", _hardswish_kinks_closed)],
 }
 
 
