@@ -18,8 +18,11 @@ It restates, in plain numpy float64, what two pages define:
 * The sibling activation gradients (SiLU, GELU, HardSwish) that the Ascend C
   backward blog post and the SwishGrad page name, with their standard
   definitions (the pages print no formula for them): `activations.py`.
+* The GroupNorm backward of the Ascend C backward blog post (its GroupNorm
+  section, both printed versions): dx by the post's formula, dgamma and dbeta
+  by their standard definitions: `group_norm.py`.
 
-Library primitives used as steps: numpy.exp, numpy matmul, numpy.sum.
+Library primitives used as steps: numpy.exp, numpy matmul, numpy.sum, numpy.mean.
 Parity status: every function here is pinned by the `-m "not gpu"` tests
 (closed forms, symbolic derivatives, finite differences of the forward,
 brute-force loops, torch fp64 autograd); none is "parity unpinned".
@@ -44,3 +47,4 @@ from .swiglu import (  # noqa: F401
 )
 from .swish import swish_fwd, swish_grad  # noqa: F401
 from .activations import act_grad, gelu_grad, hardswish_grad, silu_act_grad  # noqa: F401
+from .group_norm import group_norm_bwd, group_norm_fwd, group_norm_stats  # noqa: F401

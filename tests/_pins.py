@@ -18,6 +18,7 @@ import os
 import numpy as np
 
 import oracle.activations as oact
+import oracle.group_norm as ogn
 import oracle.numerics as onum
 import oracle.swiglu as osw
 import oracle.swish as osh
@@ -418,6 +419,105 @@ def pin_hardswish_grad():
     assert list(v) == [0.0, 0.0, 0.5, 1.0, 1.0]
 
 
+# --------------------------------------------------------------------------- GroupNorm backward
+
+def _gn_inputs(N, C, S, G, seed):
+    """x with a different mean and spread per (sample, group), dy, gamma, beta."""
+    r = _rng(seed)
+    loc = r.uniform(-2, 2, (N, G, 1, 1))
+    sc = r.uniform(0.5, 2.0, (N, G, 1, 1))
+    x = (loc + sc * r.standard_normal((N, G, C // G, S))).reshape(N, C, S)
+    return x, r.standard_normal((N, C, S)), 1.0 + 0.5 * r.standard_normal(C), r.standard_normal(C)
+
+
+def _gn_loss_local(x, gamma, beta, dy, G, eps):
+    """sum(dy * GroupNorm(x)), the forward written out group by group with explicit loops."""
+    N, C, S = x.shape
+    cg = C // G
+    total = 0.0
+    for n in range(N):
+        for g in range(G):
+            vals = [x[n, c, s] for c in range(g * cg, (g + 1) * cg) for s in range(S)]
+            mu = sum(vals) / len(vals)
+            var = sum((v - mu) ** 2 for v in vals) / len(vals)
+            inv = 1.0 / math.sqrt(var + eps)
+            for c in range(g * cg, (g + 1) * cg):
+                for s in range(S):
+                    total += dy[n, c, s] * (gamma[c] * (x[n, c, s] - mu) * inv + beta[c])
+    return total
+
+
+def pin_group_norm_fd():
+    N, C, S, G, eps = 2, 6, 5, 3, 1e-3
+    x, dy, gamma, beta = _gn_inputs(N, C, S, G, 60)
+    dx, dgamma, dbeta = ogn.group_norm_bwd(dy, x, gamma, G, eps)
+    h = 1e-5
+
+    def fd(arr, idx):
+        a0 = arr[idx]
+        arr[idx] = a0 + h
+        lp = _gn_loss_local(x, gamma, beta, dy, G, eps)
+        arr[idx] = a0 - h
+        lm = _gn_loss_local(x, gamma, beta, dy, G, eps)
+        arr[idx] = a0
+        return (lp - lm) / (2 * h)
+
+    fdx = np.array([fd(x, i) for i in np.ndindex(x.shape)]).reshape(x.shape)
+    fdg = np.array([fd(gamma, (c,)) for c in range(C)])
+    fdb = np.array([fd(beta, (c,)) for c in range(C)])
+    assert np.max(np.abs(dx - fdx)) < 1e-7 * max(1.0, np.max(np.abs(fdx)))
+    assert np.max(np.abs(dgamma - fdg)) < 1e-7 * max(1.0, np.max(np.abs(fdg)))
+    assert np.max(np.abs(dbeta - fdb)) < 1e-7 * max(1.0, np.max(np.abs(fdb)))
+
+
+def pin_group_norm_torch():
+    import torch
+    for (N, C, S, G, eps) in [(3, 8, 7, 4, 1e-5), (2, 6, 9, 1, 1e-5), (2, 6, 4, 6, 1e-2)]:
+        x, dy, gamma, beta = _gn_inputs(N, C, S, G, 61 + G)
+        xt = torch.tensor(x, requires_grad=True)
+        gt = torch.tensor(gamma, requires_grad=True)
+        bt = torch.tensor(beta, requires_grad=True)
+        torch.nn.functional.group_norm(xt, G, gt, bt, eps).backward(torch.tensor(dy))
+        dx, dgamma, dbeta = ogn.group_norm_bwd(dy, x, gamma, G, eps)
+        assert np.max(np.abs(dx - xt.grad.numpy())) < 1e-12 * max(1.0, np.max(np.abs(dx)))
+        assert np.max(np.abs(dgamma - gt.grad.numpy())) < 1e-11
+        assert np.max(np.abs(dbeta - bt.grad.numpy())) < 1e-11
+
+
+def pin_group_norm_invariants():
+    N, C, S, G = 3, 8, 11, 2
+    x, dy, gamma, _ = _gn_inputs(N, C, S, G, 62)
+    # with eps = 0 the output ignores a shift or a scaling of x within a group, so dx is
+    # orthogonal to the constants and to (x - mu) in every group
+    dx, _, _ = ogn.group_norm_bwd(dy, x, gamma, G, 0.0)
+    xg = x.reshape(N, G, -1)
+    dg = dx.reshape(N, G, -1)
+    mu = np.array([[np.mean(xg[n, g]) for g in range(G)] for n in range(N)])
+    assert np.max(np.abs(dg.sum(axis=2))) < 1e-11
+    assert np.max(np.abs((dg * (xg - mu[:, :, None])).sum(axis=2))) < 1e-10
+    # statistics against plain per-slice numpy; dbeta and dgamma against loops
+    mu_o, var_o, rstd_o = ogn.group_norm_stats(x, G, 1e-5)
+    assert np.allclose(mu_o, mu, rtol=0, atol=1e-14)
+    var = np.array([[np.var(xg[n, g]) for g in range(G)] for n in range(N)])
+    assert np.allclose(var_o, var, rtol=1e-14, atol=0)
+    _, dgamma, dbeta = ogn.group_norm_bwd(dy, x, gamma, G, 1e-5)
+    cg = C // G
+    for c in range(C):
+        g = c // cg
+        b = sum(dy[n, c, s] for n in range(N) for s in range(S))
+        gm = sum(dy[n, c, s] * (x[n, c, s] - mu[n, g]) / math.sqrt(var[n, g] + 1e-5)
+                 for n in range(N) for s in range(S))
+        assert abs(dbeta[c] - b) < 1e-12 and abs(dgamma[c] - gm) < 1e-11
+    # gamma None is gamma = 1
+    a = ogn.group_norm_bwd(dy, x, None, G, 1e-5)
+    b = ogn.group_norm_bwd(dy, x, np.ones(C), G, 1e-5)
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+    # one element per group (C = G, HxW = 1): the output is beta whatever x is, so dx = 0, dgamma = 0
+    x1 = _rng(63).standard_normal((4, 5, 1))
+    d1, g1, b1 = ogn.group_norm_bwd(_rng(64).standard_normal((4, 5, 1)), x1, np.full(5, 2.0), 5, 1e-5)
+    assert np.max(np.abs(d1)) < 1e-12 and np.max(np.abs(g1)) == 0.0
+
+
 ALL_PINS = [
     pin_sigmoid_closed_forms, pin_sigmoid_matches_scipy, pin_sigmoid_derivative,
     pin_silu_grad_fd, pin_silu_grad_symbolic, pin_b_stage_symbolic, pin_b_stage_fd,
@@ -426,4 +526,5 @@ ALL_PINS = [
     pin_swish_alternative_form, pin_swish_fd, pin_swish_cann_sample, pin_bf16_rounding,
     pin_forward_bruteforce, pin_forward_torch, pin_forward_closed_forms,
     pin_gelu_grad_fd, pin_gelu_grad_torch_and_special_values, pin_hardswish_grad,
+    pin_group_norm_fd, pin_group_norm_torch, pin_group_norm_invariants,
 ]

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle.activations as oact
+import oracle.group_norm as ogn
 import oracle.numerics as onum
 import oracle.swiglu as osw
 import oracle.swish as osh
@@ -109,6 +110,63 @@ def _hardswish_kinks_closed(grad, x):
     return np.asarray(grad, np.float64) * np.where(x < -3.0, 0.0, np.where(x <= 3.0, x / 3.0 + 0.5, 1.0))
 
 
+def _gn_parts(dy, x, gamma, G, eps):
+    dy, x = np.asarray(dy, np.float64), np.asarray(x, np.float64)
+    N, C, S = x.shape
+    g = np.ones(C) if gamma is None else np.asarray(gamma, np.float64)
+    mu, _, rstd = ogn.group_norm_stats(x, G, eps)
+    xhat = (x.reshape(N, G, -1) - mu[:, :, None]) * rstd[:, :, None]
+    gdy = (dy * g[None, :, None]).reshape(N, G, -1)
+    return dy, x, N, C, S, g, rstd, xhat, gdy
+
+
+def _gn_drops_mean_term(dy, x, gamma, G, eps):
+    dy, x, N, C, S, g, rstd, xhat, gdy = _gn_parts(dy, x, gamma, G, eps)
+    m = xhat.shape[2]
+    dx = rstd[:, :, None] * (gdy - xhat * (gdy * xhat).sum(2, keepdims=True) / m)
+    return dx.reshape(N, C, S), (dy * xhat.reshape(N, C, S)).sum((0, 2)), dy.sum((0, 2))
+
+
+def _gn_drops_xhat_term(dy, x, gamma, G, eps):
+    dy, x, N, C, S, g, rstd, xhat, gdy = _gn_parts(dy, x, gamma, G, eps)
+    m = xhat.shape[2]
+    dx = rstd[:, :, None] * (gdy - gdy.sum(2, keepdims=True) / m)
+    return dx.reshape(N, C, S), (dy * xhat.reshape(N, C, S)).sum((0, 2)), dy.sum((0, 2))
+
+
+def _gn_gamma_outside_sums(dy, x, gamma, G, eps):
+    dy, x, N, C, S, g, rstd, xhat, gdy = _gn_parts(dy, x, gamma, G, eps)
+    m = xhat.shape[2]
+    gc = np.repeat(g.reshape(G, -1), S, axis=1)[None]  # gamma of each element, [1, G, m]
+    d = dy.reshape(N, G, -1)
+    dx = rstd[:, :, None] * gc * (d - d.sum(2, keepdims=True) / m - xhat * (d * xhat).sum(2, keepdims=True) / m)
+    return dx.reshape(N, C, S), (dy * xhat.reshape(N, C, S)).sum((0, 2)), dy.sum((0, 2))
+
+
+def _gn_var_without_eps_in_last_term(dy, x, gamma, G, eps):
+    dx, dgamma, dbeta = ogn.__dict__["_orig_gn"](dy, x, gamma, G, eps)
+    dy_, x_, N, C, S, g, rstd, xhat, gdy = _gn_parts(dy, x, gamma, G, eps)
+    m = xhat.shape[2]
+    mu, var, _ = ogn.group_norm_stats(x_, G, eps)
+    xc = x_.reshape(N, G, -1) - mu[:, :, None]
+    last_ok = xhat * (gdy * xhat).sum(2, keepdims=True) / m
+    with np.errstate(divide="ignore", invalid="ignore"):  # var = 0 in the one-element groups
+        last_bad = xc * (gdy * xc).sum(2, keepdims=True) / (m * var[:, :, None])
+    return dx + (rstd[:, :, None] * (last_ok - last_bad)).reshape(N, C, S), dgamma, dbeta
+
+
+def _gn_dgamma_without_xhat(dy, x, gamma, G, eps):
+    dx, _, dbeta = ogn.__dict__["_orig_gn"](dy, x, gamma, G, eps)
+    return dx, dbeta.copy(), dbeta
+
+
+def _gn_unbiased_var(x, G, eps):
+    xg = np.asarray(x, np.float64).reshape(x.shape[0], G, -1)
+    mu = xg.mean(axis=2)
+    var = xg.var(axis=2, ddof=1)
+    return mu, var, 1.0 / np.sqrt(var + eps)
+
+
 def _bf16_truncate(x):
     v = np.asarray(x, np.float64).astype(np.float32)
     return ((v.view(np.uint32) >> 16) << 16).view(np.float32).astype(np.float64)
@@ -132,6 +190,12 @@ MUTANTS = {
     "gelu_drops_x_phi": [(oact, "gelu_grad", _gelu_drops_x_phi)],
     "hardswish_slope_one_sixth": [(oact, "hardswish_grad", _hardswish_slope_sixth)],
     "hardswish_kinks_closed": [(oact, "hardswish_grad", _hardswish_kinks_closed)],
+    "gn_drops_mean_term": [(ogn, "group_norm_bwd", _gn_drops_mean_term)],
+    "gn_drops_xhat_term": [(ogn, "group_norm_bwd", _gn_drops_xhat_term)],
+    "gn_gamma_outside_sums": [(ogn, "group_norm_bwd", _gn_gamma_outside_sums)],
+    "gn_var_without_eps_in_last_term": [(ogn, "group_norm_bwd", _gn_var_without_eps_in_last_term)],
+    "gn_dgamma_without_xhat": [(ogn, "group_norm_bwd", _gn_dgamma_without_xhat)],
+    "gn_unbiased_var": [(ogn, "group_norm_stats", _gn_unbiased_var)],
 }
 
 
@@ -139,6 +203,7 @@ MUTANTS = {
 def test_planted_mistake_is_caught(name, monkeypatch):
     monkeypatch.setitem(osw.__dict__, "_orig_b", osw.swiglu_bwd_b)
     monkeypatch.setitem(osw.__dict__, "_orig_fwd", osw.swiglu_fwd)
+    monkeypatch.setitem(ogn.__dict__, "_orig_gn", ogn.group_norm_bwd)
     for mod, attr, fn in MUTANTS[name]:
         monkeypatch.setattr(mod, attr, fn)
     caught = []
