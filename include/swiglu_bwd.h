@@ -1,11 +1,15 @@
 /*
- * swiglu_bwd.h -- C ABI of the GB300 (sm_103a) SwiGLU-FFN backward and SwishGrad.
+ * swiglu_bwd.h -- C ABI of the GB300 (sm_103a) SwiGLU-FFN backward, SwishGrad,
+ * the sibling activation gradients and the GroupNorm backward.
  *
  * Operations (sources are web pages; each function cites the section it follows):
  *   [P1] "PyPTO-Gym in practice: the fused SwiGLU backward operator"
  *        (hnwysp.cn/news/34787)
  *   [P2] "SwishGrad in CANN ops-nn: principle, implementation and the
  *        aclnnSwishBackward guide" (bhfrc.com/news/37500)
+ *   [P3] "Beyond automatic differentiation: efficient custom backward
+ *        operators in Ascend C" (cann.csdn.net): activation gradients and the
+ *        GroupNorm backward
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -235,6 +239,36 @@ swg_status swish_grad(const void* grad, const void* x, const float* scale, void*
  * act is SWG_ERR_PARAM_INVALID). */
 swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x,
                     int64_t n, swg_dtype dtype, swg_stream_t stream);
+
+/* ---- GroupNorm backward -----------------------------------------------------
+ * [P3] GroupNorm section (revised version 3.1-3.2): for x, dy of shape
+ * [N, C, HxW] (NCHW, spatial dimensions flattened, contiguous) split into G
+ * groups of C/G consecutive channels per sample, m = (C/G) HxW elements per
+ * group, mu and the biased variance var of each group recomputed from x,
+ * rstd = 1/sqrt(var + eps), x_hat = (x - mu) rstd:
+ *   dx       = rstd (gamma_c dy - sum(gamma dy)/m - x_hat sum(gamma dy x_hat)/m),
+ *   dgamma_c = sum over samples and positions of dy x_hat,
+ *   dbeta_c  = sum over samples and positions of dy
+ * (the pages give dx; dgamma and dbeta are the standard parameter gradients).
+ * gamma [C] may be NULL (gamma = 1). dgamma, dbeta [C] are optional outputs
+ * (NULL: not computed); when either is given, `workspace` must hold at least
+ * group_norm_bwd_workspace_size(N, C, HxW, G) bytes (16-byte aligned), else
+ * SWG_ERR_WORKSPACE; without them the workspace is unused and may be NULL.
+ * All tensors share `dtype` (fp32 / fp16 / bf16), aligned to their element size
+ * (SWG_ERR_UNSUPPORTED otherwise); 16-byte aligned groups take the bulk-copy
+ * path, others plain loads. Math is fp32, sums in a fixed order (dgamma and
+ * dbeta added over samples in fp64); each output is rounded once (RNE);
+ * results are bitwise reproducible.
+ * Errors: G < 1, C not a multiple of G, a negative size or a negative / NaN eps
+ * -> SWG_ERR_PARAM_INVALID; N G > 2^28 -> SWG_ERR_UNSUPPORTED; x, dy or dx NULL
+ * with N C HxW > 0 -> SWG_ERR_NULLPTR; outputs overlapping inputs or each other
+ * -> SWG_ERR_PARAM_INVALID. Empty (N C HxW == 0): no dx work; dgamma, dbeta
+ * (sums over nothing) are written as zeros. */
+size_t group_norm_bwd_workspace_size(int64_t N, int64_t C, int64_t HxW, int64_t G);
+swg_status group_norm_bwd(const void* dy, const void* x, const void* gamma, void* dx,
+                          void* dgamma, void* dbeta, int64_t N, int64_t C, int64_t HxW,
+                          int64_t G, float eps, swg_dtype dtype, void* workspace,
+                          size_t workspace_bytes, swg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) SwiGLU-FFN backward and SwishGrad.
+"""GB300 (sm_103a) SwiGLU-FFN backward, SwishGrad, activation gradients and
+the GroupNorm backward.
 
 The compute runs in hand-written CUDA kernels behind the C ABI of
 include/swiglu_bwd.h; this package is the thin Python binding over it.
@@ -7,6 +8,8 @@ include/swiglu_bwd.h; this package is the thin Python binding over it.
 from ._binding import (  # noqa: F401
     EXPORTS,
     act_grad,
+    group_norm_bwd,
+    group_norm_bwd_workspace_size,
     LIB_PATH,
     SWG_ACCUMULATE,
     SWG_FUSED,

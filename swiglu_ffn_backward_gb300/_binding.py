@@ -47,6 +47,7 @@ EXPORTS = (
     "swiglu_bwd_w_fused_workspace_size", "swiglu_bwd_w_fused",
     "swiglu_fwd",
     "act_grad",
+    "group_norm_bwd_workspace_size", "group_norm_bwd",
 )
 
 
@@ -81,6 +82,10 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, P]
     lib.swiglu_fwd.restype = st
     lib.act_grad.argtypes = [P, P, ctypes.c_int, P, I64, ctypes.c_int, P]
+    lib.group_norm_bwd_workspace_size.restype = SZ
+    lib.group_norm_bwd_workspace_size.argtypes = [I64, I64, I64, I64]
+    lib.group_norm_bwd.restype = st
+    lib.group_norm_bwd.argtypes = [P] * 6 + [I64, I64, I64, I64, ctypes.c_float, ctypes.c_int, P, SZ, P]
     lib.act_grad.restype = st
     lib.swiglu_bwd_workspace_size.argtypes = [I64, I64, I64, U]
     lib.swiglu_bwd_workspace_size.restype = SZ
@@ -344,6 +349,48 @@ def act_grad(grad, x, act: str, grad_x=None, stream=None):
     _check(lib.act_grad(grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
                         _DTYPE[grad.dtype], _stream(stream)), "act_grad")
     return grad_x
+
+
+def group_norm_bwd_workspace_size(N: int, C: int, HxW: int, G: int) -> int:
+    return int(lib.group_norm_bwd_workspace_size(N, C, HxW, G))
+
+
+def group_norm_bwd(dy, x, num_groups: int, gamma=None, eps: float = 1e-5, params: bool = True,
+                   dx=None, dgamma=None, dbeta=None, workspace=None, stream=None):
+    """GroupNorm backward for x, dy of shape [N, C, *spatial] (fp32/fp16/bf16):
+    returns (dx, dgamma, dbeta); dgamma and dbeta are None when params is False.
+    gamma [C] (same dtype) may be None (= ones). Statistics are recomputed from x."""
+    if not (isinstance(dy, torch.Tensor) and isinstance(x, torch.Tensor) and dy.is_cuda and x.is_cuda):
+        raise TypeError("dy and x must be CUDA tensors")
+    if dy.dtype != x.dtype or dy.shape != x.shape:
+        raise ValueError("dy and x must have the same dtype and shape")
+    if x.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    if x.dim() < 2:
+        raise ValueError("x must be [N, C, *spatial]")
+    N, C = x.shape[0], x.shape[1]
+    HxW = 1
+    for d in x.shape[2:]:
+        HxW *= d
+    if gamma is not None:
+        if not (isinstance(gamma, torch.Tensor) and gamma.is_cuda) or gamma.dtype != x.dtype or gamma.numel() != C:
+            raise ValueError("gamma must be a CUDA tensor of C elements with x's dtype")
+        gamma = gamma.contiguous()
+    dy, x = dy.contiguous(), x.contiguous()
+    if dx is None:
+        dx = torch.empty_like(x)
+    if params:
+        if dgamma is None:
+            dgamma = torch.empty(C, dtype=x.dtype, device=x.device)
+        if dbeta is None:
+            dbeta = torch.empty(C, dtype=x.dtype, device=x.device)
+        ws = _workspace(group_norm_bwd_workspace_size(N, C, HxW, num_groups), x.device, workspace)
+    else:
+        dgamma = dbeta = ws = None
+    _check(lib.group_norm_bwd(dy.data_ptr(), x.data_ptr(), _ptr(gamma), dx.data_ptr(), _ptr(dgamma), _ptr(dbeta),
+                              N, C, HxW, num_groups, float(eps), _DTYPE[x.dtype], _ptr(ws), _nbytes(ws),
+                              _stream(stream)), "group_norm_bwd")
+    return dx, dgamma, dbeta
 
 
 def swiglu_bwd_b_noalloc(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, stream=None):

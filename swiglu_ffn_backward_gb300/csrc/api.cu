@@ -129,6 +129,51 @@ swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x, 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------- GroupNorm backward
+size_t group_norm_bwd_workspace_size(int64_t N, int64_t C, int64_t HxW, int64_t G) {
+  if (N <= 0 || C <= 0 || HxW <= 0 || G <= 0 || C % G != 0) return 0;
+  return swg::gn_workspace_bytes(N, C, G);
+}
+
+swg_status group_norm_bwd(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma, void* dbeta,
+                          int64_t N, int64_t C, int64_t HxW, int64_t G, float eps, swg_dtype dtype,
+                          void* workspace, size_t workspace_bytes, swg_stream_t stream) {
+  if (dtype != SWG_F32 && dtype != SWG_F16 && dtype != SWG_BF16) return SWG_ERR_PARAM_INVALID;
+  if (N < 0 || C < 0 || HxW < 0 || G < 1 || C % G != 0 || !(eps >= 0.0f)) return SWG_ERR_PARAM_INVALID;
+  if (N > kMaxDim || C > kMaxDim || HxW > (int64_t(1) << 40) || N * G > (int64_t(1) << 28))
+    return SWG_ERR_UNSUPPORTED;
+  const int64_t es = dtype == SWG_F32 ? 4 : 2;
+  const int64_t n = N * C * HxW;
+  const bool params = dgamma != nullptr || dbeta != nullptr;
+  const uintptr_t mask = static_cast<uintptr_t>(es - 1);
+  auto misaligned = [&](const void* p) { return (reinterpret_cast<uintptr_t>(p) & mask) != 0; };
+  if (misaligned(dy) || misaligned(x) || misaligned(gamma) || misaligned(dx) || misaligned(dgamma) ||
+      misaligned(dbeta))
+    return SWG_ERR_UNSUPPORTED;
+  if (n > 0 && (dy == nullptr || x == nullptr || dx == nullptr)) return SWG_ERR_NULLPTR;
+  const Range outs[3] = {rng(dx, n * es), rng(dgamma, dgamma ? C * es : 0), rng(dbeta, dbeta ? C * es : 0)};
+  const Range ins[3] = {rng(dy, n * es), rng(x, n * es), rng(gamma, gamma ? C * es : 0)};
+  if (any_overlap(outs, 3, ins, 3)) return SWG_ERR_PARAM_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n == 0) {
+    if (C == 0 || !params) return SWG_OK;
+    swg_status s = check_device();
+    if (s != SWG_OK) return s;
+    if (dgamma != nullptr && cudaMemsetAsync(dgamma, 0, static_cast<size_t>(C * es), st) != cudaSuccess)
+      return SWG_ERR_CUDA;
+    if (dbeta != nullptr && cudaMemsetAsync(dbeta, 0, static_cast<size_t>(C * es), st) != cudaSuccess)
+      return SWG_ERR_CUDA;
+    return SWG_OK;
+  }
+  if (params && (workspace == nullptr || !aligned16(workspace) ||
+                 workspace_bytes < swg::gn_workspace_bytes(N, C, G)))
+    return SWG_ERR_WORKSPACE;
+  swg_status s = check_device();
+  if (s != SWG_OK) return s;
+  return cuda_status(swg::launch_group_norm_bwd(dy, x, gamma, dx, dgamma, dbeta, N, C, HxW, G, eps,
+                                                static_cast<int>(dtype), params ? workspace : nullptr, st));
+}
+
 swg_status swish_grad(const void* grad, const void* x, const float* scale, void* grad_x, int64_t n,
                       swg_dtype dtype, swg_stream_t stream) {
   swg_status st = check_elementwise(grad, x, grad_x, n, dtype);

@@ -1,0 +1,514 @@
+// GroupNorm backward: dx, dgamma, dbeta for x, dy of shape [N, C, HxW] (NCHW
+// with the spatial dimensions flattened) and gamma of shape [C].
+//
+// Source: "Beyond automatic differentiation: efficient custom backward
+// operators in Ascend C", GroupNorm section: revised version 3.1 (the formula,
+// gamma inside the group sums) and 3.2 (groups processed independently, the
+// statistics recomputed from x in the backward). With m = (C / G) HxW elements
+// per (sample, group), mu and the biased var over the group,
+// rstd = 1 / sqrt(var + eps) and x_hat = (x - mu) rstd:
+//   dx       = rstd (gamma_c dy - A / m - x_hat B / m),  A = sum gamma dy,  B = sum gamma dy x_hat
+//   dgamma_c = sum over samples and positions of dy x_hat,  dbeta_c = the same sum of dy
+//
+// One cluster of S CTAs (S <= 8) per (sample, group). CTA k of the cluster owns
+// a contiguous slice of the group and brings its x and dy into shared memory
+// with bulk copies, in up to four parts with one mbarrier each (pass 1 starts on
+// the first part while the others arrive), so HBM sees each input once:
+//   pass 1    shifted sums, shift K = the group's first x (the shifted-data
+//             variance of Chan, Golub and LeVeque, "Algorithms for computing the
+//             sample variance: analysis and recommendations", 1983):
+//             sum(x - K), sum((x - K)^2), sum(gamma dy), sum(gamma dy (x - K)),
+//             and per channel sum(dy), sum(dy (x - K));
+//   exchange  the four group sums through distributed shared memory, added in
+//             cluster-rank order by every CTA (the same value in all of them);
+//             the coefficients are formed in fp32 (this part's FP64 rate is a
+//             small fraction of its FP32 rate, and this step is on every CTA's
+//             critical path);
+//   pass 2    dx = (rstd gamma_c) dy + c2 + c3 ((x - K) - d), d = mu - K, written
+//             over x in shared memory and stored with bulk copies part by part.
+// A slice longer than the shared-memory stage is taken stage by stage and read
+// again for pass 2. Tensors whose groups do not start on 16-byte boundaries
+// take plain loads and stores. dgamma, dbeta: the per-(sample, group, slice,
+// channel) partials and the per-(sample, group) d and rstd go to the
+// workspace; a second kernel adds them over samples and slices in a fixed
+// order in fp64, so every output is bitwise reproducible.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "swg_device.cuh"
+#include "swg_launch.h"
+
+namespace swg {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kParts = 4;                  // bulk-copy parts per stage, one mbarrier each
+constexpr int kStageBytes = 96 * 1024;     // largest x and dy stage (slices longer than it are streamed)
+constexpr int kSliceBytes = 48 * 1024;     // target x and dy bytes per CTA (measured: 48 KB over 24 and 12)
+constexpr int kMinBlocks = 4;              // resident CTAs per SM the register budget is set for
+constexpr int kMaxCluster = 8;             // portable cluster size
+constexpr int64_t kMinSlice = 2048;        // elements: smaller slices do not pay for the cluster exchange
+
+enum : int { kPlain = 0, kBulk = 1, kBulkVec = 2 };
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// a 16-byte vector of T <-> floats
+template <typename T>
+struct Vec16 {
+  static constexpr int kN = 16 / static_cast<int>(sizeof(T));
+  union {
+    uint4 u;
+    T e[kN];
+  };
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct GnArgs {
+  const void* x;
+  const void* dy;
+  const void* gamma;  // null: gamma = 1
+  void* dx;
+  float* stats;       // [N G][2]: d = mu - K, rstd        (null when dgamma, dbeta are not wanted)
+  float* part;        // [N G][S][Cg][2]: sum dy, sum dy (x - K) per channel piece (null likewise)
+  int64_t hw;         // HxW
+  int64_t m;          // Cg HxW
+  int64_t slice;      // elements per CTA (multiple of 8)
+  int64_t stage;      // shared-memory stage in elements per tensor (multiple of 8)
+  int cg;             // channels per group
+  int groups;         // G
+  int S;              // cluster size
+  float eps;
+  uint32_t* status;
+};
+
+template <typename T, int kMode>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  T* xs = reinterpret_cast<T*>(smem);
+  T* ds = reinterpret_cast<T*>(smem + a.stage * static_cast<int64_t>(sizeof(T)));
+  __shared__ __align__(8) uint64_t bar[kParts];
+  __shared__ float red[2][kWarps][2];
+  __shared__ float wsum[kWarps][4];
+  __shared__ float gsum[4];
+  __shared__ float tot[4];
+  __shared__ float coef[4];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t grp = blockIdx.x / a.S;
+  const int g = static_cast<int>(grp % a.groups);
+  const int64_t base = grp * a.m;
+  const T* xg = static_cast<const T*>(a.x) + base;
+  const T* dg = static_cast<const T*>(a.dy) + base;
+  T* og = static_cast<T*>(a.dx) + base;
+  const T* gam = a.gamma != nullptr ? static_cast<const T*>(a.gamma) + static_cast<int64_t>(g) * a.cg : nullptr;
+  const int64_t lo = min(a.m, static_cast<int64_t>(rank) * a.slice);
+  const int64_t hi = min(a.m, lo + a.slice);
+  const int64_t nst = (hi - lo + a.stage - 1) / a.stage;  // stages of this slice
+  const float K = to_f(xg[0]);
+  constexpr int V = Vec16<T>::kN;
+
+  if (kMode != kPlain && tid == 0) {
+    for (int p = 0; p < kParts; ++p) mbar_init(&bar[p], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;  // bit p: parity of the next completion of bar[p]
+  bool timed_out = false;
+
+  // stage [c0, c0 + clen) of the group -> xs, ds; parts of plen elements (multiple of 8)
+  auto plen_of = [&](int64_t clen) -> int64_t {
+    if (kMode == kPlain) return clen;
+    const int64_t q = (clen + kParts - 1) / kParts;
+    return (q + 7) & ~int64_t(7);
+  };
+  auto issue_stage = [&](int64_t c0, int64_t clen) {
+    if (kMode == kPlain) {
+      for (int64_t i = tid; i < clen; i += kThreads) {
+        xs[i] = xg[c0 + i];
+        ds[i] = dg[c0 + i];
+      }
+      __syncthreads();
+    } else if (tid == 0) {
+      const int64_t plen = plen_of(clen);
+      for (int p = 0; p < kParts; ++p) {
+        const int64_t s0 = p * plen, s1 = min(clen, s0 + plen);
+        if (s0 >= s1) break;
+        const uint32_t bytes = static_cast<uint32_t>((s1 - s0) * static_cast<int64_t>(sizeof(T)));
+        mbar_arrive_expect_tx(&bar[p], 2 * bytes);
+        bulk_g2s(xs + s0, xg + c0 + s0, bytes, &bar[p]);
+        bulk_g2s(ds + s0, dg + c0 + s0, bytes, &bar[p]);
+      }
+    }
+  };
+  auto wait_part = [&](int p) {
+    if (kMode == kPlain) return;
+    if (!mbar_wait(&bar[p], (phase >> p) & 1u)) timed_out = true;
+    phase ^= 1u << p;
+  };
+
+  // ---------------------------------------------------------------- pass 1
+  // Channels are tracked incrementally (no integer division in the loops): j is
+  // the channel at stage-local position s and jend the stage-local end of j.
+  float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f;
+  float sd = 0.f, se = 0.f;  // this thread's sums of dy, dy (x - K) over the open channel
+  int cur_j = -1;            // thread 0: channel whose partials are being gathered
+  float cur_d = 0.f, cur_e = 0.f;
+  int rb = 0;                // red[] buffer of the next channel reduction
+  const bool want_part = a.part != nullptr;
+  float* part = want_part ? a.part + (grp * a.S + rank) * static_cast<int64_t>(a.cg) * 2 : nullptr;
+  // the open channel j is done (or leaves this stage): gamma-weight the thread's
+  // sums into the group sums; reduce them over the CTA for the channel partials
+  auto close_channel = [&](int j) {
+    const float gj = gam != nullptr ? to_f(gam[j]) : 1.0f;
+    ga = fmaf(gj, sd, ga);
+    ge = fmaf(gj, se, ge);
+    if (want_part) {
+      const float D = warp_sum(sd), E = warp_sum(se);
+      if (lane == 0) {
+        red[rb][warp][0] = D;
+        red[rb][warp][1] = E;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float Ds = 0.f, Es = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          Ds += red[rb][w][0];
+          Es += red[rb][w][1];
+        }
+        if (j == cur_j) {
+          cur_d += Ds;
+          cur_e += Es;
+        } else {
+          if (cur_j >= 0) {
+            part[2 * cur_j] = cur_d;
+            part[2 * cur_j + 1] = cur_e;
+          }
+          cur_j = j;
+          cur_d = Ds;
+          cur_e = Es;
+        }
+      }
+      rb ^= 1;
+    }
+    sd = 0.f;
+    se = 0.f;
+  };
+
+  for (int64_t st = 0; st < nst; ++st) {
+    const int64_t c0 = lo + st * a.stage;
+    const int clen = static_cast<int>(min(a.stage, hi - c0));
+    if (st > 0) __syncthreads();  // everyone is done with the previous stage
+    issue_stage(c0, clen);
+    const int plen = static_cast<int>(plen_of(clen));
+    int j = static_cast<int>(c0 / a.hw);
+    int64_t jend = (j + 1) * a.hw - c0;
+    bool open = false;
+    for (int p = 0; p * plen < clen; ++p) {
+      wait_part(p);
+      const int s1 = min(clen, (p + 1) * plen);
+      for (int s = p * plen; s < s1;) {
+        const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
+        if (kMode == kBulkVec) {
+          for (int v = s / V + tid; v < e / V; v += kThreads) {
+            Vec16<T> vx, vd;
+            vx.u = reinterpret_cast<const uint4*>(xs)[v];
+            vd.u = reinterpret_cast<const uint4*>(ds)[v];
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+              const float xk = to_f(vx.e[i]) - K, dv = to_f(vd.e[i]);
+              sx += xk;
+              sxx = fmaf(xk, xk, sxx);
+              sd += dv;
+              se = fmaf(dv, xk, se);
+            }
+          }
+        } else {
+          for (int i = s + tid; i < e; i += kThreads) {
+            const float xk = to_f(xs[i]) - K, dv = to_f(ds[i]);
+            sx += xk;
+            sxx = fmaf(xk, xk, sxx);
+            sd += dv;
+            se = fmaf(dv, xk, se);
+          }
+        }
+        open = true;
+        if (e == jend) {
+          close_channel(j);
+          open = false;
+          ++j;
+          jend += a.hw;
+        }
+        s = e;
+      }
+    }
+    if (open) close_channel(j);  // channel j goes on past this stage or this slice
+  }
+  if (want_part) {
+    if (tid == 0 && cur_j >= 0) {
+      part[2 * cur_j] = cur_d;
+      part[2 * cur_j + 1] = cur_e;
+    }
+    // channels of the group outside this slice get zeros
+    const int jlo = hi > lo ? static_cast<int>(lo / a.hw) : a.cg;
+    const int jhi = hi > lo ? static_cast<int>((hi - 1) / a.hw) : -1;
+    for (int jj = tid; jj < a.cg; jj += kThreads) {
+      if (jj < jlo || jj > jhi) {
+        part[2 * jj] = 0.f;
+        part[2 * jj + 1] = 0.f;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- exchange
+  sx = warp_sum(sx);
+  sxx = warp_sum(sxx);
+  ga = warp_sum(ga);
+  ge = warp_sum(ge);
+  if (lane == 0) {
+    wsum[warp][0] = sx;
+    wsum[warp][1] = sxx;
+    wsum[warp][2] = ga;
+    wsum[warp][3] = ge;
+  }
+  __syncthreads();
+  if (tid < 4) {
+    float v = 0.f;
+    for (int w = 0; w < kWarps; ++w) v += wsum[w][tid];
+    gsum[tid] = v;
+  }
+  cluster_sync();  // every CTA's gsum is written
+  if (tid < 4) {
+    float t[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < a.S) t[r] = ld_cluster_f32(&gsum[tid], static_cast<uint32_t>(r));
+    float v = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < a.S) v += t[r];
+    tot[tid] = v;
+  }
+  cluster_sync();  // every CTA is done reading its peers (and tot is visible in the CTA)
+  if (tid == 0) {
+    // fp32 and a fixed order: the same coefficients in every CTA of the cluster
+    const float inv_m = 1.0f / static_cast<float>(a.m);
+    const float d = tot[0] * inv_m;                              // mu - K
+    const float var = fmaxf(fmaf(tot[1], inv_m, -d * d), 0.0f);  // biased
+    const float rstd = rsqrtf(var + a.eps);
+    const float B = rstd * fmaf(-d, tot[2], tot[3]);             // sum gamma dy x_hat
+    coef[0] = d;
+    coef[1] = rstd;
+    coef[2] = -rstd * tot[2] * inv_m;
+    coef[3] = -rstd * rstd * B * inv_m;
+    if (a.stats != nullptr && rank == 0) {
+      a.stats[2 * grp] = d;
+      a.stats[2 * grp + 1] = rstd;
+    }
+  }
+  __syncthreads();
+  const float d = coef[0], c1 = coef[1], c2 = coef[2], c3 = coef[3];
+
+  // ---------------------------------------------------------------- pass 2
+  for (int64_t st = 0; st < nst; ++st) {
+    const int64_t c0 = lo + st * a.stage;
+    const int clen = static_cast<int>(min(a.stage, hi - c0));
+    const bool reload = nst > 1;
+    if (reload) {
+      if (kMode != kPlain && tid == 0) bulk_wait_read<0>();  // the previous stage's stores have read xs
+      __syncthreads();
+      issue_stage(c0, clen);
+    }
+    const int plen = static_cast<int>(plen_of(clen));
+    int j = static_cast<int>(c0 / a.hw);
+    int64_t jend = (j + 1) * a.hw - c0;
+    float aj = c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+    for (int p = 0; p * plen < clen; ++p) {
+      if (reload) wait_part(p);
+      const int s0 = p * plen, s1 = min(clen, s0 + plen);
+      for (int s = s0; s < s1;) {
+        const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
+        if (kMode == kBulkVec) {
+          for (int v = s / V + tid; v < e / V; v += kThreads) {
+            Vec16<T> vx, vd, vo;
+            vx.u = reinterpret_cast<const uint4*>(xs)[v];
+            vd.u = reinterpret_cast<const uint4*>(ds)[v];
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+              vo.e[i] = from_f<T>(fmaf(aj, to_f(vd.e[i]), fmaf(c3, (to_f(vx.e[i]) - K) - d, c2)));
+            reinterpret_cast<uint4*>(xs)[v] = vo.u;
+          }
+        } else {
+          for (int i = s + tid; i < e; i += kThreads)
+            xs[i] = from_f<T>(fmaf(aj, to_f(ds[i]), fmaf(c3, (to_f(xs[i]) - K) - d, c2)));
+        }
+        if (e == jend) {
+          ++j;
+          jend += a.hw;
+          if (j < a.cg) aj = c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+        }
+        s = e;
+      }
+      if (kMode != kPlain) {
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          bulk_s2g(og + c0 + s0, xs + s0, static_cast<uint32_t>((s1 - s0) * static_cast<int64_t>(sizeof(T))));
+          bulk_commit();
+        }
+      }
+    }
+    if (kMode == kPlain) {
+      __syncthreads();
+      for (int i = tid; i < clen; i += kThreads) og[c0 + i] = xs[i];
+    }
+  }
+  if (kMode != kPlain && tid == 0) bulk_wait_read<0>();  // the stores have read shared memory
+  if (timed_out && a.status != nullptr) atomicOr(a.status, kStatusTimeout);
+}
+
+// dgamma_c = sum_n rstd_n sum_k (E - d_n D),  dbeta_c = sum_n sum_k D; one warp per channel, fixed order
+template <typename T>
+__global__ void __launch_bounds__(256) gn_param_kernel(const float* __restrict__ stats, const float* __restrict__ part,
+                                                       T* dgamma, T* dbeta, int64_t N, int C, int G, int cg, int S) {
+  const int c = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const int g = c / cg, j = c % cg;
+  double sb = 0.0, sg = 0.0;
+  for (int64_t t = lane; t < N * S; t += 32) {
+    const int64_t n = t / S, k = t % S, grp = n * G + g;
+    const float* p = part + ((grp * S + k) * cg + j) * 2;
+    const double D = p[0], E = p[1];
+    sb += D;
+    sg += static_cast<double>(stats[2 * grp + 1]) * (E - static_cast<double>(stats[2 * grp]) * D);
+  }
+  sb = warp_sum(sb);
+  sg = warp_sum(sg);
+  if (lane == 0) {
+    if (dbeta != nullptr) dbeta[c] = from_f<T>(static_cast<float>(sb));
+    if (dgamma != nullptr) dgamma[c] = from_f<T>(static_cast<float>(sg));
+  }
+}
+
+inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+template <typename T, int kMode>
+cudaError_t launch_mode(const GnArgs& a, int64_t groups_total, cudaStream_t stream) {
+  const size_t smem = 2 * static_cast<size_t>(a.stage) * sizeof(T);
+  static bool attr_set = false;  // the attribute allows the largest stage; set once per instantiation
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(gn_bwd_kernel<T, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kStageBytes);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(groups_total * a.S));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gn_bwd_kernel<T, kMode>, a);
+}
+
+template <typename T>
+cudaError_t run(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t N,
+                int64_t C, int64_t HxW, int64_t G, float eps, void* ws, cudaStream_t stream) {
+  const GnPlan plan = gn_plan(N, C, HxW, G, static_cast<int>(sizeof(T)), device_sm_count());
+  const bool params = dgamma != nullptr || dbeta != nullptr;
+  GnArgs a;
+  a.x = x;
+  a.dy = dy;
+  a.gamma = gamma;
+  a.dx = dx;
+  a.stats = params ? static_cast<float*>(ws) : nullptr;
+  a.part = params ? reinterpret_cast<float*>(static_cast<char*>(ws) + al256(static_cast<size_t>(N * G) * 8))
+                  : nullptr;
+  a.hw = HxW;
+  a.m = (C / G) * HxW;
+  a.slice = plan.slice;
+  a.stage = plan.stage;
+  a.cg = static_cast<int>(C / G);
+  a.groups = static_cast<int>(G);
+  a.S = plan.S;
+  a.eps = eps;
+  a.status = status_word_ptr();
+  const int64_t es = sizeof(T);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dy) |
+                         reinterpret_cast<uintptr_t>(dx)) & 15u) == 0 &&
+                       (a.m * es) % 16 == 0;
+  const bool vec = aligned && HxW % (16 / es) == 0;
+  cudaError_t err = vec       ? launch_mode<T, kBulkVec>(a, N * G, stream)
+                    : aligned ? launch_mode<T, kBulk>(a, N * G, stream)
+                              : launch_mode<T, kPlain>(a, N * G, stream);
+  if (err != cudaSuccess || !params) return err;
+  const int64_t threads = C * 32;
+  gn_param_kernel<T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+      a.stats, a.part, static_cast<T*>(dgamma), static_cast<T*>(dbeta), N, static_cast<int>(C),
+      static_cast<int>(G), a.cg, a.S);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+GnPlan gn_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int num_sms) {
+  GnPlan p;
+  const int64_t m = (C / G) * HxW, ng = N * G;
+  p.stage = kStageBytes / (2 * elem_bytes);
+  const int64_t target = kSliceBytes / (2 * elem_bytes);
+  int64_t S = (m + target - 1) / target;  // slices of about the target size
+  S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
+  // more CTAs per group while the grid is under two CTAs per SM and slices stay long
+  while (S < kMaxCluster && ng * S < 2 * static_cast<int64_t>(num_sms) && m / (S + 1) >= kMinSlice) ++S;
+  p.S = static_cast<int>(S);
+  p.slice = (((m + S - 1) / S) + 7) & ~int64_t(7);
+  if (p.slice < p.stage) p.stage = p.slice;  // shared memory for one resident slice
+  return p;
+}
+
+size_t gn_workspace_bytes(int64_t N, int64_t C, int64_t G) {
+  // stats [N G][2] + partials [N G][S <= 8][C / G][2], fp32
+  return al256(static_cast<size_t>(N * G) * 8) + al256(static_cast<size_t>(N * C) * kMaxCluster * 8);
+}
+
+cudaError_t launch_group_norm_bwd(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma,
+                                  void* dbeta, int64_t N, int64_t C, int64_t HxW, int64_t G, float eps, int dtype,
+                                  void* ws, cudaStream_t stream) {
+  switch (dtype) {
+    case 0: return run<float>(dy, x, gamma, dx, dgamma, dbeta, N, C, HxW, G, eps, ws, stream);
+    case 1: return run<__half>(dy, x, gamma, dx, dgamma, dbeta, N, C, HxW, G, eps, ws, stream);
+    case 2: return run<__nv_bfloat16>(dy, x, gamma, dx, dgamma, dbeta, N, C, HxW, G, eps, ws, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace swg

@@ -55,6 +55,20 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
                           uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
                           cudaStream_t stream, bool accumulate = false);
 
+// ---- GroupNorm backward (group_norm_bwd.cu); dtype 0 = f32, 1 = f16, 2 = bf16
+struct GnPlan {
+  int S;          // CTAs (one cluster) per (sample, group), 1..8
+  int64_t slice;  // group elements per CTA (multiple of 8)
+  int64_t stage;  // shared-memory stage per tensor, elements
+};
+GnPlan gn_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int num_sms);
+// workspace for dgamma / dbeta: per-(sample, group) statistics + per-channel partials
+size_t gn_workspace_bytes(int64_t N, int64_t C, int64_t G);
+// dx always; dgamma, dbeta when non-null (then ws holds gn_workspace_bytes); gamma null = ones
+cudaError_t launch_group_norm_bwd(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma,
+                                  void* dbeta, int64_t N, int64_t C, int64_t HxW, int64_t G, float eps, int dtype,
+                                  void* ws, cudaStream_t stream);
+
 // module status word (timeouts)
 cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream);
 // device address of the status word on the current device (for kernels in other files)

@@ -1,4 +1,5 @@
-"""Seeded synthetic workloads for the SwiGLU-FFN backward and SwishGrad.
+"""Seeded synthetic workloads for the SwiGLU-FFN backward, SwishGrad and the
+GroupNorm backward.
 
 This package holds only input recipes (shapes, value distributions, seeds) and
 the code that draws them. It contains none of the method's arithmetic, so both
@@ -7,9 +8,12 @@ computation.
 """
 
 from .workloads import (  # noqa: F401
+    GROUP_NORM_CONFIGS,
+    GROUP_NORM_EPS,
     SWIGLU_CONFIGS,
     SWISH_CONFIG,
     SwigluShape,
+    group_norm_inputs,
     swiglu_fwd_biases,
     swiglu_inputs,
     swish_inputs,

@@ -15,6 +15,14 @@ randn from one generator seeded with the workload's seed, multiplied by its
 scale, then rounded to bf16 (round-to-nearest-even, torch's conversion).
 SwishGrad draws x then grad, in fp32, then converts to the I/O dtype.
 
+GroupNorm backward (the Ascend C backward blog post: an SD v1.5 UNet at
+batch 2 and 512 x 512, whose largest GroupNorm input is [2, 320, 64, 64] with
+32 groups, and ResNet-50 with GroupNorm, whose stage-1 activations at batch 32
+are [32, 256, 56, 56]; fp16 in the post's kernel): per (sample, group) a mean
+drawn from U(-2, 2) and a spread from U(0.5, 2), x = mean + spread * randn;
+dy = randn; gamma = 1 + 0.5 randn; eps 1e-5. Draw order: the per-group means,
+spreads, x's randn, dy, gamma, in fp32, then converted to the I/O dtype.
+
 The generator device is a parameter: the CPU and CUDA generators give
 different streams for the same seed, so a caller that compares two
 implementations must feed both from ONE draw (draw once, copy to the other
@@ -103,6 +111,29 @@ def swiglu_fwd_biases(shape: SwigluShape, device: str | torch.device = "cpu",
     b = [torch.randn(N, generator=gen, device=device, dtype=torch.float32).mul_(std).to(torch.bfloat16)
          for _ in range(2)]
     return b[0], b[1]
+
+
+GROUP_NORM_CONFIGS = {
+    # name: (N, C, HxW, G)
+    "tiny": (2, 8, 12, 4),
+    "sd_unet_64x64": (2, 320, 64 * 64, 32),
+    "resnet50_stage1_b32": (32, 256, 56 * 56, 32),
+    "vae_512x512": (1, 128, 512 * 512, 32),
+}
+GROUP_NORM_EPS = 1e-5
+
+
+def group_norm_inputs(N: int, C: int, HxW: int, G: int, dtype: torch.dtype,
+                      device: str | torch.device = "cpu", seed: int = 3) -> tuple:
+    """Draw (dy, x, gamma) for the GroupNorm backward, x and dy as [N, C, HxW]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    mean = torch.rand(N, G, 1, generator=gen, device=device).mul_(4.0).sub_(2.0)
+    spread = torch.rand(N, G, 1, generator=gen, device=device).mul_(1.5).add_(0.5)
+    x = torch.randn(N, G, (C // G) * HxW, generator=gen, device=device).mul_(spread).add_(mean)
+    dy = torch.randn(N, C, HxW, generator=gen, device=device)
+    gamma = torch.randn(C, generator=gen, device=device).mul_(0.5).add_(1.0)
+    return dy.to(dtype), x.reshape(N, C, HxW).to(dtype), gamma.to(dtype)
 
 
 def swish_inputs(n: int, dtype: torch.dtype, device: str | torch.device = "cpu",

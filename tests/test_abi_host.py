@@ -174,3 +174,44 @@ def test_act_grad_argument_checks(swg):
     assert lib.act_grad(FAKE, None, 1, FAKE + 8192, 10, b.SWG_F32, None) == b.SWG_ERR_NULLPTR
     assert lib.act_grad(FAKE, FAKE + 4096, 1, FAKE + 16, 100, b.SWG_F32, None) == b.SWG_ERR_PARAM_INVALID
     assert lib.act_grad(None, None, 2, None, 0, b.SWG_BF16, None) == b.SWG_OK  # empty
+
+
+def test_group_norm_argument_checks(swg):
+    lib, b = _lib(swg)
+    gn = lib.group_norm_bwd
+    A = [FAKE + i * 0x1000000 for i in range(6)]  # dy, x, gamma, dx, dgamma, dbeta
+    ws_ok = lib.group_norm_bwd_workspace_size(2, 8, 12, 4)
+    assert ws_ok > 0 and lib.group_norm_bwd_workspace_size(2, 8, 12, 3) == 0
+    assert lib.group_norm_bwd_workspace_size(0, 8, 12, 4) == 0
+    # G < 1, C not a multiple of G, negative sizes, NaN / negative eps, bad dtype
+    assert gn(*A, 2, 8, 12, 0, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    assert gn(*A, 2, 8, 12, 3, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    assert gn(*A, -1, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    assert gn(*A, 2, 8, 12, 4, float("nan"), b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    assert gn(*A, 2, 8, 12, 4, -1.0, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    assert gn(*A, 2, 8, 12, 4, 1e-5, 9, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    # too many (sample, group) pairs for the grid
+    assert gn(*A, 1 << 20, 1 << 9, 1, 1 << 9, 1e-5, b.SWG_F32, FAKE, 1 << 40, None) == b.SWG_ERR_UNSUPPORTED
+    # NULL x, dy or dx for a non-empty tensor
+    for i in (0, 1, 3):
+        args = list(A)
+        args[i] = None
+        assert gn(*args, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_NULLPTR
+    # pointers not aligned to the element size
+    args = list(A)
+    args[1] = FAKE + 2
+    assert gn(*args, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_UNSUPPORTED
+    # dx overlapping x; dgamma overlapping gamma
+    args = list(A)
+    args[3] = A[1] + 64
+    assert gn(*args, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    args = list(A)
+    args[4] = A[2]
+    assert gn(*args, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
+    # dgamma / dbeta wanted: workspace missing, short or misaligned
+    assert gn(*A, 2, 8, 12, 4, 1e-5, b.SWG_F32, None, 0, None) == b.SWG_ERR_WORKSPACE
+    assert gn(*A, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE, ws_ok - 1, None) == b.SWG_ERR_WORKSPACE
+    assert gn(*A, 2, 8, 12, 4, 1e-5, b.SWG_F32, FAKE + 8, ws_ok, None) == b.SWG_ERR_WORKSPACE
+    # empty without parameter gradients: nothing to do, no device needed, NULL data pointers accepted
+    assert gn(None, None, None, None, None, None, 0, 8, 12, 4, 1e-5, b.SWG_BF16, None, 0, None) == b.SWG_OK
+    assert gn(None, None, None, None, None, None, 2, 8, 0, 4, 1e-5, b.SWG_F16, None, 0, None) == b.SWG_OK
