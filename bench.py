@@ -13,6 +13,10 @@ and the x stage as three calls -- is timed beside it and reported under
 129 MB L2, so no flush is needed between steps; SwishGrad (100 MB of bf16 I/O
 per launch) is timed over back-to-back launches that rotate through six
 input/output sets (576 MB), so that every launch reads its inputs from HBM.
+The sibling activation gradients (GELU, HardSwish) are timed the same way;
+the GroupNorm backward on ResNet-50 stage-1 activations at batch 32
+([32, 256, 56, 56], 32 groups, fp16) over three rotating sets (462 MB), with
+PyTorch's own GroupNorm backward on the same inputs beside it.
 
 Prints ONE JSON line (rank 0). `value` is milliseconds per backward (lower is
 better); `pct_roofline` is the roofline time max(8MKN / tensor peak,
@@ -320,6 +324,53 @@ def run_ours(args, rank, world):
     swg.swg_check()
     del sets
 
+    # GroupNorm backward (dx, dgamma, dbeta): ResNet-50 stage-1 activations at batch 32,
+    # [32, 256, 56, 56], 32 groups, fp16; three rotating input/output sets (462 MB, over L2).
+    # PyTorch's own CUDA GroupNorm backward on the same inputs is timed beside it (its
+    # forward's mean and rstd computed outside the timing).
+    from synth import GROUP_NORM_CONFIGS, GROUP_NORM_EPS, group_norm_inputs
+    gN, gC, gHW, gG = GROUP_NORM_CONFIGS["resnet50_stage1_b32"]
+    gsets = []
+    for j in range(3):
+        g_dy, g_x, g_gam = group_norm_inputs(gN, gC, gHW, gG, torch.float16, device=dev, seed=20 + j)
+        gsets.append(dict(dy=g_dy, x=g_x, g=g_gam, dx=torch.empty_like(g_x), dg=torch.empty_like(g_gam),
+                          db=torch.empty_like(g_gam),
+                          ws=torch.empty(swg.group_norm_bwd_workspace_size(gN, gC, gHW, gG), dtype=torch.uint8,
+                                         device=dev)))
+
+    def gn_ours(s_):
+        swg.group_norm_bwd(s_["dy"], s_["x"], gG, gamma=s_["g"], eps=GROUP_NORM_EPS, dx=s_["dx"],
+                           dgamma=s_["dg"], dbeta=s_["db"], workspace=s_["ws"])
+
+    def gn_torch(s_):
+        torch.ops.aten.native_group_norm_backward(s_["dy"], s_["x"], s_["mean"], s_["rstd"], s_["g"], gN, gC,
+                                                  gHW, gG, [True, True, True])
+
+    for s_ in gsets:
+        _, s_["mean"], s_["rstd"] = torch.ops.aten.native_group_norm(s_["x"], s_["g"], None, gN, gC, gHW, gG,
+                                                                      GROUP_NORM_EPS)
+
+    def time_rot(fn, n=60):
+        for i in range(max(3, args.warmup)):
+            fn(gsets[i % 3])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        for i in range(n):
+            ev[i].record(stream)
+            fn(gsets[i % 3])
+        ev[n].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
+
+    gn_ms = time_rot(gn_ours)
+    swg.swg_check()
+    gn_torch_ms = time_rot(gn_torch)
+    gn_bytes = 3.0 * gN * gC * gHW * 2 + 3.0 * gC * 2
+    gn = {"workload": "resnet50 stage-1 activations, batch 32", "shape": [gN, gC, 56, 56], "groups": gG,
+          "dtype": "f16", "ms": round(gn_ms, 5), "gbs": round(gn_bytes / (gn_ms * 1e-3) / 1e9, 1),
+          "frac_hbm": round(gn_bytes / (gn_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+          "torch_native_ms": round(gn_torch_ms, 5)}
+    del gsets
+
     # accumulate mode: the public whole-backward call (fused chain, dg/dfc not
     # returned) with and without SWG_ACCUMULATE, device-resident inputs
     acc_outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
@@ -424,6 +475,7 @@ def run_ours(args, rank, world):
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
                        "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
         "act_grad": {"n": SWISH_N, "dtype": "bf16", **act},
+        "group_norm_bwd": gn,
         "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
         "swiglu_fwd": fwd,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -46,9 +46,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kParts = 4;                  // bulk-copy parts per stage, one mbarrier each
 constexpr int kStageBytes = 96 * 1024;     // largest x and dy stage (slices longer than it are streamed)
 constexpr int kSliceBytes = 48 * 1024;     // target x and dy bytes per CTA (measured: 48 KB over 24 and 12)
-constexpr int kMinBlocks = 4;              // resident CTAs per SM the register budget is set for
+constexpr int kMinBlocks = 1024 / kThreads;  // resident CTAs per SM the register budget is set for
 constexpr int kMaxCluster = 8;             // portable cluster size
 constexpr int64_t kMinSlice = 2048;        // elements: smaller slices do not pay for the cluster exchange
+constexpr int kPipeSliceBytes = 56 * 1024;     // persistent form: target x and dy bytes per buffer
+constexpr int kPipeMaxSliceBytes = 56 * 1024;  // persistent form: largest buffer (two per CTA)
 
 enum : int { kPlain = 0, kBulk = 1, kBulkVec = 2 };
 
@@ -85,13 +87,64 @@ __device__ __forceinline__ double warp_sum(double v) {
   return v;
 }
 
+// pass-1 sums over stage-local [s, e) of one channel (vectorised: s, e multiples of the vector)
+template <typename T, bool kVec>
+__device__ __forceinline__ void acc_range(const T* xs, const T* ds, int s, int e, float K, float& sx, float& sxx,
+                                          float& sd, float& se) {
+  if (kVec) {
+    constexpr int V = Vec16<T>::kN;
+    for (int v = s / V + static_cast<int>(threadIdx.x); v < e / V; v += kThreads) {
+      Vec16<T> vx, vd;
+      vx.u = reinterpret_cast<const uint4*>(xs)[v];
+      vd.u = reinterpret_cast<const uint4*>(ds)[v];
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const float xk = to_f(vx.e[i]) - K, dv = to_f(vd.e[i]);
+        sx += xk;
+        sxx = fmaf(xk, xk, sxx);
+        sd += dv;
+        se = fmaf(dv, xk, se);
+      }
+    }
+  } else {
+    for (int i = s + static_cast<int>(threadIdx.x); i < e; i += kThreads) {
+      const float xk = to_f(xs[i]) - K, dv = to_f(ds[i]);
+      sx += xk;
+      sxx = fmaf(xk, xk, sxx);
+      sd += dv;
+      se = fmaf(dv, xk, se);
+    }
+  }
+}
+
+// pass 2 over stage-local [s, e) of one channel: dx = aj dy + c2 + c3 ((x - K) - d), written over x
+template <typename T, bool kVec>
+__device__ __forceinline__ void dx_range(T* xs, const T* ds, int s, int e, float K, float aj, float d, float c2,
+                                         float c3) {
+  if (kVec) {
+    constexpr int V = Vec16<T>::kN;
+    for (int v = s / V + static_cast<int>(threadIdx.x); v < e / V; v += kThreads) {
+      Vec16<T> vx, vd, vo;
+      vx.u = reinterpret_cast<const uint4*>(xs)[v];
+      vd.u = reinterpret_cast<const uint4*>(ds)[v];
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        vo.e[i] = from_f<T>(fmaf(aj, to_f(vd.e[i]), fmaf(c3, (to_f(vx.e[i]) - K) - d, c2)));
+      reinterpret_cast<uint4*>(xs)[v] = vo.u;
+    }
+  } else {
+    for (int i = s + static_cast<int>(threadIdx.x); i < e; i += kThreads)
+      xs[i] = from_f<T>(fmaf(aj, to_f(ds[i]), fmaf(c3, (to_f(xs[i]) - K) - d, c2)));
+  }
+}
+
 struct GnArgs {
   const void* x;
   const void* dy;
   const void* gamma;  // null: gamma = 1
   void* dx;
   float* stats;       // [N G][2]: d = mu - K, rstd        (null when dgamma, dbeta are not wanted)
-  float* part;        // [N G][S][Cg][2]: sum dy, sum dy (x - K) per channel piece (null likewise)
+  float* part;        // [N G][S][Cg][warps][2]: sum dy, sum dy (x - K) per channel and warp (null likewise)
   int64_t hw;         // HxW
   int64_t m;          // Cg HxW
   int64_t slice;      // elements per CTA (multiple of 8)
@@ -100,20 +153,74 @@ struct GnArgs {
   int groups;         // G
   int S;              // cluster size
   float eps;
+  float inv_m;        // 1 / m, rounded once
   uint32_t* status;
 };
 
+// The group's coefficients from the cluster's per-warp sums, computed by every
+// warp (the same inputs in the same order give the same values in all warps,
+// so no block barrier is needed to share them). After the cluster barrier that
+// follows the writes of ws[warp][0..3] = sum(x - K), sum((x - K)^2),
+// sum(gamma dy), sum(gamma dy (x - K)) in every CTA of the cluster.
+struct GnCoef {
+  float d, c1, c2, c3;  // d = mu - K, c1 = rstd; dx = (c1 gamma_c) dy + c2 + c3 ((x - K) - d)
+};
+__device__ __forceinline__ GnCoef cluster_coef(const float (*ws)[4], const GnArgs& a) {
+  const int lane = threadIdx.x & 31;
+  float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+  for (int p = lane; p < a.S * kWarps; p += 32) {  // (rank, warp) pairs, fixed assignment to lanes
+    const uint32_t r = static_cast<uint32_t>(p / kWarps);
+    const int w = p % kWarps;
+    const float t0 = ld_cluster_f32(&ws[w][0], r), t1 = ld_cluster_f32(&ws[w][1], r);
+    const float t2 = ld_cluster_f32(&ws[w][2], r), t3 = ld_cluster_f32(&ws[w][3], r);
+    v0 += t0;
+    v1 += t1;
+    v2 += t2;
+    v3 += t3;
+  }
+  v0 = warp_sum(v0);
+  v1 = warp_sum(v1);
+  v2 = warp_sum(v2);
+  v3 = warp_sum(v3);
+  GnCoef c;
+  c.d = v0 * a.inv_m;                                         // mu - K
+  const float var = fmaxf(fmaf(v1, a.inv_m, -c.d * c.d), 0.0f);  // biased
+  c.c1 = rsqrtf(var + a.eps);                                 // rstd
+  const float B = c.c1 * fmaf(-c.d, v2, v3);                  // sum gamma dy x_hat
+  c.c2 = -c.c1 * v2 * a.inv_m;
+  c.c3 = -c.c1 * c.c1 * B * a.inv_m;
+  return c;
+}
+
+// channel j closes (ends, or the slice ends inside it): gamma-weight the thread's sums into the
+// group sums; the warp's channel partials go to the workspace
+template <typename T>
+__device__ __forceinline__ void close_channel(int j, const T* gam, float* part, float& sd, float& se, float& ga,
+                                              float& ge) {
+  const float gj = gam != nullptr ? to_f(gam[j]) : 1.0f;
+  ga = fmaf(gj, sd, ga);
+  ge = fmaf(gj, se, ge);
+  if (part != nullptr) {
+    const float D = warp_sum(sd), E = warp_sum(se);
+    if ((threadIdx.x & 31) == 0) {
+      float* q = part + (static_cast<int64_t>(j) * kWarps + (threadIdx.x >> 5)) * 2;
+      q[0] = D;
+      q[1] = E;
+    }
+  }
+  sd = 0.f;
+  se = 0.f;
+}
+
+// One cluster per (sample, group); slices longer than the stage are streamed
+// (read again for pass 2); misaligned groups take plain loads and stores.
 template <typename T, int kMode>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   T* xs = reinterpret_cast<T*>(smem);
   T* ds = reinterpret_cast<T*>(smem + a.stage * static_cast<int64_t>(sizeof(T)));
   __shared__ __align__(8) uint64_t bar[kParts];
-  __shared__ float red[2][kWarps][2];
   __shared__ float wsum[kWarps][4];
-  __shared__ float gsum[4];
-  __shared__ float tot[4];
-  __shared__ float coef[4];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -128,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
   const int64_t hi = min(a.m, lo + a.slice);
   const int64_t nst = (hi - lo + a.stage - 1) / a.stage;  // stages of this slice
   const float K = to_f(xg[0]);
-  constexpr int V = Vec16<T>::kN;
+  float* part = a.part != nullptr ? a.part + (grp * a.S + rank) * static_cast<int64_t>(a.cg) * kWarps * 2 : nullptr;
 
   if (kMode != kPlain && tid == 0) {
     for (int p = 0; p < kParts; ++p) mbar_init(&bar[p], 1);
@@ -171,92 +278,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
 
   // ---------------------------------------------------------------- pass 1
   // Channels are tracked incrementally (no integer division in the loops): j is
-  // the channel at stage-local position s and jend the stage-local end of j.
-  float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f;
-  float sd = 0.f, se = 0.f;  // this thread's sums of dy, dy (x - K) over the open channel
-  int cur_j = -1;            // thread 0: channel whose partials are being gathered
-  float cur_d = 0.f, cur_e = 0.f;
-  int rb = 0;                // red[] buffer of the next channel reduction
-  const bool want_part = a.part != nullptr;
-  float* part = want_part ? a.part + (grp * a.S + rank) * static_cast<int64_t>(a.cg) * 2 : nullptr;
-  // the open channel j is done (or leaves this stage): gamma-weight the thread's
-  // sums into the group sums; reduce them over the CTA for the channel partials
-  auto close_channel = [&](int j) {
-    const float gj = gam != nullptr ? to_f(gam[j]) : 1.0f;
-    ga = fmaf(gj, sd, ga);
-    ge = fmaf(gj, se, ge);
-    if (want_part) {
-      const float D = warp_sum(sd), E = warp_sum(se);
-      if (lane == 0) {
-        red[rb][warp][0] = D;
-        red[rb][warp][1] = E;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float Ds = 0.f, Es = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-          Ds += red[rb][w][0];
-          Es += red[rb][w][1];
-        }
-        if (j == cur_j) {
-          cur_d += Ds;
-          cur_e += Es;
-        } else {
-          if (cur_j >= 0) {
-            part[2 * cur_j] = cur_d;
-            part[2 * cur_j + 1] = cur_e;
-          }
-          cur_j = j;
-          cur_d = Ds;
-          cur_e = Es;
-        }
-      }
-      rb ^= 1;
-    }
-    sd = 0.f;
-    se = 0.f;
-  };
-
+  // the channel at stage-local position s, jend the stage-local end of j. The
+  // open channel's sums stay in registers across stages.
+  float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f, sd = 0.f, se = 0.f;
+  bool open = false;
+  int j = 0;
   for (int64_t st = 0; st < nst; ++st) {
     const int64_t c0 = lo + st * a.stage;
     const int clen = static_cast<int>(min(a.stage, hi - c0));
     if (st > 0) __syncthreads();  // everyone is done with the previous stage
     issue_stage(c0, clen);
     const int plen = static_cast<int>(plen_of(clen));
-    int j = static_cast<int>(c0 / a.hw);
+    j = static_cast<int>(c0 / a.hw);
     int64_t jend = (j + 1) * a.hw - c0;
-    bool open = false;
     for (int p = 0; p * plen < clen; ++p) {
       wait_part(p);
       const int s1 = min(clen, (p + 1) * plen);
       for (int s = p * plen; s < s1;) {
         const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
-        if (kMode == kBulkVec) {
-          for (int v = s / V + tid; v < e / V; v += kThreads) {
-            Vec16<T> vx, vd;
-            vx.u = reinterpret_cast<const uint4*>(xs)[v];
-            vd.u = reinterpret_cast<const uint4*>(ds)[v];
-#pragma unroll
-            for (int i = 0; i < V; ++i) {
-              const float xk = to_f(vx.e[i]) - K, dv = to_f(vd.e[i]);
-              sx += xk;
-              sxx = fmaf(xk, xk, sxx);
-              sd += dv;
-              se = fmaf(dv, xk, se);
-            }
-          }
-        } else {
-          for (int i = s + tid; i < e; i += kThreads) {
-            const float xk = to_f(xs[i]) - K, dv = to_f(ds[i]);
-            sx += xk;
-            sxx = fmaf(xk, xk, sxx);
-            sd += dv;
-            se = fmaf(dv, xk, se);
-          }
-        }
+        acc_range<T, kMode == kBulkVec>(xs, ds, s, e, K, sx, sxx, sd, se);
         open = true;
         if (e == jend) {
-          close_channel(j);
+          close_channel(j, gam, part, sd, se, ga, ge);
           open = false;
           ++j;
           jend += a.hw;
@@ -264,23 +307,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
         s = e;
       }
     }
-    if (open) close_channel(j);  // channel j goes on past this stage or this slice
   }
-  if (want_part) {
-    if (tid == 0 && cur_j >= 0) {
-      part[2 * cur_j] = cur_d;
-      part[2 * cur_j + 1] = cur_e;
-    }
-    // channels of the group outside this slice get zeros
-    const int jlo = hi > lo ? static_cast<int>(lo / a.hw) : a.cg;
-    const int jhi = hi > lo ? static_cast<int>((hi - 1) / a.hw) : -1;
-    for (int jj = tid; jj < a.cg; jj += kThreads) {
-      if (jj < jlo || jj > jhi) {
-        part[2 * jj] = 0.f;
-        part[2 * jj + 1] = 0.f;
-      }
-    }
-  }
+  if (open) close_channel(j, gam, part, sd, se, ga, ge);  // the slice ends inside channel j
 
   // ---------------------------------------------------------------- exchange
   sx = warp_sum(sx);
@@ -293,43 +321,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
     wsum[warp][2] = ga;
     wsum[warp][3] = ge;
   }
-  __syncthreads();
-  if (tid < 4) {
-    float v = 0.f;
-    for (int w = 0; w < kWarps; ++w) v += wsum[w][tid];
-    gsum[tid] = v;
+  cluster_sync();  // every warp's sums in every CTA are written
+  const GnCoef cf = cluster_coef(wsum, a);
+  if (a.stats != nullptr && rank == 0 && tid == 0) {
+    a.stats[2 * grp] = cf.d;
+    a.stats[2 * grp + 1] = cf.c1;
   }
-  cluster_sync();  // every CTA's gsum is written
-  if (tid < 4) {
-    float t[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < a.S) t[r] = ld_cluster_f32(&gsum[tid], static_cast<uint32_t>(r));
-    float v = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < a.S) v += t[r];
-    tot[tid] = v;
-  }
-  cluster_sync();  // every CTA is done reading its peers (and tot is visible in the CTA)
-  if (tid == 0) {
-    // fp32 and a fixed order: the same coefficients in every CTA of the cluster
-    const float inv_m = 1.0f / static_cast<float>(a.m);
-    const float d = tot[0] * inv_m;                              // mu - K
-    const float var = fmaxf(fmaf(tot[1], inv_m, -d * d), 0.0f);  // biased
-    const float rstd = rsqrtf(var + a.eps);
-    const float B = rstd * fmaf(-d, tot[2], tot[3]);             // sum gamma dy x_hat
-    coef[0] = d;
-    coef[1] = rstd;
-    coef[2] = -rstd * tot[2] * inv_m;
-    coef[3] = -rstd * rstd * B * inv_m;
-    if (a.stats != nullptr && rank == 0) {
-      a.stats[2 * grp] = d;
-      a.stats[2 * grp + 1] = rstd;
-    }
-  }
-  __syncthreads();
-  const float d = coef[0], c1 = coef[1], c2 = coef[2], c3 = coef[3];
 
   // ---------------------------------------------------------------- pass 2
   for (int64_t st = 0; st < nst; ++st) {
@@ -342,65 +339,199 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
       issue_stage(c0, clen);
     }
     const int plen = static_cast<int>(plen_of(clen));
-    int j = static_cast<int>(c0 / a.hw);
-    int64_t jend = (j + 1) * a.hw - c0;
-    float aj = c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+    int jj = static_cast<int>(c0 / a.hw);
+    int64_t jend = (jj + 1) * a.hw - c0;
+    float aj = cf.c1 * (gam != nullptr ? to_f(gam[jj]) : 1.0f);
     for (int p = 0; p * plen < clen; ++p) {
       if (reload) wait_part(p);
-      const int s0 = p * plen, s1 = min(clen, s0 + plen);
-      for (int s = s0; s < s1;) {
+      const int s1 = min(clen, (p + 1) * plen);
+      for (int s = p * plen; s < s1;) {
         const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
-        if (kMode == kBulkVec) {
-          for (int v = s / V + tid; v < e / V; v += kThreads) {
-            Vec16<T> vx, vd, vo;
-            vx.u = reinterpret_cast<const uint4*>(xs)[v];
-            vd.u = reinterpret_cast<const uint4*>(ds)[v];
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-              vo.e[i] = from_f<T>(fmaf(aj, to_f(vd.e[i]), fmaf(c3, (to_f(vx.e[i]) - K) - d, c2)));
-            reinterpret_cast<uint4*>(xs)[v] = vo.u;
-          }
-        } else {
-          for (int i = s + tid; i < e; i += kThreads)
-            xs[i] = from_f<T>(fmaf(aj, to_f(ds[i]), fmaf(c3, (to_f(xs[i]) - K) - d, c2)));
-        }
+        dx_range<T, kMode == kBulkVec>(xs, ds, s, e, K, aj, cf.d, cf.c2, cf.c3);
         if (e == jend) {
-          ++j;
+          ++jj;
           jend += a.hw;
-          if (j < a.cg) aj = c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+          if (jj < a.cg) aj = cf.c1 * (gam != nullptr ? to_f(gam[jj]) : 1.0f);
         }
         s = e;
       }
-      if (kMode != kPlain) {
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-          bulk_s2g(og + c0 + s0, xs + s0, static_cast<uint32_t>((s1 - s0) * static_cast<int64_t>(sizeof(T))));
-          bulk_commit();
-        }
-      }
     }
-    if (kMode == kPlain) {
+    if (kMode != kPlain) {
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        bulk_s2g(og + c0, xs, static_cast<uint32_t>(clen * static_cast<int>(sizeof(T))));
+        bulk_commit();
+      }
+    } else {
       __syncthreads();
       for (int i = tid; i < clen; i += kThreads) og[c0 + i] = xs[i];
     }
   }
+  cluster_sync();  // no CTA leaves while a peer may still read its sums
   if (kMode != kPlain && tid == 0) bulk_wait_read<0>();  // the stores have read shared memory
   if (timed_out && a.status != nullptr) atomicOr(a.status, kStatusTimeout);
 }
 
-// dgamma_c = sum_n rstd_n sum_k (E - d_n D),  dbeta_c = sum_n sum_k D; one warp per channel, fixed order
+// Persistent, double-buffered form for groups whose slices fit two shared-memory
+// buffers (16-byte aligned groups): cluster c takes groups c, c + #clusters, ...
+// and, while it works on one group, the bulk copies of its next group's slices
+// fill the other buffer; the stores of dx drain behind. One cluster barrier per
+// group (the per-warp sums alternate between two slots) and one block barrier
+// (before the stores); no barrier in pass 1.
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a, int64_t items) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bar[2][kParts];
+  __shared__ float wsum[2][kWarps][4];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t ncl = gridDim.x / a.S;
+  const int64_t lo = min(a.m, static_cast<int64_t>(rank) * a.slice);
+  const int len = static_cast<int>(min(a.m, lo + a.slice) - lo);  // the same slice of every group
+  const int plen = len > 0 ? static_cast<int>((((len + kParts - 1) / kParts) + 7) & ~7) : 1;
+  const int np = len > 0 ? (len + plen - 1) / plen : 0;
+  const int j0 = len > 0 ? static_cast<int>(lo / a.hw) : 0;            // first channel of the slice
+  const int64_t jend0 = (static_cast<int64_t>(j0) + 1) * a.hw - lo;     // slice-local end of channel j0
+  // buffer b: x at smem + 2 b slice, dy at smem + (2 b + 1) slice (elements of T)
+  auto xbuf = [&](int b) { return reinterpret_cast<T*>(smem) + 2 * b * a.slice; };
+  auto dbuf = [&](int b) { return reinterpret_cast<T*>(smem) + (2 * b + 1) * a.slice; };
+  const T* X = static_cast<const T*>(a.x);
+  const T* DY = static_cast<const T*>(a.dy);
+  T* DX = static_cast<T*>(a.dx);
+
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b)
+      for (int p = 0; p < kParts; ++p) mbar_init(&bar[b][p], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;  // bit b * kParts + p: parity of the next completion of bar[b][p]
+  bool timed_out = false;
+
+  auto issue = [&](int64_t item, int b) {  // thread 0: this CTA's slice of group `item` -> buffer b
+    const int64_t off = item * a.m + lo;
+    for (int p = 0; p < np; ++p) {
+      const int s0 = p * plen, s1 = min(len, s0 + plen);
+      const uint32_t bytes = static_cast<uint32_t>((s1 - s0) * static_cast<int>(sizeof(T)));
+      mbar_arrive_expect_tx(&bar[b][p], 2 * bytes);
+      bulk_g2s(xbuf(b) + s0, X + off + s0, bytes, &bar[b][p]);
+      bulk_g2s(dbuf(b) + s0, DY + off + s0, bytes, &bar[b][p]);
+    }
+  };
+
+  int64_t w = blockIdx.x / a.S;
+  float K = w < items ? to_f(X[w * a.m]) : 0.0f;
+  if (tid == 0 && w < items) issue(w, 0);
+  for (int it = 0; w < items; w += ncl, ++it) {
+    const int b = it & 1;
+    const int64_t wn = w + ncl;
+    float K_next = 0.0f;
+    if (wn < items) {
+      K_next = to_f(X[wn * a.m]);  // used by the next group: its latency hides behind this one
+      if (tid == 0) {
+        bulk_wait_read<0>();  // the stores of the previous group have read buffer b ^ 1
+        issue(wn, b ^ 1);
+      }
+    }
+    T* xs = xbuf(b);
+    const T* ds = dbuf(b);
+    const int g = static_cast<int>(w % a.groups);
+    const T* gam = a.gamma != nullptr ? static_cast<const T*>(a.gamma) + static_cast<int64_t>(g) * a.cg : nullptr;
+    float* part = a.part != nullptr ? a.part + (w * a.S + rank) * static_cast<int64_t>(a.cg) * kWarps * 2 : nullptr;
+
+    // pass 1 (no block barrier: channel partials are per warp)
+    float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f, sd = 0.f, se = 0.f;
+    {
+      int j = j0;
+      int64_t jend = jend0;
+      bool open = false;
+      for (int p = 0; p < np; ++p) {
+        if (!mbar_wait(&bar[b][p], (phase >> (b * kParts + p)) & 1u)) timed_out = true;
+        phase ^= 1u << (b * kParts + p);
+        const int s1 = min(len, (p + 1) * plen);
+        for (int s = p * plen; s < s1;) {
+          const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
+          acc_range<T, kVec>(xs, ds, s, e, K, sx, sxx, sd, se);
+          open = true;
+          if (e == jend) {
+            close_channel(j, gam, part, sd, se, ga, ge);
+            open = false;
+            ++j;
+            jend += a.hw;
+          }
+          s = e;
+        }
+      }
+      if (open) close_channel(j, gam, part, sd, se, ga, ge);
+    }
+
+    // exchange: one cluster barrier; every warp forms the coefficients itself
+    sx = warp_sum(sx);
+    sxx = warp_sum(sxx);
+    ga = warp_sum(ga);
+    ge = warp_sum(ge);
+    if (lane == 0) {
+      wsum[b][warp][0] = sx;
+      wsum[b][warp][1] = sxx;
+      wsum[b][warp][2] = ga;
+      wsum[b][warp][3] = ge;
+    }
+    cluster_sync();
+    const GnCoef cf = cluster_coef(wsum[b], a);
+    if (a.stats != nullptr && rank == 0 && tid == 0) {
+      a.stats[2 * w] = cf.d;
+      a.stats[2 * w + 1] = cf.c1;
+    }
+
+    // pass 2: dx over x in buffer b, one bulk store for the slice
+    {
+      int j = j0;
+      int64_t jend = jend0;
+      float aj = cf.c1 * (gam != nullptr && len > 0 ? to_f(gam[j]) : 1.0f);
+      for (int s = 0; s < len;) {
+        const int e = static_cast<int>(min(static_cast<int64_t>(len), jend));
+        dx_range<T, kVec>(xs, ds, s, e, K, aj, cf.d, cf.c2, cf.c3);
+        if (e == jend) {
+          ++j;
+          jend += a.hw;
+          if (j < a.cg) aj = cf.c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+        }
+        s = e;
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0 && len > 0) {
+        bulk_s2g(DX + w * a.m + lo, xs, static_cast<uint32_t>(len * static_cast<int>(sizeof(T))));
+        bulk_commit();
+      }
+    }
+    K = K_next;
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its sums
+  if (tid == 0) bulk_wait_read<0>();
+  if (timed_out && a.status != nullptr) atomicOr(a.status, kStatusTimeout);
+}
+
+// dgamma_c = sum_n rstd_n sum_k,w (E - d_n D),  dbeta_c = sum_n sum_k,w D over the slices k that hold
+// channel c and the warps w; one warp per channel, a fixed order (bitwise reproducible)
 template <typename T>
 __global__ void __launch_bounds__(256) gn_param_kernel(const float* __restrict__ stats, const float* __restrict__ part,
-                                                       T* dgamma, T* dbeta, int64_t N, int C, int G, int cg, int S) {
+                                                       T* dgamma, T* dbeta, int64_t N, int C, int G, int cg, int S,
+                                                       int64_t hw, int64_t slice) {
   const int c = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (c >= C) return;
   const int g = c / cg, j = c % cg;
+  const int64_t k0 = (j * hw) / slice;
+  const int64_t k1 = min(static_cast<int64_t>(S - 1), ((j + 1) * hw - 1) / slice);
+  const int64_t per = (k1 - k0 + 1) * kWarps;
   double sb = 0.0, sg = 0.0;
-  for (int64_t t = lane; t < N * S; t += 32) {
-    const int64_t n = t / S, k = t % S, grp = n * G + g;
-    const float* p = part + ((grp * S + k) * cg + j) * 2;
+  for (int64_t t = lane; t < N * per; t += 32) {
+    const int64_t n = t / per, r = t - n * per;
+    const int64_t k = k0 + r / kWarps, w = r % kWarps, grp = n * G + g;
+    const float* p = part + ((((grp * S + k) * cg + j) * kWarps) + w) * 2;
     const double D = p[0], E = p[1];
     sb += D;
     sg += static_cast<double>(stats[2 * grp + 1]) * (E - static_cast<double>(stats[2 * grp]) * D);
@@ -440,10 +571,59 @@ cudaError_t launch_mode(const GnArgs& a, int64_t groups_total, cudaStream_t stre
   return cudaLaunchKernelEx(&cfg, gn_bwd_kernel<T, kMode>, a);
 }
 
+// clusters of the persistent form that fit on the device at once (cached per instantiation, S and buffer size)
+template <typename T, bool kVec>
+cudaError_t launch_pipe(const GnArgs& a, int64_t items, cudaStream_t stream) {
+  const size_t smem = 4 * static_cast<size_t>(a.slice) * sizeof(T);
+  static bool attr_set = false;
+  static int cached_S = 0, cached_clusters = 0;
+  static size_t cached_smem = 0;
+  static int cached_dev = -1;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(gn_bwd_pipe_kernel<T, kVec>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kPipeMaxSliceBytes);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (cached_S != a.S || cached_smem != smem || cached_dev != dev) {
+    cfg.gridDim = dim3(static_cast<unsigned>(a.S));
+    int n = 0;
+    cudaError_t err = cudaOccupancyMaxActiveClusters(&n, gn_bwd_pipe_kernel<T, kVec>, &cfg);
+    if (err != cudaSuccess) return err;
+    cached_S = a.S;
+    cached_smem = smem;
+    cached_dev = dev;
+    cached_clusters = n > 0 ? n : 1;
+  }
+  const int64_t clusters = items < cached_clusters ? items : cached_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * a.S));
+  return cudaLaunchKernelEx(&cfg, gn_bwd_pipe_kernel<T, kVec>, a, items);
+}
+
 template <typename T>
 cudaError_t run(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t N,
                 int64_t C, int64_t HxW, int64_t G, float eps, void* ws, cudaStream_t stream) {
-  const GnPlan plan = gn_plan(N, C, HxW, G, static_cast<int>(sizeof(T)), device_sm_count());
+  const int sms = device_sm_count();
+  const int64_t es = sizeof(T);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dy) |
+                         reinterpret_cast<uintptr_t>(dx)) & 15u) == 0 &&
+                       ((C / G) * HxW * es) % 16 == 0;
+  const GnPlan pipe = gn_pipe_plan(N, C, HxW, G, static_cast<int>(es), sms);
+  const bool use_pipe = aligned && pipe.S > 0;
+  const GnPlan plan = use_pipe ? pipe : gn_plan(N, C, HxW, G, static_cast<int>(es), sms);
   const bool params = dgamma != nullptr || dbeta != nullptr;
   GnArgs a;
   a.x = x;
@@ -461,20 +641,18 @@ cudaError_t run(const void* dy, const void* x, const void* gamma, void* dx, void
   a.groups = static_cast<int>(G);
   a.S = plan.S;
   a.eps = eps;
+  a.inv_m = 1.0f / static_cast<float>(a.m);
   a.status = status_word_ptr();
-  const int64_t es = sizeof(T);
-  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dy) |
-                         reinterpret_cast<uintptr_t>(dx)) & 15u) == 0 &&
-                       (a.m * es) % 16 == 0;
   const bool vec = aligned && HxW % (16 / es) == 0;
-  cudaError_t err = vec       ? launch_mode<T, kBulkVec>(a, N * G, stream)
+  cudaError_t err = use_pipe  ? (vec ? launch_pipe<T, true>(a, N * G, stream) : launch_pipe<T, false>(a, N * G, stream))
+                    : vec     ? launch_mode<T, kBulkVec>(a, N * G, stream)
                     : aligned ? launch_mode<T, kBulk>(a, N * G, stream)
                               : launch_mode<T, kPlain>(a, N * G, stream);
   if (err != cudaSuccess || !params) return err;
   const int64_t threads = C * 32;
   gn_param_kernel<T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
       a.stats, a.part, static_cast<T*>(dgamma), static_cast<T*>(dbeta), N, static_cast<int>(C),
-      static_cast<int>(G), a.cg, a.S);
+      static_cast<int>(G), a.cg, a.S, HxW, a.slice);
   return cudaGetLastError();
 }
 
@@ -495,9 +673,22 @@ GnPlan gn_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int
   return p;
 }
 
+GnPlan gn_pipe_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int num_sms) {
+  GnPlan p;
+  const int64_t m = (C / G) * HxW, ng = N * G;
+  const int64_t target = kPipeSliceBytes / (2 * elem_bytes);
+  int64_t S = (m + target - 1) / target;
+  S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
+  while (S < kMaxCluster && ng * S < 2 * static_cast<int64_t>(num_sms) && m / (S + 1) >= kMinSlice) ++S;
+  p.slice = (((m + S - 1) / S) + 7) & ~int64_t(7);
+  p.stage = p.slice;
+  p.S = p.slice <= kPipeMaxSliceBytes / (2 * elem_bytes) ? static_cast<int>(S) : 0;  // 0: does not fit
+  return p;
+}
+
 size_t gn_workspace_bytes(int64_t N, int64_t C, int64_t G) {
-  // stats [N G][2] + partials [N G][S <= 8][C / G][2], fp32
-  return al256(static_cast<size_t>(N * G) * 8) + al256(static_cast<size_t>(N * C) * kMaxCluster * 8);
+  // stats [N G][2] + partials [N G][S <= 8][C / G][warps][2], fp32
+  return al256(static_cast<size_t>(N * G) * 8) + al256(static_cast<size_t>(N * C) * kMaxCluster * kWarps * 8);
 }
 
 cudaError_t launch_group_norm_bwd(const void* dy, const void* x, const void* gamma, void* dx, void* dgamma,

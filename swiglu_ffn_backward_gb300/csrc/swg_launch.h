@@ -62,6 +62,8 @@ struct GnPlan {
   int64_t stage;  // shared-memory stage per tensor, elements
 };
 GnPlan gn_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int num_sms);
+// persistent double-buffered form (16-byte aligned groups); S = 0 when two buffers do not fit
+GnPlan gn_pipe_plan(int64_t N, int64_t C, int64_t HxW, int64_t G, int elem_bytes, int num_sms);
 // workspace for dgamma / dbeta: per-(sample, group) statistics + per-channel partials
 size_t gn_workspace_bytes(int64_t N, int64_t C, int64_t G);
 // dx always; dgamma, dbeta when non-null (then ws holds gn_workspace_bytes); gamma null = ones

@@ -6,11 +6,13 @@ fp64 value rounded once to the I/O dtype, plus the scale-aware checks. Inputs:
 the GroupNorm recipe of synth/workloads.py (a different mean and spread per
 group, gamma around 1).
 
-Shapes cover the three load paths of the kernel (bulk copies with 16-byte
-vectors, bulk copies with scalar math when HxW is not a multiple of the
-vector, plain loads when a group does not start on 16 bytes), one to eight
-CTAs per group, slices longer than the shared-memory stage (read again for
-pass 2), empty slices, one channel per group and one element per group.
+Shapes cover both kernels and their load paths: the persistent
+double-buffered kernel (16-byte aligned groups whose slices fit two buffers;
+16-byte vectors, or scalar math when HxW is not a multiple of the vector;
+one or several groups per cluster) and the one-group-per-cluster kernel
+(slices longer than the shared-memory stage, read again for pass 2; plain
+loads when a group does not start on 16 bytes); one to eight CTAs per group,
+empty slices, one channel per group and one element per group.
 """
 
 import numpy as np
@@ -66,6 +68,8 @@ SMALL = [
     (2, 640, 1024, 32), # several CTAs per group
     (1, 4, 200000, 2),  # eight CTAs per group, slices longer than the stage
     (3, 9, 17, 3),      # ragged everything
+    (1, 8, 20001, 1),   # streamed slices with scalar math (aligned groups, HxW not a vector multiple)
+    (64, 32, 64, 32),   # 2048 small groups: each persistent cluster walks several of them
 ]
 
 
