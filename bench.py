@@ -420,19 +420,27 @@ def run_ours(args, rank, world):
            "pct_roofline": round(fwd_roof / fwd_ms, 4)}
     del fout
 
-    # e2e: host buffers in pinned memory, H2D of every input and D2H of the
-    # results inside the timed region, through the public swiglu_bwd call
+    # e2e: every input and output in pinned host memory, all host<->device copies
+    # inside the timed region. The public call is swiglu_bwd_host (the fused
+    # backward from host buffers: chunked over M, copies overlapped with the
+    # compute); beside it, the same work as PyTorch copies around the
+    # device-resident swiglu_bwd call (copies, then compute, then copies).
     host_in = {k: v.cpu().pin_memory() for k, v in inp.items()}
-    dev_in = {k: torch.empty_like(v) for k, v in inp.items()}
     outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
-    use_fused = args.path == "fused"
-    ws_full = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 1 if use_fused else 0), 16),
-                          dtype=torch.uint8, device=dev)
+    ws_host = torch.empty(swg.swiglu_bwd_host_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def e2e_step():
+        swg.swiglu_bwd_host(**host_in, out=host_out, workspace=ws_host)
+
+    dev_in = {k: torch.empty_like(v) for k, v in inp.items()}
+    use_fused = args.path == "fused"
+    ws_full = torch.empty(max(swg.swiglu_bwd_workspace_size(M, K, N, 1 if use_fused else 0), 16),
+                          dtype=torch.uint8, device=dev)
+
+    def e2e_serial_step():
         for k in dev_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
         swg.swiglu_bwd(**dev_in, fused=use_fused, return_dg=False, out=outs, workspace=ws_full)
@@ -440,19 +448,25 @@ def run_ours(args, rank, world):
             host_out[k].copy_(outs[k], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    _barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    swg.swg_check()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    def time_e2e(step):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        _barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        swg.swg_check()
+        return _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    e2e_ms = time_e2e(e2e_step)
+    e2e_serial_ms = time_e2e(e2e_serial_step)
+    del ws_host, dev_in, ws_full
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -479,7 +493,9 @@ def run_ours(args, rank, world):
         "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
         "swiglu_fwd": fwd,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "call": f"swiglu_bwd ({args.path}, dg/dfc not returned)"},
+                "steps": e2e_steps, "call": "swiglu_bwd_host (fused; pinned host buffers, copies overlapped)",
+                "serial_ms": round(e2e_serial_ms, 3),
+                "serial_call": f"torch copies + swiglu_bwd ({args.path}, dg/dfc not returned)"},
         "gpu_launches": launches[args.path] * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

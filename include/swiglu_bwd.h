@@ -213,6 +213,30 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc,
                       unsigned flags, void* workspace, size_t workspace_bytes,
                       swg_stream_t stream);
 
+/* ---- whole fused backward from host buffers ------------------------------------
+ * The whole backward of swiglu_bwd(..., SWG_FUSED, ...) (dx, dw_g, dw_fc, db_g,
+ * db_fc; dg and dfc are not produced) with every tensor argument in HOST
+ * memory, same shapes and layouts as swiglu_bwd. Page-locked host buffers
+ * (cudaHostAlloc / cudaHostRegister) let the copies overlap: M is cut into
+ * chunks of about 32768 rows; while one chunk is computed, the next chunk's
+ * rows are copied in and the previous chunk's dx is copied out, on two
+ * internal streams ordered against `stream` with events. dw and db are
+ * reduced once over every chunk's fp32 partials (one rounding, as in
+ * swiglu_bwd). `workspace` is DEVICE memory of at least
+ * swiglu_bwd_host_workspace_size(M, K, N) bytes, 16-byte aligned (it holds
+ * two chunks of inputs and of dx, W, the outputs and the partials: about
+ * 0.8 GB at M = 220000, K = 512, N = 1024). The call is asynchronous on
+ * `stream`: the host outputs are complete once the work enqueued on `stream`
+ * up to this call has finished (e.g. after cudaStreamSynchronize). Outputs
+ * are overwritten (no SWG_ACCUMULATE). Errors as swiglu_bwd, plus
+ * SWG_ERR_WORKSPACE for a missing or short workspace. */
+size_t swiglu_bwd_host_workspace_size(int64_t M, int64_t K, int64_t N);
+swg_status swiglu_bwd_host(const void* x, const void* w_g, const void* w_fc,
+                           const void* dy, const void* g, const void* fc,
+                           void* dx, void* dw_g, void* dw_fc, void* db_g, void* db_fc,
+                           int64_t M, int64_t K, int64_t N, void* workspace,
+                           size_t workspace_bytes, swg_stream_t stream);
+
 /* ---- SwishGrad ---------------------------------------------------------------
  * [P2] section 1.2: grad_x = grad * sigma(beta x) * (1 + beta x (1 - sigma(beta x))),
  * beta = *scale, or 1.0 when scale is NULL ([P2] 3.5). grad, x, grad_x hold n

@@ -48,6 +48,7 @@ EXPORTS = (
     "swiglu_fwd",
     "act_grad",
     "group_norm_bwd_workspace_size", "group_norm_bwd",
+    "swiglu_bwd_host_workspace_size", "swiglu_bwd_host",
 )
 
 
@@ -82,6 +83,10 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, P]
     lib.swiglu_fwd.restype = st
     lib.act_grad.argtypes = [P, P, ctypes.c_int, P, I64, ctypes.c_int, P]
+    lib.swiglu_bwd_host_workspace_size.restype = SZ
+    lib.swiglu_bwd_host_workspace_size.argtypes = [I64, I64, I64]
+    lib.swiglu_bwd_host.restype = st
+    lib.swiglu_bwd_host.argtypes = [P] * 11 + [I64, I64, I64, P, SZ, P]
     lib.group_norm_bwd_workspace_size.restype = SZ
     lib.group_norm_bwd_workspace_size.argtypes = [I64, I64, I64, I64]
     lib.group_norm_bwd.restype = st
@@ -349,6 +354,35 @@ def act_grad(grad, x, act: str, grad_x=None, stream=None):
     _check(lib.act_grad(grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
                         _DTYPE[grad.dtype], _stream(stream)), "act_grad")
     return grad_x
+
+
+def swiglu_bwd_host_workspace_size(M: int, K: int, N: int) -> int:
+    return int(lib.swiglu_bwd_host_workspace_size(M, K, N))
+
+
+def swiglu_bwd_host(x, w_g, w_fc, dy, g, fc, out: dict | None = None, workspace=None, stream=None) -> dict:
+    """Whole fused backward with every tensor in host memory (bf16 CPU tensors; pinned ones let the
+    copies overlap the compute). Returns host tensors dx, dw_g, dw_fc, db_g, db_fc (pinned when
+    allocated here); they are complete once `stream` (default: the current CUDA stream) has run."""
+    ins = dict(x=x, w_g=w_g, w_fc=w_fc, dy=dy, g=g, fc=fc)
+    for k, t in ins.items():
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{k} must be a bf16 CPU tensor")
+    ins = {k: t.contiguous() for k, t in ins.items()}
+    M, K = ins["x"].shape
+    N = ins["w_g"].shape[1]
+    if out is None:
+        out = {}
+    shapes = dict(dx=(M, K), dw_g=(K, N), dw_fc=(K, N), db_g=(1, N), db_fc=(1, N))
+    for k, shp in shapes.items():
+        if k not in out:
+            out[k] = torch.empty(shp, dtype=torch.bfloat16, pin_memory=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ws = _workspace(swiglu_bwd_host_workspace_size(M, K, N), dev, workspace)
+    _check(lib.swiglu_bwd_host(*(ins[k].data_ptr() for k in ("x", "w_g", "w_fc", "dy", "g", "fc")),
+                               *(out[k].data_ptr() for k in ("dx", "dw_g", "dw_fc", "db_g", "db_fc")),
+                               M, K, N, _ptr(ws), _nbytes(ws), _stream(stream)), "swiglu_bwd_host")
+    return out
 
 
 def group_norm_bwd_workspace_size(N: int, C: int, HxW: int, G: int) -> int:

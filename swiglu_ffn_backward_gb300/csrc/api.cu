@@ -8,6 +8,7 @@
 // short-circuit with no launch; a missing beta means 1.0).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/swiglu_bwd.h"
@@ -370,6 +371,208 @@ swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, cons
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g),
       static_cast<const uint16_t*>(fc), static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
       static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, workspace, plan, s));
+}
+
+// ---------------------------------------------------------------- whole backward from host buffers
+// The fused backward with every tensor in host memory. M is cut into chunks of
+// at least kHostChunkRows rows; while chunk c is computed (dx, and the fused w
+// stage's fp32 split partials into chunk c's own slots), chunk c + 1's rows are
+// copied in on one internal stream and chunk c - 1's dx is copied out on
+// another, each chunk's device buffers alternating between two sets. One
+// fixed-order reduction over every chunk's partials gives dw and db with one
+// rounding, as in the single-call backward. Workspace layout (256-byte aligned
+// regions): W_g, W_fc | two input sets (x, dy, g, fc rows of a chunk) | two dx
+// sets | dw_g, dw_fc, db_g, db_fc | dw partials [S total][2][K][N] fp32 |
+// db partials [S total][2N] fp32 (a single chunk: the fused w stage's own
+// workspace instead of the partial blocks).
+namespace {
+
+constexpr int64_t kHostChunkRows = 32768;
+
+struct HostPlan {
+  int64_t chunks, rows;  // chunk count, rows per chunk (multiple of 64; the last may be shorter)
+  int64_t splits_total;  // sum of the chunks' M-splits (chunks > 1)
+  size_t off_w, off_in[2], off_dx[2], off_out, off_dwp, off_dbp, total;
+};
+
+HostPlan host_plan(int64_t M, int64_t K, int64_t N, int sms) {
+  HostPlan p{};
+  // floor(M / kHostChunkRows) chunks (at most 256) of equal 64-row multiples: every chunk, the last
+  // included, keeps at least 16K rows, so each one splits over M (its partials path needs two splits)
+  p.chunks = M >= 2 * kHostChunkRows ? std::min<int64_t>(M / kHostChunkRows, 256) : (M > 0 ? 1 : 0);
+  p.rows = p.chunks > 0 ? (((M + p.chunks - 1) / p.chunks) + 63) / 64 * 64 : 0;
+  size_t off = 0;
+  p.off_w = off;
+  off += align256(static_cast<size_t>(2 * K * N) * 2);
+  const size_t in_bytes = static_cast<size_t>(p.rows) * static_cast<size_t>(K + 3 * N) * 2;
+  const size_t dx_bytes = static_cast<size_t>(p.rows) * static_cast<size_t>(K) * 2;
+  for (int b = 0; b < 2; ++b) {
+    p.off_in[b] = off;
+    off += align256(in_bytes);
+  }
+  for (int b = 0; b < 2; ++b) {
+    p.off_dx[b] = off;
+    off += align256(dx_bytes);
+  }
+  p.off_out = off;
+  off += align256(static_cast<size_t>(2 * K * N + 2 * N) * 2);
+  if (p.chunks > 1) {
+    for (int64_t c = 0; c < p.chunks; ++c) {
+      const int64_t r = std::min(p.rows, M - c * p.rows);
+      p.splits_total += swg::fw_plan(r, K, N, sms).splits;
+    }
+    p.off_dwp = off;
+    off += align256(static_cast<size_t>(p.splits_total) * 2 * K * N * 4);
+    p.off_dbp = off;
+    off += align256(static_cast<size_t>(p.splits_total) * 2 * N * 4);
+  } else {
+    p.off_dwp = off;
+    off += align256(p.chunks == 1 ? swg::fw_plan(M, K, N, sms).ws_bytes : 0);
+    p.off_dbp = p.off_dwp;
+  }
+  p.total = off;
+  return p;
+}
+
+// the internal copy streams and the events that order them against the caller's stream (per device,
+// created once; the enqueue of one call holds the lock, so calls from several host threads take turns)
+struct HostStreams {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, w_in = nullptr, reduced = nullptr, end = nullptr;
+  cudaEvent_t loaded[2] = {}, computed[2] = {}, dx_out[2] = {};
+};
+std::mutex g_host_mu;
+HostStreams g_host[64];
+
+cudaError_t host_streams(int dev, HostStreams** out) {
+  HostStreams& h = g_host[dev];
+  if (h.h2d == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking);
+    cudaEvent_t* evs[] = {&h.start, &h.w_in, &h.reduced, &h.end, &h.loaded[0], &h.loaded[1],
+                          &h.computed[0], &h.computed[1], &h.dx_out[0], &h.dx_out[1]};
+    for (cudaEvent_t* ev : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  *out = &h;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t swiglu_bwd_host_workspace_size(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K <= 0 || N <= 0) return 0;
+  return host_plan(M, K, N, swg::device_sm_count()).total;
+}
+
+swg_status swiglu_bwd_host(const void* x, const void* w_g, const void* w_fc, const void* dy, const void* g,
+                           const void* fc, void* dx, void* dw_g, void* dw_fc, void* db_g, void* db_fc, int64_t M,
+                           int64_t K, int64_t N, void* workspace, size_t workspace_bytes, swg_stream_t stream) {
+  swg_status st = check_shape(M, K, N);
+  if (st != SWG_OK) return st;
+  if (K == 0 || N == 0) return SWG_OK;
+  if (!w_g || !w_fc || !dw_g || !dw_fc || !db_g || !db_fc) return SWG_ERR_NULLPTR;
+  if (M > 0 && (!x || !dy || !g || !fc || !dx)) return SWG_ERR_NULLPTR;
+  const int64_t kn = K * N * 2, mn = M * N * 2;
+  const Range outs[] = {rng(dx, M * K * 2), rng(dw_g, kn), rng(dw_fc, kn), rng(db_g, N * 2), rng(db_fc, N * 2)};
+  const Range ins[] = {rng(x, M * K * 2), rng(w_g, kn), rng(w_fc, kn), rng(dy, mn), rng(g, mn), rng(fc, mn)};
+  if (any_overlap(outs, 5, ins, 6)) return SWG_ERR_PARAM_INVALID;
+  st = check_device();
+  if (st != SWG_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+  const int sms = swg::device_sm_count();
+  const HostPlan hp = host_plan(M, K, N, sms);
+  if (workspace == nullptr || workspace_bytes < hp.total) return SWG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SWG_ERR_UNSUPPORTED;
+
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  HostStreams* hs = nullptr;
+  if (host_streams(dev, &hs) != cudaSuccess) return SWG_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto dev16 = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
+  uint16_t* wg_d = dev16(hp.off_w);
+  uint16_t* wfc_d = wg_d + K * N;
+  uint16_t* dwg_d = dev16(hp.off_out);
+  uint16_t* dwfc_d = dwg_d + K * N;
+  uint16_t* dbg_d = dwfc_d + K * N;
+  uint16_t* dbfc_d = dbg_d + N;
+  const auto* xh = static_cast<const uint8_t*>(x);
+  const auto* dyh = static_cast<const uint8_t*>(dy);
+  const auto* gh = static_cast<const uint8_t*>(g);
+  const auto* fch = static_cast<const uint8_t*>(fc);
+  auto* dxh = static_cast<uint8_t*>(dx);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+    return e == cudaSuccess;
+  };
+
+  ok(cudaEventRecord(hs->start, cs));
+  ok(cudaStreamWaitEvent(hs->h2d, hs->start, 0));
+  ok(cudaStreamWaitEvent(hs->d2h, hs->start, 0));
+  ok(cudaMemcpyAsync(wg_d, w_g, kn, h2d, hs->h2d));
+  ok(cudaMemcpyAsync(wfc_d, w_fc, kn, h2d, hs->h2d));
+  ok(cudaEventRecord(hs->w_in, hs->h2d));
+  ok(cudaStreamWaitEvent(cs, hs->w_in, 0));
+  if (M == 0) {
+    ok(cudaMemsetAsync(dwg_d, 0, static_cast<size_t>(2 * K * N + 2 * N) * 2, cs));
+  }
+  int64_t split_off = 0;
+  for (int64_t c = 0; c < hp.chunks && e == cudaSuccess; ++c) {
+    const int b = static_cast<int>(c & 1);
+    const int64_t r0 = c * hp.rows, rows = std::min(hp.rows, M - r0);
+    uint16_t* xin = dev16(hp.off_in[b]);
+    uint16_t* dyin = xin + hp.rows * K;
+    uint16_t* gin = dyin + hp.rows * N;
+    uint16_t* fcin = gin + hp.rows * N;
+    uint16_t* dxo = dev16(hp.off_dx[b]);
+    // rows of chunk c in; buffer set b was last read by chunk c - 2's kernels
+    if (c >= 2) ok(cudaStreamWaitEvent(hs->h2d, hs->computed[b], 0));
+    ok(cudaMemcpyAsync(xin, xh + r0 * K * 2, static_cast<size_t>(rows * K * 2), h2d, hs->h2d));
+    ok(cudaMemcpyAsync(dyin, dyh + r0 * N * 2, static_cast<size_t>(rows * N * 2), h2d, hs->h2d));
+    ok(cudaMemcpyAsync(gin, gh + r0 * N * 2, static_cast<size_t>(rows * N * 2), h2d, hs->h2d));
+    ok(cudaMemcpyAsync(fcin, fch + r0 * N * 2, static_cast<size_t>(rows * N * 2), h2d, hs->h2d));
+    ok(cudaEventRecord(hs->loaded[b], hs->h2d));
+    // compute; dx set b was last copied out for chunk c - 2
+    ok(cudaStreamWaitEvent(cs, hs->loaded[b], 0));
+    if (c >= 2) ok(cudaStreamWaitEvent(cs, hs->dx_out[b], 0));
+    ok(swg::launch_fused_x(dyin, gin, fcin, wg_d, wfc_d, dxo, nullptr, nullptr, rows, K, N, cs));
+    if (hp.chunks == 1) {
+      const swg::FwPlan fp = swg::fw_plan(rows, K, N, sms);
+      ok(swg::launch_fused_w(xin, dyin, gin, fcin, dwg_d, dwfc_d, dbg_d, dbfc_d, rows, K, N, ws + hp.off_dwp, fp,
+                             cs));
+    } else {
+      const swg::FwPlan fp = swg::fw_plan(rows, K, N, sms);
+      float* dwp = reinterpret_cast<float*>(ws + hp.off_dwp) + split_off * 2 * K * N;
+      float* dbp = reinterpret_cast<float*>(ws + hp.off_dbp) + split_off * 2 * N;
+      ok(swg::launch_fused_w_partials(xin, dyin, gin, fcin, rows, K, N, dwp, dbp, fp, cs));
+      split_off += fp.splits;
+    }
+    ok(cudaEventRecord(hs->computed[b], cs));
+    // dx of chunk c out
+    ok(cudaStreamWaitEvent(hs->d2h, hs->computed[b], 0));
+    ok(cudaMemcpyAsync(dxh + r0 * K * 2, dxo, static_cast<size_t>(rows * K * 2), d2h, hs->d2h));
+    ok(cudaEventRecord(hs->dx_out[b], hs->d2h));
+  }
+  if (hp.chunks > 1) {
+    ok(swg::launch_w_split_reduce(reinterpret_cast<const float*>(ws + hp.off_dwp), hp.splits_total, K, N, dwg_d,
+                                  dwfc_d, cs));
+    ok(swg::launch_db_reduce(reinterpret_cast<const float*>(ws + hp.off_dbp), hp.splits_total, N, dbg_d, dbfc_d,
+                             cs));
+  }
+  ok(cudaEventRecord(hs->reduced, cs));
+  ok(cudaStreamWaitEvent(hs->d2h, hs->reduced, 0));
+  ok(cudaMemcpyAsync(dw_g, dwg_d, kn, d2h, hs->d2h));
+  ok(cudaMemcpyAsync(dw_fc, dwfc_d, kn, d2h, hs->d2h));
+  ok(cudaMemcpyAsync(db_g, dbg_d, N * 2, d2h, hs->d2h));
+  ok(cudaMemcpyAsync(db_fc, dbfc_d, N * 2, d2h, hs->d2h));
+  ok(cudaEventRecord(hs->end, hs->d2h));
+  ok(cudaStreamWaitEvent(cs, hs->end, 0));
+  return cuda_status(e);
 }
 
 // ---------------------------------------------------------------- whole backward

@@ -768,9 +768,13 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
                          true);
 }
 
-cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
-                           uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
-                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+namespace {
+
+// the FW kernel alone: fp32 split partials into dw_part / db_part when plan.splits > 1, else bf16 dw
+// straight into dw_g, dw_fc (db always as partials)
+cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                             uint16_t* dw_g, uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, float* dw_part,
+                             float* db_part, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
   CUtensorMap mdy, mg, mfc, mx2, mx3;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 64) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 64) ||
@@ -799,9 +803,8 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   a.fc = fc;
   a.dw_g = dw_g;
   a.dw_fc = dw_fc;
-  const size_t dw_part = plan.splits > 1 ? static_cast<size_t>(plan.splits) * 2 * K * N * sizeof(float) : 0;
-  a.ws = static_cast<float*>(ws);
-  a.db_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(dw_part));
+  a.ws = dw_part;
+  a.db_part = db_part;
   a.splits = static_cast<int>(plan.splits);
   a.kb_per = static_cast<int>(plan.kb_per);
   a.nkb_total = static_cast<int>((M + 63) / 64);
@@ -809,13 +812,31 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   a.x3d = x3d;
   a.accumulate = accumulate ? 1 : 0;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
-  cudaError_t e = launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
+  return launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
+}
+
+}  // namespace
+
+cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                           uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
+                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+  const size_t dw_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * 2 * K * N * sizeof(float) : 0;
+  float* dw_part = static_cast<float*>(ws);
+  float* db_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(dw_bytes));
+  cudaError_t e = launch_fw_kernel(x, dy, g, fc, dw_g, dw_fc, M, K, N, dw_part, db_part, plan, stream, accumulate);
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {
-    e = launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
+    e = launch_w_split_reduce(dw_part, plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
     if (e != cudaSuccess) return e;
   }
-  return launch_db_reduce(a.db_part, plan.splits, N, db_g, db_fc, stream, accumulate);
+  return launch_db_reduce(db_part, plan.splits, N, db_g, db_fc, stream, accumulate);
+}
+
+cudaError_t launch_fused_w_partials(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                                    int64_t M, int64_t K, int64_t N, float* dw_part, float* db_part,
+                                    const FwPlan& plan, cudaStream_t stream) {
+  if (plan.splits < 2) return cudaErrorInvalidValue;  // one split would write bf16 dw directly
+  return launch_fw_kernel(x, dy, g, fc, nullptr, nullptr, M, K, N, dw_part, db_part, plan, stream, false);
 }
 
 }  // namespace swg

@@ -93,6 +93,11 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
                            int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate = false);
 cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
                                   uint16_t* dw_fc, cudaStream_t stream, bool accumulate = false);
+// the fused w stage's kernel alone (plan.splits >= 2): fp32 partials into dw_part [splits][2][K][N] and
+// db_part [splits][2N], no reduction (the caller reduces several such blocks at once)
+cudaError_t launch_fused_w_partials(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                                    int64_t M, int64_t K, int64_t N, float* dw_part, float* db_part,
+                                    const FwPlan& plan, cudaStream_t stream);
 
 // tensor-map encoding (driver entry point resolved once)
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,

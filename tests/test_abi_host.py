@@ -215,3 +215,22 @@ def test_group_norm_argument_checks(swg):
     # empty without parameter gradients: nothing to do, no device needed, NULL data pointers accepted
     assert gn(None, None, None, None, None, None, 0, 8, 12, 4, 1e-5, b.SWG_BF16, None, 0, None) == b.SWG_OK
     assert gn(None, None, None, None, None, None, 2, 8, 0, 4, 1e-5, b.SWG_F16, None, 0, None) == b.SWG_OK
+
+
+def test_host_path_argument_checks(swg):
+    lib, b = _lib(swg)
+    A = [FAKE + i * 0x1000000 for i in range(11)]  # x, w_g, w_fc, dy, g, fc, dx, dw_g, dw_fc, db_g, db_fc
+    assert lib.swiglu_bwd_host_workspace_size(220000, 512, 1024) > 0
+    assert lib.swiglu_bwd_host_workspace_size(-1, 512, 1024) == 0
+    # K, N not multiples of 8; negative M
+    assert lib.swiglu_bwd_host(*A, 4, 12, 16, FAKE, 1 << 30, None) == b.SWG_ERR_UNSUPPORTED
+    assert lib.swiglu_bwd_host(*A, -1, 8, 16, FAKE, 1 << 30, None) == b.SWG_ERR_PARAM_INVALID
+    # NULL weights, outputs or (M > 0) activations
+    for i in (1, 6, 7, 10, 0, 3):
+        args = list(A)
+        args[i] = None
+        assert lib.swiglu_bwd_host(*args, 4, 8, 16, FAKE, 1 << 30, None) == b.SWG_ERR_NULLPTR, i
+    # dx overlapping dy
+    args = list(A)
+    args[6] = A[3] + 16
+    assert lib.swiglu_bwd_host(*args, 4, 8, 16, FAKE, 1 << 30, None) == b.SWG_ERR_PARAM_INVALID
