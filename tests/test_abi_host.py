@@ -234,3 +234,41 @@ def test_host_path_argument_checks(swg):
     args = list(A)
     args[6] = A[3] + 16
     assert lib.swiglu_bwd_host(*args, 4, 8, 16, FAKE, 1 << 30, None) == b.SWG_ERR_PARAM_INVALID
+
+
+def _al256(v):
+    return (v + 255) & ~255
+
+
+def _fw_splits(M, K, N, sms):
+    nkb = (M + 63) // 64
+    tiles = ((N + 63) // 64) * ((K + 511) // 512)
+    s = max(1, sms // tiles)
+    s = min(s, max(1, nkb // 8), 64)
+    kb_per = (nkb + s - 1) // s if nkb > 0 else 0
+    return (nkb + kb_per - 1) // kb_per if kb_per > 0 else 1
+
+
+def _fw_ws(M, K, N, sms):
+    s = _fw_splits(M, K, N, sms)
+    return _al256(s * 2 * K * N * 4 if s > 1 else 0) + _al256(s * 2 * N * 4)
+
+
+@pytest.mark.parametrize("M", [0, 256, 40000, 65535, 65536, 70001, 220000, 3_000_000])
+def test_host_path_workspace_follows_the_chunk_plan(swg, M):
+    # without a device the library plans for 148 SMs; the layout: W | 2 input sets | 2 dx sets |
+    # outputs | partials of every chunk (or the fused w stage's own workspace for one chunk)
+    K, N, sms = 512, 1024, 148
+    chunks = min(M // 32768, 256) if M >= 65536 else (1 if M > 0 else 0)
+    rows = ((((M + chunks - 1) // chunks) + 63) // 64) * 64 if chunks else 0
+    if chunks > 1:
+        last = M - (chunks - 1) * rows
+        assert 16384 <= last <= rows  # every chunk splits over M
+    total = _al256(2 * K * N * 2) + 2 * _al256(rows * (K + 3 * N) * 2) + 2 * _al256(rows * K * 2)
+    total += _al256((2 * K * N + 2 * N) * 2)
+    if chunks > 1:
+        st = sum(_fw_splits(min(rows, M - c * rows), K, N, sms) for c in range(chunks))
+        total += _al256(st * 2 * K * N * 4) + _al256(st * 2 * N * 4)
+    elif chunks == 1:
+        total += _al256(_fw_ws(M, K, N, sms))
+    assert swg.swiglu_bwd_host_workspace_size(M, K, N) == total
