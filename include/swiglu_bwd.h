@@ -284,7 +284,7 @@ swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x,
  * dbeta added over samples in fp64); each output is rounded once (RNE);
  * results are bitwise reproducible.
  * Errors: G < 1, C not a multiple of G, a negative size or a negative / NaN eps
- * -> SWG_ERR_PARAM_INVALID; N G > 2^28 -> SWG_ERR_UNSUPPORTED; x, dy or dx NULL
+ * -> SWG_ERR_PARAM_INVALID; N G >= 2^28 or N C HxW >= 2^60 -> SWG_ERR_UNSUPPORTED; x, dy or dx NULL
  * with N C HxW > 0 -> SWG_ERR_NULLPTR; outputs overlapping inputs or each other
  * -> SWG_ERR_PARAM_INVALID. Empty (N C HxW == 0): no dx work; dgamma, dbeta
  * (sums over nothing) are written as zeros. */

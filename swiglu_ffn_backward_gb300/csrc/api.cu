@@ -141,8 +141,11 @@ swg_status group_norm_bwd(const void* dy, const void* x, const void* gamma, void
                           void* workspace, size_t workspace_bytes, swg_stream_t stream) {
   if (dtype != SWG_F32 && dtype != SWG_F16 && dtype != SWG_BF16) return SWG_ERR_PARAM_INVALID;
   if (N < 0 || C < 0 || HxW < 0 || G < 1 || C % G != 0 || !(eps >= 0.0f)) return SWG_ERR_PARAM_INVALID;
-  if (N > kMaxDim || C > kMaxDim || HxW > (int64_t(1) << 40) || N * G > (int64_t(1) << 28))
+  // sizes: every index fits 64 bits (N C HxW elements, and their bytes, below 2^60); the grid of
+  // N G clusters of up to 8 CTAs stays below 2^31 blocks
+  if (N > kMaxDim || C > kMaxDim || HxW > (int64_t(1) << 40) || N * G >= (int64_t(1) << 28))
     return SWG_ERR_UNSUPPORTED;
+  if (N > 0 && C > 0 && HxW > ((int64_t(1) << 60) / N) / C) return SWG_ERR_UNSUPPORTED;
   const int64_t es = dtype == SWG_F32 ? 4 : 2;
   const int64_t n = N * C * HxW;
   const bool params = dgamma != nullptr || dbeta != nullptr;

@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "swg_device.cuh"
 #include "swg_launch.h"
 
@@ -549,7 +551,9 @@ inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 template <typename T, int kMode>
 cudaError_t launch_mode(const GnArgs& a, int64_t groups_total, cudaStream_t stream) {
   const size_t smem = 2 * static_cast<size_t>(a.stage) * sizeof(T);
+  static std::mutex mu;
   static bool attr_set = false;  // the attribute allows the largest stage; set once per instantiation
+  std::lock_guard<std::mutex> lk(mu);
   if (!attr_set) {
     cudaError_t err = cudaFuncSetAttribute(gn_bwd_kernel<T, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kStageBytes);
@@ -575,10 +579,12 @@ cudaError_t launch_mode(const GnArgs& a, int64_t groups_total, cudaStream_t stre
 template <typename T, bool kVec>
 cudaError_t launch_pipe(const GnArgs& a, int64_t items, cudaStream_t stream) {
   const size_t smem = 4 * static_cast<size_t>(a.slice) * sizeof(T);
+  static std::mutex mu;  // guards the attribute flag and the occupancy cache
   static bool attr_set = false;
   static int cached_S = 0, cached_clusters = 0;
   static size_t cached_smem = 0;
   static int cached_dev = -1;
+  std::lock_guard<std::mutex> lk(mu);
   if (!attr_set) {
     cudaError_t err = cudaFuncSetAttribute(gn_bwd_pipe_kernel<T, kVec>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kPipeMaxSliceBytes);

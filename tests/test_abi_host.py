@@ -190,8 +190,9 @@ def test_group_norm_argument_checks(swg):
     assert gn(*A, 2, 8, 12, 4, float("nan"), b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
     assert gn(*A, 2, 8, 12, 4, -1.0, b.SWG_F32, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
     assert gn(*A, 2, 8, 12, 4, 1e-5, 9, FAKE, ws_ok, None) == b.SWG_ERR_PARAM_INVALID
-    # too many (sample, group) pairs for the grid
-    assert gn(*A, 1 << 20, 1 << 9, 1, 1 << 9, 1e-5, b.SWG_F32, FAKE, 1 << 40, None) == b.SWG_ERR_UNSUPPORTED
+    # too many (sample, group) pairs for the grid; an element count past 2^60
+    assert gn(*A, 1 << 19, 1 << 9, 1, 1 << 9, 1e-5, b.SWG_F32, FAKE, 1 << 40, None) == b.SWG_ERR_UNSUPPORTED
+    assert gn(*A, 1 << 20, 1 << 20, 1 << 21, 1, 1e-5, b.SWG_F32, FAKE, 1 << 40, None) == b.SWG_ERR_UNSUPPORTED
     # NULL x, dy or dx for a non-empty tensor
     for i in (0, 1, 3):
         args = list(A)
