@@ -364,11 +364,31 @@ def run_ours(args, rank, world):
     gn_ms = time_rot(gn_ours)
     swg.swg_check()
     gn_torch_ms = time_rot(gn_torch)
+
+    def time_graph(fn, reps=20):
+        # the same calls replayed from a CUDA graph: no host launch overhead between them
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for s_ in gsets:
+                fn(s_)
+        for _ in range(3):
+            graph.replay()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        return g0.elapsed_time(g1) / (reps * len(gsets))
+
+    gn_graph_ms = time_graph(gn_ours)
+    swg.swg_check()
     gn_bytes = 3.0 * gN * gC * gHW * 2 + 3.0 * gC * 2
     gn = {"workload": "resnet50 stage-1 activations, batch 32", "shape": [gN, gC, 56, 56], "groups": gG,
           "dtype": "f16", "ms": round(gn_ms, 5), "gbs": round(gn_bytes / (gn_ms * 1e-3) / 1e9, 1),
           "frac_hbm": round(gn_bytes / (gn_ms * 1e-3) / 1e9 / pk["hbm"], 4),
-          "torch_native_ms": round(gn_torch_ms, 5)}
+          "graph_ms": round(gn_graph_ms, 5), "torch_native_ms": round(gn_torch_ms, 5)}
     del gsets
 
     # accumulate mode: the public whole-backward call (fused chain, dg/dfc not
