@@ -12,7 +12,7 @@
 //
 // One cluster of S CTAs (S <= 8) per (sample, group). CTA k of the cluster owns
 // a contiguous slice of the group and brings its x and dy into shared memory
-// with bulk copies, in up to four parts with one mbarrier each (pass 1 starts on
+// with bulk copies, in up to two parts with one mbarrier each (pass 1 starts on
 // the first part while the others arrive), so HBM sees each input once:
 //   pass 1    shifted sums, shift K = the group's first x (the shifted-data
 //             variance of Chan, Golub and LeVeque, "Algorithms for computing the
@@ -45,7 +45,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kParts = 4;                  // bulk-copy parts per stage, one mbarrier each
+constexpr int kParts = 2;                  // bulk-copy parts per stage, one mbarrier each (measured: 2 over 4 and 1)
 constexpr int kStageBytes = 96 * 1024;     // largest x and dy stage (slices longer than it are streamed)
 constexpr int kSliceBytes = 48 * 1024;     // target x and dy bytes per CTA (measured: 48 KB over 24 and 12)
 constexpr int kMinBlocks = 1024 / kThreads;  // resident CTAs per SM the register budget is set for
