@@ -373,7 +373,17 @@ def swiglu_bwd_host(x, w_g, w_fc, dy, g, fc, out: dict | None = None, workspace=
     N = ins["w_g"].shape[1]
     if out is None:
         out = {}
+    for k, t in ins.items():
+        want = {"x": M * K, "w_g": K * N, "w_fc": K * N, "dy": M * N, "g": M * N, "fc": M * N}[k]
+        if t.numel() != want:
+            raise ValueError(f"{k} must have {want} elements for M={M}, K={K}, N={N}")
     shapes = dict(dx=(M, K), dw_g=(K, N), dw_fc=(K, N), db_g=(1, N), db_fc=(1, N))
+    for k, t in out.items():
+        shp = shapes[k]
+        # the library copies into these buffers: a short or strided one would be overrun
+        if (not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16
+                or t.numel() != shp[0] * shp[1] or not t.is_contiguous()):
+            raise ValueError(f"out[{k!r}] must be a contiguous bf16 CPU tensor of {shp[0] * shp[1]} elements")
     for k, shp in shapes.items():
         if k not in out:
             out[k] = torch.empty(shp, dtype=torch.bfloat16, pin_memory=True)

@@ -273,3 +273,17 @@ def test_host_path_workspace_follows_the_chunk_plan(swg, M):
     elif chunks == 1:
         total += _al256(_fw_ws(M, K, N, sms))
     assert swg.swiglu_bwd_host_workspace_size(M, K, N) == total
+
+
+def test_host_path_binding_checks_buffers(swg):
+    import torch
+    bf = dict(dtype=torch.bfloat16)
+    M, K, N = 4, 8, 16
+    ins = dict(x=torch.zeros(M, K, **bf), w_g=torch.zeros(K, N, **bf), w_fc=torch.zeros(K, N, **bf),
+               dy=torch.zeros(M, N, **bf), g=torch.zeros(M, N, **bf), fc=torch.zeros(M, N, **bf))
+    with pytest.raises(ValueError):  # a short output would be overrun by the copies
+        swg.swiglu_bwd_host(**ins, out={"dx": torch.zeros(M, K - 1, **bf)})
+    with pytest.raises(ValueError):  # dy with the wrong row count
+        swg.swiglu_bwd_host(**dict(ins, dy=torch.zeros(M + 1, N, **bf)))
+    with pytest.raises(TypeError):   # fp32 inputs
+        swg.swiglu_bwd_host(**dict(ins, x=torch.zeros(M, K)))
