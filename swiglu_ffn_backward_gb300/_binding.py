@@ -147,6 +147,21 @@ def _workspace(nbytes: int, device, given):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
+def _out(t, shape, dtype, device, name="output"):
+    """An output buffer: allocated when None, else checked. A short, strided,
+    mistyped or other-device tensor would be written out of bounds by the
+    kernels, so it is refused here."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    n = 1
+    for d in shape:
+        n *= d
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != torch.device(device)
+            or t.dtype != dtype or t.numel() != n or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor of {n} elements on {device}")
+    return t
+
+
 def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
@@ -165,9 +180,9 @@ def swiglu_bwd_x_fused(dy, g, fc, w_g, w_fc, dx=None, dg=None, dfc=None, return_
     K = w_g.shape[0]
     if g.shape != dy.shape or fc.shape != dy.shape or w_g.shape != (K, N) or w_fc.shape != (K, N):
         raise ValueError("shape mismatch: dy, g, fc [M, N]; w_g, w_fc [K, N]")
-    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    mk = lambda t, shape: _out(t, shape, torch.bfloat16, dy.device)  # noqa: E731
     dx = mk(dx, (M, K))
-    if return_dg:
+    if return_dg or dg is not None or dfc is not None:
         dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
     _check(lib.swiglu_bwd_x_fused(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(),
                                   dx.data_ptr(), _ptr(dg), _ptr(dfc), M, K, N, _stream(stream)),
@@ -183,7 +198,7 @@ def swiglu_bwd_w_fused(x, dy, g, fc, dw_g=None, dw_fc=None, db_g=None, db_fc=Non
     N = dy.shape[1]
     if dy.shape != (M, N) or g.shape != (M, N) or fc.shape != (M, N):
         raise ValueError("dy, g, fc must be [M, N] with M = x.shape[0]")
-    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=x.device) if t is None else t  # noqa: E731
+    mk = lambda t, shape: _out(t, shape, torch.bfloat16, x.device)  # noqa: E731
     dw_g, dw_fc = mk(dw_g, (K, N)), mk(dw_fc, (K, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
     ws = _workspace(lib.swiglu_bwd_w_fused_workspace_size(M, K, N), x.device, workspace)
@@ -216,7 +231,7 @@ def swiglu_bwd_b(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, workspace=
     M, N = dy.shape
     if g.shape != dy.shape or fc.shape != dy.shape:
         raise ValueError("dy, g, fc must have the same [M, N] shape")
-    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    mk = lambda t, shape: _out(t, shape, torch.bfloat16, dy.device)  # noqa: E731
     dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
     ws = _workspace(lib.swiglu_bwd_b_workspace_size(M, N), dy.device, workspace)
@@ -233,10 +248,8 @@ def swiglu_bwd_w(x, dg, dfc, dw_g=None, dw_fc=None, workspace=None, stream=None)
     N = dg.shape[1]
     if dg.shape != (M, N) or dfc.shape != (M, N):
         raise ValueError("dg, dfc must be [M, N] with M = x.shape[0]")
-    if dw_g is None:
-        dw_g = torch.empty((K, N), dtype=torch.bfloat16, device=x.device)
-    if dw_fc is None:
-        dw_fc = torch.empty((K, N), dtype=torch.bfloat16, device=x.device)
+    dw_g = _out(dw_g, (K, N), torch.bfloat16, x.device, "dw_g")
+    dw_fc = _out(dw_fc, (K, N), torch.bfloat16, x.device, "dw_fc")
     ws = _workspace(lib.swiglu_bwd_w_workspace_size(M, K, N), x.device, workspace)
     _check(lib.swiglu_bwd_w(x.data_ptr(), dg.data_ptr(), dfc.data_ptr(), dw_g.data_ptr(), dw_fc.data_ptr(),
                             M, K, N, _ptr(ws), _nbytes(ws), _stream(stream)), "swiglu_bwd_w")
@@ -250,8 +263,7 @@ def swiglu_bwd_x(dg, dfc, w_g, w_fc, dx=None, stream=None):
     K = w_g.shape[0]
     if dfc.shape != (M, N) or w_g.shape != (K, N) or w_fc.shape != (K, N):
         raise ValueError("shape mismatch: dg, dfc [M, N]; w_g, w_fc [K, N]")
-    if dx is None:
-        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dg.device)
+    dx = _out(dx, (M, K), torch.bfloat16, dg.device, "dx")
     _check(lib.swiglu_bwd_x(dg.data_ptr(), dfc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dx.data_ptr(),
                             M, K, N, _stream(stream)), "swiglu_bwd_x")
     return dx
@@ -275,8 +287,7 @@ def swiglu_fwd(x, w_g, w_fc, b_g=None, b_fc=None, out: dict | None = None, strea
         biases.append(b)
     out = dict(out or {})
     for k in ("g", "fc", "y"):
-        if out.get(k) is None:
-            out[k] = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+        out[k] = _out(out.get(k), (M, N), torch.bfloat16, x.device, k)
     _check(lib.swiglu_fwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), _ptr(biases[0]), _ptr(biases[1]),
                           out["g"].data_ptr(), out["fc"].data_ptr(), out["y"].data_ptr(), M, K, N,
                           _stream(stream)), "swiglu_fwd")
@@ -301,11 +312,10 @@ def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = T
     if accumulate and any(out.get(k) is None for k in ("dw_g", "dw_fc", "db_g", "db_fc")):
         raise ValueError("accumulate=True needs dw_g, dw_fc, db_g and db_fc in `out`")
     shapes = dict(dx=(M, K), dw_g=(K, N), dw_fc=(K, N), db_g=(1, N), db_fc=(1, N))
-    if return_dg:
+    if return_dg or out.get("dg") is not None or out.get("dfc") is not None:
         shapes.update(dg=(M, N), dfc=(M, N))
     for k, shp in shapes.items():
-        if out.get(k) is None:
-            out[k] = torch.empty(shp, dtype=torch.bfloat16, device=x.device)
+        out[k] = _out(out.get(k), shp, torch.bfloat16, x.device, k)
     flags = (SWG_FUSED if fused else SWG_UNFUSED) | (SWG_ACCUMULATE if accumulate else 0)
     ws_flags = flags | (SWG_WS_DG_GIVEN if return_dg else 0)
     ws = _workspace(lib.swiglu_bwd_workspace_size(M, K, N, ws_flags), x.device, workspace)
@@ -326,8 +336,7 @@ def swish_grad(grad, x, scale=None, grad_x=None, stream=None):
     if grad.dtype not in _DTYPE:
         raise TypeError(f"unsupported dtype {grad.dtype}")
     grad, x = grad.contiguous(), x.contiguous()
-    if grad_x is None:
-        grad_x = torch.empty_like(grad)
+    grad_x = _out(grad_x, tuple(grad.shape), grad.dtype, grad.device, "grad_x")
     sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
     _check(lib.swish_grad(grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
                           _DTYPE[grad.dtype], _stream(stream)), "swish_grad")
@@ -349,8 +358,7 @@ def act_grad(grad, x, act: str, grad_x=None, stream=None):
     if grad.dtype not in _DTYPE:
         raise TypeError(f"unsupported dtype {grad.dtype}")
     grad, x = grad.contiguous(), x.contiguous()
-    if grad_x is None:
-        grad_x = torch.empty_like(grad)
+    grad_x = _out(grad_x, tuple(grad.shape), grad.dtype, grad.device, "grad_x")
     _check(lib.act_grad(grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
                         _DTYPE[grad.dtype], _stream(stream)), "act_grad")
     return grad_x
@@ -421,13 +429,10 @@ def group_norm_bwd(dy, x, num_groups: int, gamma=None, eps: float = 1e-5, params
             raise ValueError("gamma must be a CUDA tensor of C elements with x's dtype")
         gamma = gamma.contiguous()
     dy, x = dy.contiguous(), x.contiguous()
-    if dx is None:
-        dx = torch.empty_like(x)
+    dx = _out(dx, tuple(x.shape), x.dtype, x.device, "dx")
     if params:
-        if dgamma is None:
-            dgamma = torch.empty(C, dtype=x.dtype, device=x.device)
-        if dbeta is None:
-            dbeta = torch.empty(C, dtype=x.dtype, device=x.device)
+        dgamma = _out(dgamma, (C,), x.dtype, x.device, "dgamma")
+        dbeta = _out(dbeta, (C,), x.dtype, x.device, "dbeta")
         ws = _workspace(group_norm_bwd_workspace_size(N, C, HxW, num_groups), x.device, workspace)
     else:
         dgamma = dbeta = ws = None
@@ -446,7 +451,7 @@ def swiglu_bwd_b_noalloc(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, st
     M, N = dy.shape
     if g.shape != dy.shape or fc.shape != dy.shape:
         raise ValueError("dy, g, fc must have the same [M, N] shape")
-    mk = lambda t, shape: torch.empty(shape, dtype=torch.bfloat16, device=dy.device) if t is None else t  # noqa: E731
+    mk = lambda t, shape: _out(t, shape, torch.bfloat16, dy.device)  # noqa: E731
     dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
     _check(lib.swiglu_bwd_b_noalloc(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),

@@ -81,3 +81,24 @@ def test_act_grad_rejects_unknown_activation():
     t = torch.zeros(8, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         swg.act_grad(t, t, "relu")
+
+
+def test_bindings_refuse_outputs_that_would_be_overrun():
+    swg = _swg()
+    g, x = swish_inputs(1000, torch.bfloat16, device="cuda", seed=3)
+    for bad in (torch.empty(999, dtype=torch.bfloat16, device="cuda"),         # short
+                torch.empty(1000, dtype=torch.float32, device="cuda"),         # wrong dtype
+                torch.empty(2000, dtype=torch.bfloat16, device="cuda")[::2],   # strided
+                torch.empty(1000, dtype=torch.bfloat16)):                       # host memory
+        with pytest.raises(ValueError):
+            swg.act_grad(g, x, "gelu", grad_x=bad)
+        with pytest.raises(ValueError):
+            swg.swish_grad(g, x, 1.0, grad_x=bad)
+    dy, xx, gam = (t.cuda() for t in __import__("synth").group_norm_inputs(2, 8, 12, 4, torch.float16, seed=1))
+    with pytest.raises(ValueError):
+        swg.group_norm_bwd(dy, xx, 4, gamma=gam, dgamma=torch.empty(7, dtype=torch.float16, device="cuda"))
+    from synth import SWIGLU_CONFIGS, swiglu_inputs
+    inp = swiglu_inputs(SWIGLU_CONFIGS["tiny"][0], device="cuda")
+    M, K = inp["x"].shape
+    with pytest.raises(ValueError):
+        swg.swiglu_bwd(**inp, out={"dx": torch.empty(M - 1, K, dtype=torch.bfloat16, device="cuda")})
