@@ -306,6 +306,20 @@ def run_ours(args, rank, world):
     sw_t = [sw_ev[i].elapsed_time(sw_ev[i + 1]) for i in range(sw_n)]
     sw_ms = statistics.median(sw_t)
     sw_gbs = 3.0 * SWISH_N * 2 / (sw_ms * 1e-3) / 1e9
+    # the same bytes (two reads, one write of 2^24 bf16) through PyTorch's own
+    # elementwise kernel, same rotation and timing: what a launch of this
+    # traffic reaches on this GPU
+    for i in range(sw_warm):
+        g_, x_, o_ = sets[i % 6]
+        torch.add(g_, x_, out=o_)
+    for i in range(sw_n):
+        g_, x_, o_ = sets[(sw_warm + i) % 6]
+        sw_ev[i].record(stream)
+        torch.add(g_, x_, out=o_)
+    sw_ev[sw_n].record(stream)
+    torch.cuda.synchronize()
+    add_ms = statistics.median([sw_ev[i].elapsed_time(sw_ev[i + 1]) for i in range(sw_n)])
+    add_gbs = 3.0 * SWISH_N * 2 / (add_ms * 1e-3) / 1e9
     # the sibling activation gradients through the same streaming kernels, same timing
     act = {}
     for name in ("gelu", "hardswish"):
@@ -488,9 +502,12 @@ def run_ours(args, rank, world):
     e2e_serial_ms = time_e2e(e2e_serial_step)
     del ws_host, dev_in, ws_full
 
+    llm = None if args.no_llm else llm_leg(swg, pk, stream)
+    tail = tail_leg(swg, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, sample_rows=args.cpu_rows)
+        cpu = cpu_baseline(inp)
 
     roof_ms = _roofline_ms(pk)
     line = {
@@ -507,11 +524,16 @@ def run_ours(args, rank, world):
         "other_path": {"path": other, "ms": round(ms_other, 4), "pct_roofline": round(roof_ms / ms_other, 4),
                        "stages": describe(per_other)},
         "swish_grad": {"n": SWISH_N, "dtype": "bf16", "scale": 1.702, "ms": round(sw_ms, 5),
-                       "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4)},
+                       "gbs": round(sw_gbs, 1), "frac_hbm": round(sw_gbs / pk["hbm"], 4),
+                       "same_bytes_torch_add": {"ms": round(add_ms, 5), "gbs": round(add_gbs, 1),
+                                                "frac_hbm": round(add_gbs / pk["hbm"], 4)},
+                       "vs_torch_add": round(add_ms / sw_ms, 4)},
         "act_grad": {"n": SWISH_N, "dtype": "bf16", **act},
         "group_norm_bwd": gn,
         "swiglu_bwd_call": {"unit": "ms", "fused": True, **acc_ms},
         "swiglu_fwd": fwd,
+        "llm": llm,
+        "tail": tail,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "call": "swiglu_bwd_host (fused; pinned host buffers, copies overlapped)",
                 "serial_ms": round(e2e_serial_ms, 3),
@@ -525,59 +547,201 @@ def run_ours(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
-# ---------------------------------------------------------------- CPU oracle
-def cpu_baseline(inp=None, sample_rows=32768, repeats=1):
-    """Time the fp64 oracle on the first `sample_rows` rows of the workload and
-    scale to the full M (the oracle's cost is linear in M)."""
-    import numpy as np
+# ---------------------------------------------------------------- other workloads
+def _chain_timer(seq, steps, stream):
+    """Per-launch CUDA-event times (ms, mean over steps) of a list of (name, fn), and the
+    whole sequence's time per step."""
     import torch
 
+    for _ in range(3):
+        for _, fn in seq:
+            fn()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        for j, (_, fn) in enumerate(seq):
+            evs[i][j].record(stream)
+            fn()
+        evs[i][len(seq)].record(stream)
+    torch.cuda.synchronize()
+    per = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps for j, (name, _) in enumerate(seq)}
+    total = sum(e[0].elapsed_time(e[len(seq)]) for e in evs) / steps
+    return total, per
+
+
+def llm_leg(swg, pk, stream, steps=10):
+    """The whole backward at LLM-FFN scale (M=16384 tokens, K=4096 hidden, N=14336
+    intermediate, bf16): both chains, per-kernel time and fraction of the measured
+    bf16 peak (burst and sustained), and which chain is faster at this shape."""
+    import torch
+
+    from synth import SWIGLU_CONFIGS, swiglu_inputs
+
+    sh = SWIGLU_CONFIGS["llm"][0]
+    Ml, Kl, Nl = sh.M, sh.K, sh.N
+    dev = torch.device("cuda")
+    inp = swiglu_inputs(sh, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    dg, dfc = torch.empty((Ml, Nl), **bf), torch.empty((Ml, Nl), **bf)
+    db_g, db_fc = torch.empty((1, Nl), **bf), torch.empty((1, Nl), **bf)
+    dw_g, dw_fc = torch.empty((Kl, Nl), **bf), torch.empty((Kl, Nl), **bf)
+    dx = torch.empty((Ml, Kl), **bf)
+    ws_b = torch.empty(max(swg.swiglu_bwd_b_workspace_size(Ml, Nl), 16), dtype=torch.uint8, device=dev)
+    ws_w = torch.empty(max(swg.swiglu_bwd_w_workspace_size(Ml, Kl, Nl), 16), dtype=torch.uint8, device=dev)
+    ws_fw = torch.empty(max(swg.swiglu_bwd_w_fused_workspace_size(Ml, Kl, Nl), 16), dtype=torch.uint8, device=dev)
+    chains = {
+        "unfused": [
+            ("b_stage", lambda: swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"], dg, dfc, db_g, db_fc,
+                                                 workspace=ws_b)),
+            ("w_gemm", lambda: swg.swiglu_bwd_w(inp["x"], dg, dfc, dw_g, dw_fc, workspace=ws_w)),
+            ("x_gemm", lambda: swg.swiglu_bwd_x(dg, dfc, inp["w_g"], inp["w_fc"], dx)),
+        ],
+        "fused": [
+            ("x_fused", lambda: swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"], dx)),
+            ("w_fused", lambda: swg.swiglu_bwd_w_fused(inp["x"], inp["dy"], inp["g"], inp["fc"], dw_g, dw_fc,
+                                                       db_g, db_fc, workspace=ws_fw)),
+        ],
+    }
+    flop_gemm = 4.0 * Ml * Kl * Nl
+    flop = 2 * flop_gemm
+    byts = 6.0 * Ml * Nl + 4.0 * Ml * Kl + 8.0 * Kl * Nl + 4.0 * Nl
+    roof_ms = max(flop / (pk["bf16"] * 1e12), byts / (pk["hbm"] * 1e9)) * 1e3
+    out = {"workload": "swiglu_bwd LLM FFN M=16384 K=4096 N=14336 bf16, seed 3", "M": Ml, "K": Kl, "N": Nl,
+           "roofline_ms": round(roof_ms, 4), "steps": steps}
+    for name, seq in chains.items():
+        total, per = _chain_timer(seq, steps, stream)
+        kern = {}
+        for k, t in per.items():
+            if k == "b_stage":
+                gbs = (10.0 * Ml * Nl + 4.0 * Nl) / (t * 1e-3) / 1e9
+                kern[k] = {"ms": round(t, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm"], 4)}
+            else:
+                tf = flop_gemm / (t * 1e-3) / 1e12
+                kern[k] = {"ms": round(t, 4), "tflops": round(tf, 1), "frac_burst": round(tf / pk["bf16"], 4),
+                           "frac_sustained": round(tf / pk["bf16_sustained"], 4)}
+        out[name] = {"ms": round(total, 4), "tflops": round(flop / (total * 1e-3) / 1e12, 1),
+                     "pct_roofline": round(roof_ms / total, 4), "kernels": kern}
+    swg.swg_check()
+    out["faster_path"] = min(chains, key=lambda n: out[n]["ms"])
+    del inp, dg, dfc, ws_b, ws_w, ws_fw
+    torch.cuda.empty_cache()
+    return out
+
+
+def tail_leg(swg, stream, reps=20):
+    """The dynamic-M tail sweep (K=512, N=1024, M in 1, 127, 1025, 4097, 65537): the
+    public whole-backward call per chain, microseconds per call. L2 is flushed
+    (a 512 MB write) before each timed call, outside its events."""
+    import torch
+
+    from synth import SWIGLU_CONFIGS, swiglu_inputs
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rows = []
+    for sh in SWIGLU_CONFIGS["tail"]:
+        inp = swiglu_inputs(sh, device="cuda")
+        r = {"M": sh.M}
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        out = dict(dx=torch.empty((sh.M, sh.K), **bf), dw_g=torch.empty((sh.K, sh.N), **bf),
+                   dw_fc=torch.empty((sh.K, sh.N), **bf), db_g=torch.empty((1, sh.N), **bf),
+                   db_fc=torch.empty((1, sh.N), **bf))
+        for fused in (False, True):
+            ws = torch.empty(max(swg.swiglu_bwd_workspace_size(sh.M, sh.K, sh.N, 1 if fused else 0), 16),
+                             dtype=torch.uint8, device="cuda")
+
+            def call():
+                swg.swiglu_bwd(**inp, fused=fused, return_dg=False, out=out, workspace=ws)
+
+            for _ in range(3):
+                call()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            r["fused_us" if fused else "unfused_us"] = round(statistics.median(ts) * 1e3, 2)
+        rows.append(r)
+    swg.swg_check()
+    del flush
+    return {"K": 512, "N": 1024, "call": "swiglu_bwd (dg, dfc not returned), L2 flushed before each call",
+            "rows": rows}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_inputs(inp, rows):
+    """The first `rows` rows of the workload widened exactly to fp64 (outside any timing)."""
+    import numpy as np
+
+    h = {}
+    for k, v in inp.items():
+        t = v[:rows] if k in ("x", "dy", "g", "fc") else v
+        h[k] = t.detach().float().cpu().numpy().astype(np.float64)
+    return h
+
+
+def _time_oracle(h):
     import oracle
+
+    t0 = time.perf_counter()
+    oracle.swiglu_bwd(h["x"], h["w_g"], h["w_fc"], h["dy"], h["g"], h["fc"], stage_dtype="bf16")
+    return time.perf_counter() - t0
+
+
+def _cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(inp=None):
+    """Time the fp64 oracle, as it stands, on the whole workload (all M rows) once."""
     from synth import SWIGLU_CONFIGS, swiglu_inputs
 
     if inp is None:
         inp = swiglu_inputs(SWIGLU_CONFIGS["pages"][0], device="cpu")
-    ms_ = min(sample_rows, M)
-    h = {}
-    for k, v in inp.items():
-        t = v[:ms_] if k in ("x", "dy", "g", "fc") else v
-        h[k] = t.detach().float().cpu().numpy().astype(np.float64)
-    times = []
-    for _ in range(repeats):
-        t0 = time.perf_counter()
-        oracle.swiglu_bwd(h["x"], h["w_g"], h["w_fc"], h["dy"], h["g"], h["fc"], stage_dtype="bf16")
-        times.append(time.perf_counter() - t0)
-    t = min(times)
-    full_ms = t * (M / ms_) * 1e3
-    del torch
-    return {"value": round(full_ms, 1), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {ms_} of {M} rows (K={K}, N={N}), fp64 numpy, scaled by M/{ms_}; "
-                      f"sample wall time {t:.2f} s; BLAS threads = library default"}
+    h = _oracle_inputs(inp, M)
+    t = _time_oracle(h)
+    del h
+    return {"value": round(t * 1e3, 1), "unit": "ms", "cores": _cpu_threads(), "kind": "oracle",
+            "sample": f"the whole workload (M={M}, K={K}, N={N}), one run of the fp64 numpy oracle; "
+                      f"BLAS threads = library default"}
 
 
 def run_reference(args, rank, world):
+    """The fp64 CPU oracle on the same workload, metric and unit. Each step runs
+    the oracle on a sample of the first `rows` rows (sized so that warm-up and
+    steps end within about two minutes); ms_per_step is the measured time of
+    such a step and value is that time scaled to all M rows (the oracle's work
+    is linear in M), labelled as an extrapolation in config."""
     if rank != 0:
         return
     from synth import SWIGLU_CONFIGS, swiglu_inputs
 
     inp = swiglu_inputs(SWIGLU_CONFIGS["pages"][0], device="cpu")
-    # size each step's row sample so that warmup + steps finish in about two minutes
-    probe = cpu_baseline(inp, sample_rows=2048)
-    sec_per_row = probe["value"] * 1e-3 / M
+    probe_rows = 2048
+    sec_per_row = _time_oracle(_oracle_inputs(inp, probe_rows)) / probe_rows
     budget = 120.0 / (args.steps + args.warmup + 1)
-    rows = int(min(args.ref_rows, max(256, budget / max(sec_per_row, 1e-12))))
+    rows = int(min(args.ref_rows, M, max(256, budget / max(sec_per_row, 1e-12))))
+    h = _oracle_inputs(inp, rows)
     for _ in range(args.warmup):
-        cpu_baseline(inp, sample_rows=rows)
-    vals = [cpu_baseline(inp, sample_rows=rows)["value"] for _ in range(args.steps)]
-    cb = cpu_baseline(inp, sample_rows=rows)
-    v = statistics.median(vals)
-    cb["value"] = v
+        _time_oracle(h)
+    t_steps = [_time_oracle(h) for _ in range(args.steps)]
+    step_ms = statistics.median(t_steps) * 1e3
+    v = round(step_ms * M / rows, 1)
+    cb = {"value": v, "unit": "ms", "cores": _cpu_threads(), "kind": "oracle",
+          "sample": f"first {rows} of {M} rows per step (K={K}, N={N}), fp64 numpy; value = step time x M/{rows}"}
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 2), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, bf16 inputs widened to fp64)",
-        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
-                   "path": "fp64 CPU oracle (numpy), row sample scaled to the full M"},
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "sample_rows": rows,
+                   "path": "fp64 CPU oracle (numpy) on the first sample_rows rows per step",
+                   "value_kind": f"extrapolated: measured step time x M/sample_rows = x {M / rows:.2f}"},
         "cpu_baseline": cb,
         "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -592,9 +756,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
                     help="which chain the timed step runs (the other is timed too and reported beside it)")
-    ap.add_argument("--cpu-rows", type=int, default=32768)
     ap.add_argument("--ref-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-llm", action="store_true", help="skip the LLM-FFN-shape leg")
     ap.add_argument("--m", type=int, default=None,
                     help="rows M of a smaller case of the same kernels (profiling only; the metric is M=220000)")
     ap.add_argument("--profile-only", action="store_true",

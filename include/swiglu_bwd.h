@@ -98,6 +98,26 @@ const char* swg_status_string(swg_status s);
  * returns SWG_ERR_CUDA if the stream reports an error. SWG_OK otherwise. */
 swg_status swg_check(swg_stream_t stream);
 
+/* ---- fault injection for tests of the timeout path ------------------------------
+ * No counterpart on the pages. Every pipeline wait in the tcgen05 kernels is a
+ * bounded spin (about 2 s); this arms a one-shot fault for the NEXT launch of
+ * one kernel by this process, so that a test can see a wait run out without
+ * faulting or hanging the GPU: that launch's operand producer stops issuing
+ * copies before ring entry `entry` (nothing is left in flight), and each of its
+ * waits gives up after `wait_limit_cycles` SM clock cycles. The consumer's wait
+ * on the missing entry then runs out; the kernel sets the status word, stops,
+ * waits (bounded) for the work it did issue, frees its tensor memory and
+ * returns. That launch's outputs are incomplete; swg_check() then reports
+ * SWG_ERR_TIMEOUT and clears the word, and later calls run normally.
+ *   kernel: SWG_INJECT_X_GEMM (the x stage's GEMM, swiglu_bwd_x and the
+ *           unfused swiglu_bwd) or SWG_INJECT_FUSED_X (the fused x kernel,
+ *           swiglu_bwd_x_fused and the fused swiglu_bwd).
+ * SWG_INJECT_NONE disarms an armed, unused injection (entry and limit are then
+ * ignored); a later call replaces it. Returns SWG_ERR_PARAM_INVALID for another
+ * kernel, entry < 0 or a limit below 1024 cycles. For tests only. */
+typedef enum { SWG_INJECT_NONE = 0, SWG_INJECT_X_GEMM = 1, SWG_INJECT_FUSED_X = 2 } swg_inject_kernel;
+swg_status swg_inject_stall(swg_inject_kernel kernel, int64_t entry, int64_t wait_limit_cycles);
+
 /* ---- b stage -----------------------------------------------------------------
  * [P1] "Algorithm overview and formulas" items 1-2; "Kernel signatures",
  * fused_swiglu_bwd_b_kernel(dy, g, fc, dg, dfc, db_g, db_fc):
@@ -123,9 +143,10 @@ swg_status swiglu_bwd_b(const void* dy, const void* g, const void* fc,
  * loads the library until the process exits. Nothing is allocated.
  * - Limit: the partials must fit the array, which holds for every M when
  *   N <= 524288; larger shapes return SWG_ERR_WORKSPACE with nothing launched.
- * - The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
+ * - Each call looks up the array's device address on the current device
+ *   (so calls stay valid across a cudaDeviceReset); the first call on a
+ *   device also loads the library's device code there, so make that first
+ *   call before any stream capture.
  * - Every call shares the array and it keeps the last call's contents (no
  *   call needs it zeroed). Calls that overlap on the GPU, e.g. on two streams
  *   at once, race on it and give wrong db; serialise them. */

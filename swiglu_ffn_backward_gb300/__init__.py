@@ -17,6 +17,9 @@ from ._binding import (  # noqa: F401
     SwgError,
     status_string,
     swg_check,
+    swg_inject_stall,
+    SWG_INJECT_FUSED_X,
+    SWG_INJECT_X_GEMM,
     swiglu_bwd,
     swiglu_bwd_b,
     swiglu_bwd_b_noalloc,

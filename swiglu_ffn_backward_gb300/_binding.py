@@ -49,6 +49,7 @@ EXPORTS = (
     "act_grad",
     "group_norm_bwd_workspace_size", "group_norm_bwd",
     "swiglu_bwd_host_workspace_size", "swiglu_bwd_host",
+    "swg_inject_stall",
 )
 
 
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
     lib.swg_status_string.restype = ctypes.c_char_p
     lib.swg_check.argtypes = [P]
     lib.swg_check.restype = st
+    lib.swg_inject_stall.argtypes = [ctypes.c_int, I64, I64]
+    lib.swg_inject_stall.restype = st
     lib.swiglu_bwd_b_workspace_size.argtypes = [I64, I64]
     lib.swiglu_bwd_b_workspace_size.restype = SZ
     lib.swiglu_bwd_b.argtypes = [P, P, P, P, P, P, P, I64, I64, P, SZ, P]
@@ -121,10 +124,41 @@ def _check(status: int, what: str) -> None:
         raise SwgError(status, f"{what}: {status_string(status)}")
 
 
-def _stream(stream=None) -> int:
+def _stream(stream=None, device=None) -> int:
+    """The raw handle of `stream`, or of the current stream of `device` when
+    stream is None. A torch stream of another device is refused: the kernels
+    would run on the wrong GPU."""
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        stream = torch.cuda.current_stream(device)
+    if hasattr(stream, "cuda_stream"):
+        if device is not None and getattr(stream, "device", None) is not None and \
+                torch.device(stream.device) != torch.device(device):
+            raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _device_of(*tensors) -> torch.device:
+    """The one CUDA device that every given tensor (None skipped) lives on.
+    The library launches on the current device, so tensors spread over two
+    GPUs, or on a GPU other than the current one without the switch below,
+    would be read through the wrong device's address space."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"all tensors must be on one device: got {dev} and {t.device}")
+    return dev
+
+
+def _call(dev, fn, *args):
+    """Run one C-ABI call with `dev` as the current device (and so the device
+    the library resolves its launch configuration and status word on)."""
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _ptr(t):
@@ -184,8 +218,9 @@ def swiglu_bwd_x_fused(dy, g, fc, w_g, w_fc, dx=None, dg=None, dfc=None, return_
     dx = mk(dx, (M, K))
     if return_dg or dg is not None or dfc is not None:
         dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
-    _check(lib.swiglu_bwd_x_fused(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(),
-                                  dx.data_ptr(), _ptr(dg), _ptr(dfc), M, K, N, _stream(stream)),
+    dev = _device_of(dy, g, fc, w_g, w_fc, dx, dg, dfc)
+    _check(_call(dev, lib.swiglu_bwd_x_fused, dy.data_ptr(), g.data_ptr(), fc.data_ptr(), w_g.data_ptr(),
+                 w_fc.data_ptr(), dx.data_ptr(), _ptr(dg), _ptr(dfc), M, K, N, _stream(stream, dev)),
            "swiglu_bwd_x_fused")
     return dx, dg, dfc
 
@@ -201,11 +236,22 @@ def swiglu_bwd_w_fused(x, dy, g, fc, dw_g=None, dw_fc=None, db_g=None, db_fc=Non
     mk = lambda t, shape: _out(t, shape, torch.bfloat16, x.device)  # noqa: E731
     dw_g, dw_fc = mk(dw_g, (K, N)), mk(dw_fc, (K, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
-    ws = _workspace(lib.swiglu_bwd_w_fused_workspace_size(M, K, N), x.device, workspace)
-    _check(lib.swiglu_bwd_w_fused(x.data_ptr(), dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dw_g.data_ptr(),
-                                  dw_fc.data_ptr(), db_g.data_ptr(), db_fc.data_ptr(), M, K, N, _ptr(ws),
-                                  _nbytes(ws), _stream(stream)), "swiglu_bwd_w_fused")
+    dev = _device_of(x, dy, g, fc, dw_g, dw_fc, db_g, db_fc, workspace)
+    ws = _workspace(_call(dev, lib.swiglu_bwd_w_fused_workspace_size, M, K, N), x.device, workspace)
+    _check(_call(dev, lib.swiglu_bwd_w_fused, x.data_ptr(), dy.data_ptr(), g.data_ptr(), fc.data_ptr(),
+                 dw_g.data_ptr(), dw_fc.data_ptr(), db_g.data_ptr(), db_fc.data_ptr(), M, K, N, _ptr(ws),
+                 _nbytes(ws), _stream(stream, dev)), "swiglu_bwd_w_fused")
     return dw_g, dw_fc, db_g, db_fc
+
+
+SWG_INJECT_X_GEMM = 1
+SWG_INJECT_FUSED_X = 2
+
+
+def swg_inject_stall(kernel: int, entry: int, wait_limit_cycles: int) -> None:
+    """Arm a one-shot stall in the next launch of `kernel` (tests of the timeout path;
+    see include/swiglu_bwd.h)."""
+    _check(lib.swg_inject_stall(kernel, entry, wait_limit_cycles), "swg_inject_stall")
 
 
 def swg_check(stream=None) -> None:
@@ -234,10 +280,11 @@ def swiglu_bwd_b(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, workspace=
     mk = lambda t, shape: _out(t, shape, torch.bfloat16, dy.device)  # noqa: E731
     dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
-    ws = _workspace(lib.swiglu_bwd_b_workspace_size(M, N), dy.device, workspace)
-    _check(lib.swiglu_bwd_b(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),
-                            db_g.data_ptr(), db_fc.data_ptr(), M, N, _ptr(ws), _nbytes(ws),
-                            _stream(stream)), "swiglu_bwd_b")
+    dev = _device_of(dy, g, fc, dg, dfc, db_g, db_fc, workspace)
+    ws = _workspace(_call(dev, lib.swiglu_bwd_b_workspace_size, M, N), dy.device, workspace)
+    _check(_call(dev, lib.swiglu_bwd_b, dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),
+                 db_g.data_ptr(), db_fc.data_ptr(), M, N, _ptr(ws), _nbytes(ws), _stream(stream, dev)),
+           "swiglu_bwd_b")
     return dg, dfc, db_g, db_fc
 
 
@@ -250,9 +297,10 @@ def swiglu_bwd_w(x, dg, dfc, dw_g=None, dw_fc=None, workspace=None, stream=None)
         raise ValueError("dg, dfc must be [M, N] with M = x.shape[0]")
     dw_g = _out(dw_g, (K, N), torch.bfloat16, x.device, "dw_g")
     dw_fc = _out(dw_fc, (K, N), torch.bfloat16, x.device, "dw_fc")
-    ws = _workspace(lib.swiglu_bwd_w_workspace_size(M, K, N), x.device, workspace)
-    _check(lib.swiglu_bwd_w(x.data_ptr(), dg.data_ptr(), dfc.data_ptr(), dw_g.data_ptr(), dw_fc.data_ptr(),
-                            M, K, N, _ptr(ws), _nbytes(ws), _stream(stream)), "swiglu_bwd_w")
+    dev = _device_of(x, dg, dfc, dw_g, dw_fc, workspace)
+    ws = _workspace(_call(dev, lib.swiglu_bwd_w_workspace_size, M, K, N), x.device, workspace)
+    _check(_call(dev, lib.swiglu_bwd_w, x.data_ptr(), dg.data_ptr(), dfc.data_ptr(), dw_g.data_ptr(),
+                 dw_fc.data_ptr(), M, K, N, _ptr(ws), _nbytes(ws), _stream(stream, dev)), "swiglu_bwd_w")
     return dw_g, dw_fc
 
 
@@ -264,8 +312,9 @@ def swiglu_bwd_x(dg, dfc, w_g, w_fc, dx=None, stream=None):
     if dfc.shape != (M, N) or w_g.shape != (K, N) or w_fc.shape != (K, N):
         raise ValueError("shape mismatch: dg, dfc [M, N]; w_g, w_fc [K, N]")
     dx = _out(dx, (M, K), torch.bfloat16, dg.device, "dx")
-    _check(lib.swiglu_bwd_x(dg.data_ptr(), dfc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dx.data_ptr(),
-                            M, K, N, _stream(stream)), "swiglu_bwd_x")
+    dev = _device_of(dg, dfc, w_g, w_fc, dx)
+    _check(_call(dev, lib.swiglu_bwd_x, dg.data_ptr(), dfc.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(),
+                 dx.data_ptr(), M, K, N, _stream(stream, dev)), "swiglu_bwd_x")
     return dx
 
 
@@ -288,9 +337,10 @@ def swiglu_fwd(x, w_g, w_fc, b_g=None, b_fc=None, out: dict | None = None, strea
     out = dict(out or {})
     for k in ("g", "fc", "y"):
         out[k] = _out(out.get(k), (M, N), torch.bfloat16, x.device, k)
-    _check(lib.swiglu_fwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), _ptr(biases[0]), _ptr(biases[1]),
-                          out["g"].data_ptr(), out["fc"].data_ptr(), out["y"].data_ptr(), M, K, N,
-                          _stream(stream)), "swiglu_fwd")
+    dev = _device_of(x, w_g, w_fc, biases[0], biases[1], out["g"], out["fc"], out["y"])
+    _check(_call(dev, lib.swiglu_fwd, x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), _ptr(biases[0]),
+                 _ptr(biases[1]), out["g"].data_ptr(), out["fc"].data_ptr(), out["y"].data_ptr(), M, K, N,
+                 _stream(stream, dev)), "swiglu_fwd")
     return out
 
 
@@ -318,11 +368,12 @@ def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = T
         out[k] = _out(out.get(k), shp, torch.bfloat16, x.device, k)
     flags = (SWG_FUSED if fused else SWG_UNFUSED) | (SWG_ACCUMULATE if accumulate else 0)
     ws_flags = flags | (SWG_WS_DG_GIVEN if return_dg else 0)
-    ws = _workspace(lib.swiglu_bwd_workspace_size(M, K, N, ws_flags), x.device, workspace)
-    _check(lib.swiglu_bwd(x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dy.data_ptr(), g.data_ptr(),
-                          fc.data_ptr(), _ptr(out.get("dg")), _ptr(out.get("dfc")), out["dx"].data_ptr(),
-                          out["dw_g"].data_ptr(), out["dw_fc"].data_ptr(), out["db_g"].data_ptr(),
-                          out["db_fc"].data_ptr(), M, K, N, flags, _ptr(ws), _nbytes(ws), _stream(stream)),
+    dev = _device_of(x, w_g, w_fc, dy, g, fc, workspace, *out.values())
+    ws = _workspace(_call(dev, lib.swiglu_bwd_workspace_size, M, K, N, ws_flags), x.device, workspace)
+    _check(_call(dev, lib.swiglu_bwd, x.data_ptr(), w_g.data_ptr(), w_fc.data_ptr(), dy.data_ptr(), g.data_ptr(),
+                 fc.data_ptr(), _ptr(out.get("dg")), _ptr(out.get("dfc")), out["dx"].data_ptr(),
+                 out["dw_g"].data_ptr(), out["dw_fc"].data_ptr(), out["db_g"].data_ptr(),
+                 out["db_fc"].data_ptr(), M, K, N, flags, _ptr(ws), _nbytes(ws), _stream(stream, dev)),
            "swiglu_bwd")
     return out
 
@@ -338,8 +389,9 @@ def swish_grad(grad, x, scale=None, grad_x=None, stream=None):
     grad, x = grad.contiguous(), x.contiguous()
     grad_x = _out(grad_x, tuple(grad.shape), grad.dtype, grad.device, "grad_x")
     sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
-    _check(lib.swish_grad(grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
-                          _DTYPE[grad.dtype], _stream(stream)), "swish_grad")
+    dev = _device_of(grad, x, grad_x)
+    _check(_call(dev, lib.swish_grad, grad.data_ptr(), x.data_ptr(), sc, grad_x.data_ptr(), grad.numel(),
+                 _DTYPE[grad.dtype], _stream(stream, dev)), "swish_grad")
     return grad_x
 
 
@@ -359,8 +411,9 @@ def act_grad(grad, x, act: str, grad_x=None, stream=None):
         raise TypeError(f"unsupported dtype {grad.dtype}")
     grad, x = grad.contiguous(), x.contiguous()
     grad_x = _out(grad_x, tuple(grad.shape), grad.dtype, grad.device, "grad_x")
-    _check(lib.act_grad(grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
-                        _DTYPE[grad.dtype], _stream(stream)), "act_grad")
+    dev = _device_of(grad, x, grad_x)
+    _check(_call(dev, lib.act_grad, grad.data_ptr(), x.data_ptr(), SWG_ACT[act], grad_x.data_ptr(), grad.numel(),
+                 _DTYPE[grad.dtype], _stream(stream, dev)), "act_grad")
     return grad_x
 
 
@@ -395,11 +448,14 @@ def swiglu_bwd_host(x, w_g, w_fc, dy, g, fc, out: dict | None = None, workspace=
     for k, shp in shapes.items():
         if k not in out:
             out[k] = torch.empty(shp, dtype=torch.bfloat16, pin_memory=True)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    ws = _workspace(swiglu_bwd_host_workspace_size(M, K, N), dev, workspace)
-    _check(lib.swiglu_bwd_host(*(ins[k].data_ptr() for k in ("x", "w_g", "w_fc", "dy", "g", "fc")),
-                               *(out[k].data_ptr() for k in ("dx", "dw_g", "dw_fc", "db_g", "db_fc")),
-                               M, K, N, _ptr(ws), _nbytes(ws), _stream(stream)), "swiglu_bwd_host")
+    # the device is the workspace's when one is given, else the current one
+    dev = workspace.device if workspace is not None else torch.device("cuda", torch.cuda.current_device())
+    if not dev.type == "cuda":
+        raise ValueError("workspace must be a CUDA tensor")
+    ws = _workspace(_call(dev, swiglu_bwd_host_workspace_size, M, K, N), dev, workspace)
+    _check(_call(dev, lib.swiglu_bwd_host, *(ins[k].data_ptr() for k in ("x", "w_g", "w_fc", "dy", "g", "fc")),
+                 *(out[k].data_ptr() for k in ("dx", "dw_g", "dw_fc", "db_g", "db_fc")),
+                 M, K, N, _ptr(ws), _nbytes(ws), _stream(stream, dev)), "swiglu_bwd_host")
     return out
 
 
@@ -436,9 +492,10 @@ def group_norm_bwd(dy, x, num_groups: int, gamma=None, eps: float = 1e-5, params
         ws = _workspace(group_norm_bwd_workspace_size(N, C, HxW, num_groups), x.device, workspace)
     else:
         dgamma = dbeta = ws = None
-    _check(lib.group_norm_bwd(dy.data_ptr(), x.data_ptr(), _ptr(gamma), dx.data_ptr(), _ptr(dgamma), _ptr(dbeta),
-                              N, C, HxW, num_groups, float(eps), _DTYPE[x.dtype], _ptr(ws), _nbytes(ws),
-                              _stream(stream)), "group_norm_bwd")
+    dev = _device_of(dy, x, gamma, dx, dgamma, dbeta, ws)
+    _check(_call(dev, lib.group_norm_bwd, dy.data_ptr(), x.data_ptr(), _ptr(gamma), dx.data_ptr(), _ptr(dgamma),
+                 _ptr(dbeta), N, C, HxW, num_groups, float(eps), _DTYPE[x.dtype], _ptr(ws), _nbytes(ws),
+                 _stream(stream, dev)), "group_norm_bwd")
     return dx, dgamma, dbeta
 
 
@@ -454,7 +511,8 @@ def swiglu_bwd_b_noalloc(dy, g, fc, dg=None, dfc=None, db_g=None, db_fc=None, st
     mk = lambda t, shape: _out(t, shape, torch.bfloat16, dy.device)  # noqa: E731
     dg, dfc = mk(dg, (M, N)), mk(dfc, (M, N))
     db_g, db_fc = mk(db_g, (1, N)), mk(db_fc, (1, N))
-    _check(lib.swiglu_bwd_b_noalloc(dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(), dfc.data_ptr(),
-                                    db_g.data_ptr(), db_fc.data_ptr(), M, N, _stream(stream)),
+    dev = _device_of(dy, g, fc, dg, dfc, db_g, db_fc)
+    _check(_call(dev, lib.swiglu_bwd_b_noalloc, dy.data_ptr(), g.data_ptr(), fc.data_ptr(), dg.data_ptr(),
+                 dfc.data_ptr(), db_g.data_ptr(), db_fc.data_ptr(), M, N, _stream(stream, dev)),
            "swiglu_bwd_b_noalloc")
     return dg, dfc, db_g, db_fc

@@ -95,6 +95,17 @@ const char* swg_status_string(swg_status s) {
   return "SWG_ERR_?: unknown status";
 }
 
+swg_status swg_inject_stall(swg_inject_kernel kernel, int64_t entry, int64_t wait_limit_cycles) {
+  if (kernel == SWG_INJECT_NONE) {
+    swg::arm_injection(0, -1, 0);
+    return SWG_OK;
+  }
+  if (kernel != SWG_INJECT_X_GEMM && kernel != SWG_INJECT_FUSED_X) return SWG_ERR_PARAM_INVALID;
+  if (entry < 0 || wait_limit_cycles < 1024) return SWG_ERR_PARAM_INVALID;
+  swg::arm_injection(static_cast<int>(kernel), entry, static_cast<long long>(wait_limit_cycles));
+  return SWG_OK;
+}
+
 swg_status swg_check(swg_stream_t stream) {
   uint32_t v = 0;
   cudaError_t e = swg::read_and_clear_status(&v, reinterpret_cast<cudaStream_t>(stream));

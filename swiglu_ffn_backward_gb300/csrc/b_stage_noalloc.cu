@@ -17,12 +17,12 @@
 // them.
 //
 // Host code must not pass the array's name to a kernel: on the host it is a
-// stand-in, not a device address. The device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, by the first
-// call on that device; make that first call before any stream capture.
+// stand-in, not a device address. Every call looks the device address up with
+// cudaGetSymbolAddress on the current device (the device the call launches
+// on), so the address is never stale, not even after a cudaDeviceReset. The
+// first call on a device also loads the library's device code there; make
+// that first call before any stream capture.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/swiglu_bwd.h"
 #include "swg_launch.h"
@@ -30,25 +30,14 @@
 namespace {
 
 constexpr size_t kScratchBytes = SWG_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_b_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// device address of g_b_scratch on the current device (looked up once per device)
+// device address of g_b_scratch on the current device, looked up on every call
 swg_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SWG_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_b_scratch) != cudaSuccess || p == nullptr) return SWG_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_b_scratch) != cudaSuccess || p == nullptr) return SWG_ERR_CUDA;
+  *out = p;
   return SWG_OK;
 }
 

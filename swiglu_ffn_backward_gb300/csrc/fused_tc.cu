@@ -117,6 +117,8 @@ struct FusedArgs {
   int cluster_tiles;  // work items of CS CTAs; cluster c takes c, c + nclusters, ...
   int accumulate;     // FW: dw, db += this call's sums (one rounding of old + new)
   int mtiles;         // FX: 128-row tiles of M
+  long long wait_limit;  // cycles before a pipeline wait gives up
+  int64_t stall_at;      // test injection: the producer stops before this ring entry (-1: never)
 };
 
 // One CTA's share of one cluster tile.
@@ -258,12 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ operand producer
     if (lane == 0) {
       uint32_t gj = 0;  // ring entries issued, over all tiles
-      for (int ct = cluster; ct < args.cluster_tiles && !s.abort_flag; ct += nclusters) {
+      bool stopped = false;  // test injection: nothing more is issued
+      for (int ct = cluster; ct < args.cluster_tiles && !s.abort_flag && !stopped; ct += nclusters) {
         const Tile tl = tile_of<MODE, CS>(ct, crank, args);
         const int total = tl.nst * tl.eps;
         for (int j = 0; j < total && !s.abort_flag; ++j, ++gj) {
+          if (static_cast<int64_t>(gj) == args.stall_at) {
+            stopped = true;
+            break;
+          }
           const int e = gj % kRE;
-          if (gj >= kRE && !mbar_wait(&s.ring_empty[e], ((gj / kRE) - 1) & 1)) {
+          if (gj >= kRE && !mbar_wait(&s.ring_empty[e], ((gj / kRE) - 1) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
             break;
           }
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the peers' last releases arrive on this CTA's barriers: see them land
         // before this CTA can leave
         for (uint32_t j = gj > static_cast<uint32_t>(kRE) ? gj - kRE : 0u; j < gj; ++j)
-          if (!mbar_wait(&s.ring_empty[j % kRE], (j / kRE) & 1)) {
+          if (!mbar_wait(&s.ring_empty[j % kRE], (j / kRE) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
             break;
           }
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_of<MODE, CS>(ct, crank, args);
         if (tt > 0) {
           // the previous tile's epilogue must have read the accumulator out
-          if (!mbar_wait(&s.tmem_free, (tt - 1) & 1)) {
+          if (!mbar_wait(&s.tmem_free, (tt - 1) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
             break;
           }
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < tl.nst && ok; ++i, ++gi) {
           const int a = gi % kAS;
-          if (!mbar_wait(&s.a_full[a], (gi / kAS) & 1)) {
+          if (!mbar_wait(&s.a_full[a], (gi / kAS) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
             ok = false;
             break;
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_slot = smem_u32(s.aop[a]);
           for (int q = 0; q < tl.eps; ++q, ++gj) {
             const int e = gj % kRE;
-            if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1)) {
+            if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
               flag_timeout(s, args.status);
               ok = false;
               break;
@@ -370,6 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&s.accum);  // this tile's accumulator is complete
       }
+      // after a timeout the epilogue may have stopped waiting: see every MMA this thread
+      // issued complete before the CTA frees TMEM (tt accumulator phases were committed)
+      if (s.abort_flag && tt > 0) mbar_wait(&s.accum, (tt - 1) & 1, args.wait_limit);
     }
   } else {
     // ------------------------------------------------------------ transform
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // waits for A slot a to be released by the MMAs of stage st - kAS
     auto acquire_slot = [&](uint32_t st, int a) {
-      if (!dead && st >= kAS && !mbar_wait(&s.a_empty[a], ((st / kAS) - 1) & 1)) {
+      if (!dead && st >= kAS && !mbar_wait(&s.a_empty[a], ((st / kAS) - 1) & 1, args.wait_limit)) {
         flag_timeout(s, args.status);
         dead = true;
       }
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(tix);
         bool acc_ok = false;
         if (!dead && !s.abort_flag) {
-          acc_ok = mbar_wait(&s.accum, tix & 1);
+          acc_ok = mbar_wait(&s.accum, tix & 1, args.wait_limit);
           if (!acc_ok) flag_timeout(s, args.status);
         }
         const int q = warp & 3;         // TMEM lane quarter this warp may read
@@ -581,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gi += nst;
         bool acc_ok = false;
         if (!dead && !s.abort_flag) {
-          acc_ok = mbar_wait(&s.accum, tt & 1);
+          acc_ok = mbar_wait(&s.accum, tt & 1, args.wait_limit);
           if (!acc_ok) flag_timeout(s, args.status);
         }
         if (want_db) {
@@ -670,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && s.abort_flag) {
     // drain: ring copies issued but never waited on must land before the CTA exits
     for (uint32_t i = s.ring_consumed; i < s.ring_issued; ++i)
-      if (!mbar_wait(&s.ring_full[i % kRE], (i / kRE) & 1)) break;
+      if (!mbar_wait(&s.ring_full[i % kRE], (i / kRE) & 1, args.wait_limit)) break;
   }
   __syncthreads();
   if (warp == 1) {
@@ -763,6 +773,9 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
   a.dx = dx;
   a.dg_out = dg;
   a.dfc_out = dfc;
+  const Injection inj = take_injection(2);
+  a.wait_limit = inj.wait_limit;
+  a.stall_at = inj.stall_at;
   const int64_t mclusters = ((M + 127) / 128 + CS - 1) / CS;  // tail CTAs run on zero-filled rows
   return launch<kFX, CS>(static_cast<unsigned>(mclusters * CS * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, mdx, a,
                          true);
@@ -811,6 +824,8 @@ cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16
   a.tiles_n = static_cast<int>(((N + 63) / 64 + CS - 1) / CS * CS);  // clusters of CS n tiles
   a.x3d = x3d;
   a.accumulate = accumulate ? 1 : 0;
+  a.wait_limit = kWaitLimitCycles;
+  a.stall_at = -1;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
   return launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
 }

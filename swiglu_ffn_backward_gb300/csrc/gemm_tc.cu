@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded; on timeout the kernel ORs a flag into the
 // module status word, stops issuing, waits (bounded) for its own TMA copies
 // and MMAs still in flight, frees TMEM and returns.
+#include <atomic>
 #include <mutex>
 
 #include "swg_device.cuh"
@@ -78,6 +79,8 @@ struct GemmArgs {
   int splits, kb_per, nkb_total;
   int tiles_kw, tiles_nw;  // dw tile grid per problem
   int accumulate;          // dw += this call's sums (one rounding of old + new)
+  long long wait_limit;    // cycles before a pipeline wait gives up
+  int stall_at;            // test injection: the producer stops before this k block (-1: never)
 };
 
 __device__ __forceinline__ void flag_timeout(Smem& s) {
@@ -148,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nkb; ++i) {
       const int st = i % STAGES;
       const int use = i / STAGES;
-      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1)) {
+      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, args.wait_limit)) {
         flag_timeout(s);
         break;
       }
-      if (s.abort_flag) break;
+      if (s.abort_flag || i == args.stall_at) break;
       mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
       const int kb = kb_begin + i;
       if (MODE == kModeX) {
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, MODE == kModeW, MODE == kModeW);
     for (int i = 0; i < nkb; ++i) {
       const int st = i % STAGES;
-      if (!mbar_wait(&s.full[st], (i / STAGES) & 1)) {
+      if (!mbar_wait(&s.full[st], (i / STAGES) & 1, args.wait_limit)) {
         flag_timeout(s);
         break;
       }
@@ -199,10 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&s.empty[st]);
     }
     umma_commit(&s.accum);
+    // after a timeout the epilogue may have stopped waiting: see every MMA this thread
+    // issued complete before the CTA frees TMEM
+    if (s.abort_flag) mbar_wait(&s.accum, 0, args.wait_limit);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const bool ok = mbar_wait(&s.accum, 0);
+    const bool ok = mbar_wait(&s.accum, 0, args.wait_limit);
     if (!ok) flag_timeout(s);
     tc_fence_after();
     const int r = q * 32 + lane;  // accumulator row
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && s.abort_flag) {
     // drain: TMA copies issued but never consumed must land before the CTA exits
     for (uint32_t i = s.consumed; i < s.issued; ++i) {
-      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1, args.wait_limit)) break;
     }
   }
   __syncthreads();
@@ -401,6 +407,9 @@ cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_
   a.dx = dx;
   a.tiles_k = static_cast<int>((K + BN - 1) / BN);
   a.nkb_half = static_cast<int>((N + BK - 1) / BK);
+  const Injection inj = take_injection(1);
+  a.wait_limit = inj.wait_limit;
+  a.stall_at = static_cast<int>(inj.stall_at);
   const int64_t tiles = ((M + BM - 1) / BM) * a.tiles_k;
   cudaError_t e = prepare_kernel<kModeX>();
   if (e != cudaSuccess) return e;
@@ -429,6 +438,8 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
   a.tiles_kw = static_cast<int>((K + BM - 1) / BM);
   a.tiles_nw = static_cast<int>((N + BN - 1) / BN);
   a.accumulate = accumulate ? 1 : 0;
+  a.wait_limit = kWaitLimitCycles;
+  a.stall_at = -1;
   const int64_t ctas = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
   cudaError_t e = prepare_kernel<kModeW>();
   if (e != cudaSuccess) return e;
@@ -447,6 +458,25 @@ cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, in
       reinterpret_cast<const float4*>(ws), static_cast<int>(splits), per_prob4, reinterpret_cast<uint2*>(dw_g),
       reinterpret_cast<uint2*>(dw_fc), accumulate ? 1 : 0);
   return cudaGetLastError();
+}
+
+namespace {
+std::atomic<int> g_inject_kernel{0};
+std::atomic<int64_t> g_inject_stall{-1};
+std::atomic<long long> g_inject_limit{kWaitLimitCycles};
+}  // namespace
+
+void arm_injection(int kernel, int64_t stall_at, long long wait_limit) {
+  g_inject_stall.store(stall_at);
+  g_inject_limit.store(wait_limit);
+  g_inject_kernel.store(kernel);
+}
+
+Injection take_injection(int kernel) {
+  int expected = kernel;
+  if (kernel != 0 && g_inject_kernel.compare_exchange_strong(expected, 0))
+    return Injection{g_inject_stall.load(), g_inject_limit.load()};
+  return Injection{-1, kWaitLimitCycles};
 }
 
 uint32_t* status_word_ptr() {

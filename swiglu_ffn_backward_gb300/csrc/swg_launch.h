@@ -71,6 +71,18 @@ cudaError_t launch_group_norm_bwd(const void* dy, const void* x, const void* gam
                                   void* dbeta, int64_t N, int64_t C, int64_t HxW, int64_t G, float eps, int dtype,
                                   void* ws, cudaStream_t stream);
 
+// one-shot fault injection for tests of the timeout path (swg_inject_stall): the next
+// launch of `kernel` (1 = x GEMM, 2 = fused x) stops issuing operand copies at ring
+// entry `stall_at` and gives every pipeline wait `wait_limit` cycles. take_injection
+// returns the values for that launch (stall_at -1 and the normal limit when none is armed)
+// and disarms it.
+struct Injection {
+  int64_t stall_at;
+  long long wait_limit;
+};
+void arm_injection(int kernel, int64_t stall_at, long long wait_limit);
+Injection take_injection(int kernel);
+
 // module status word (timeouts)
 cudaError_t read_and_clear_status(uint32_t* out, cudaStream_t stream);
 // device address of the status word on the current device (for kernels in other files)

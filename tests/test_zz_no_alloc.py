@@ -38,3 +38,25 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert_all([compare(n, gt, to_f64(rf)) for n, gt, rf in zip(names, got, ref)])
         for gt, rf in zip(got, ref):  # same kernel, same plan: the same bits
             assert torch.equal(gt, rf)
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_array_limit_and_empty():
+    """N = 524288 fills the array exactly (one partial row pair of 8N bytes);
+    M = 0 writes zero column sums. Both against swiglu_bwd_b, twice in a row."""
+    import swiglu_ffn_backward_gb300 as swg
+    from synth import SwigluShape
+    shape = SwigluShape("noalloc_limit", 8, 8, 524288, 3, "tail")
+    inp = swiglu_inputs(shape, device="cuda")
+    for _ in range(2):
+        ref = swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"])
+        got = swg.swiglu_bwd_b_noalloc(inp["dy"], inp["g"], inp["fc"])
+        swg.swg_check()
+        for gt, rf in zip(got, ref):
+            assert torch.equal(gt, rf)
+    z = torch.empty((0, 1024), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        dg, dfc, db_g, db_fc = swg.swiglu_bwd_b_noalloc(z, z, z)
+        swg.swg_check()
+        assert dg.numel() == 0 and dfc.numel() == 0
+        assert torch.count_nonzero(db_g).item() == 0 and torch.count_nonzero(db_fc).item() == 0
