@@ -9,6 +9,10 @@ Because those absolute tolerances can exceed the outputs' own magnitude at
 small scales (an all-zero output would pass at the pages' shape), every
 comparison also applies a scale-aware check:
   max|gpu - ref| <= 2^-6 * max|ref|   and   ||gpu - ref||_2 <= 2^-8 * ||ref||_2.
+The relative-L2 part applies to tensors of at least L2_MIN_N elements: on a
+handful of elements a single bf16 rounding that falls on the other side of a
+tie from the oracle's (one ulp, up to 2^-7 of the value, which the
+element-wise contract allows) can by itself exceed 2^-8 of the norm.
 """
 
 from __future__ import annotations
@@ -22,6 +26,7 @@ ATOL_ELEM = 1e-4
 ATOL_RED = 1e-3
 MAX_REL = 2.0 ** -6
 L2_REL = 2.0 ** -8
+L2_MIN_N = 64
 
 ATOL = dict(dg=ATOL_ELEM, dfc=ATOL_ELEM, grad_x=ATOL_ELEM,
             db_g=ATOL_RED, db_fc=ATOL_RED, dw_g=ATOL_RED, dw_fc=ATOL_RED, dx=ATOL_RED,
@@ -54,7 +59,7 @@ def compare(name: str, got, ref, dtype: str = "bf16", atol: float | None = None,
     el2 = float(np.linalg.norm(err)) if finite else float("inf")
     ok = finite and bad == 0
     if scale_aware and rmax > 0:
-        ok = ok and emax <= MAX_REL * rmax and el2 <= L2_REL * rl2
+        ok = ok and emax <= MAX_REL * rmax and (r.size < L2_MIN_N or el2 <= L2_REL * rl2)
     rep.update(ok=ok, finite=finite, bad=bad, max_err=emax, max_ref=rmax,
                rel_l2=(el2 / rl2 if rl2 > 0 else 0.0))
     return rep
