@@ -89,6 +89,13 @@ typedef enum { SWG_ACT_SILU = 0, SWG_ACT_GELU = 1, SWG_ACT_HARDSWISH = 2 } swg_a
  * Without the flag every output is overwritten (the same result as the pages'
  * zero-then-accumulate on zeroed outputs). */
 #define SWG_ACCUMULATE 2u
+/* The library chooses the chain (replaces SWG_FUSED / SWG_UNFUSED): fused when
+ * K <= 512 and M >= 32768, unfused otherwise -- the faster one in measurements
+ * on GB300 (fused: 0.80 vs 1.07 ms at M=220000 K=512 N=1024 and faster from
+ * M = 65537 on at K=512; unfused: faster at M <= 4097, and 5.48 vs 6.85 ms at
+ * the LLM FFN shape M=16384 K=4096 N=14336, where the fused kernels would form
+ * dg, dfc eight times each). The workspace query resolves it the same way. */
+#define SWG_AUTO 4u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* swg_status_string(swg_status s);
@@ -216,7 +223,7 @@ swg_status swiglu_fwd(const void* x, const void* w_g, const void* w_fc,
 
 /* ---- whole backward ----------------------------------------------------------
  * [P1] "Kernel overview and call chain": b, then w and x on b's dg, dfc.
- * flags: SWG_UNFUSED or SWG_FUSED, optionally | SWG_ACCUMULATE.
+ * flags: SWG_UNFUSED, SWG_FUSED or SWG_AUTO, optionally | SWG_ACCUMULATE.
  * dg, dfc are optional outputs: pass NULL to skip them. With SWG_UNFUSED and
  * NULL dg/dfc, the workspace holds them (4*M*N bytes more). With SWG_FUSED the
  * call runs swiglu_bwd_x_fused then swiglu_bwd_w_fused: the w and x GEMMs

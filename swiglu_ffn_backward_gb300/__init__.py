@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     group_norm_bwd_workspace_size,
     LIB_PATH,
     SWG_ACCUMULATE,
+    SWG_AUTO,
     SWG_FUSED,
     SWG_UNFUSED,
     SwgError,

@@ -33,6 +33,7 @@ _DTYPE = {torch.float32: SWG_F32, torch.float16: SWG_F16, torch.bfloat16: SWG_BF
 SWG_UNFUSED = 0
 SWG_FUSED = 1
 SWG_ACCUMULATE = 2
+SWG_AUTO = 4
 SWG_WS_DG_GIVEN = 0x100
 
 EXPORTS = (
@@ -344,10 +345,12 @@ def swiglu_fwd(x, w_g, w_fc, b_g=None, b_fc=None, out: dict | None = None, strea
     return out
 
 
-def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = True,
+def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool | None = None, return_dg: bool = True,
                out: dict | None = None, workspace=None, stream=None, accumulate: bool = False) -> dict:
     """The whole backward. Returns a dict with dx, dw_g, dw_fc, db_g, db_fc
     (and dg, dfc when return_dg). `out` may supply any of those tensors.
+    fused: True (SWG_FUSED), False (SWG_UNFUSED) or None (SWG_AUTO: the library
+    picks the chain measured faster for the shape).
     accumulate=True adds this call's db and dw into out's db_g, db_fc, dw_g,
     dw_fc (which must then be given) instead of overwriting them."""
     x, w_g, w_fc, dy, g, fc = (_dev_bf16(t, n) for t, n in (
@@ -366,7 +369,7 @@ def swiglu_bwd(x, w_g, w_fc, dy, g, fc, fused: bool = False, return_dg: bool = T
         shapes.update(dg=(M, N), dfc=(M, N))
     for k, shp in shapes.items():
         out[k] = _out(out.get(k), shp, torch.bfloat16, x.device, k)
-    flags = (SWG_FUSED if fused else SWG_UNFUSED) | (SWG_ACCUMULATE if accumulate else 0)
+    flags = (SWG_AUTO if fused is None else SWG_FUSED if fused else SWG_UNFUSED) | (SWG_ACCUMULATE if accumulate else 0)
     ws_flags = flags | (SWG_WS_DG_GIVEN if return_dg else 0)
     dev = _device_of(x, w_g, w_fc, dy, g, fc, workspace, *out.values())
     ws = _workspace(_call(dev, lib.swiglu_bwd_workspace_size, M, K, N, ws_flags), x.device, workspace)

@@ -593,8 +593,24 @@ swg_status swiglu_bwd_host(const void* x, const void* w_g, const void* w_fc, con
 // Unfused workspace layout: [dg scratch 2MN | dfc scratch 2MN] (only when the
 // caller passes NULL dg/dfc) | b-stage partials | w-stage partials; each
 // region starts on a 256-byte boundary.
+// SWG_AUTO: the chain measured faster for the shape on GB300. The fused chain
+// forms dg, dfc once per 512 columns of K in each of its two kernels, the
+// unfused one once in the b stage but writes and re-reads them through HBM.
+// Measured (whole backward, N = 1024 unless stated): K = 512, M = 220000:
+// fused 0.80 ms, unfused 1.07 ms; K = 512, M = 65537: 0.285 vs 0.346 ms;
+// K = 512, M <= 4097: fused slower (fixed costs of its two persistent
+// launches); K = 4096, N = 14336, M = 16384: fused 6.85 ms, unfused 5.48 ms.
+bool auto_fused(int64_t M, int64_t K) { return K <= 512 && M >= 32768; }
+
+unsigned resolve_auto(int64_t M, int64_t K, unsigned flags) {
+  if (!(flags & SWG_AUTO)) return flags;
+  flags &= ~(SWG_AUTO | SWG_FUSED);
+  return auto_fused(M, K) ? (flags | SWG_FUSED) : flags;
+}
+
 size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags) {
   if (M <= 0 || K <= 0 || N <= 0) return 0;
+  flags = resolve_auto(M, K, flags);
   const bool fused = (flags & SWG_FUSED) != 0;
   if (fused) return swg::fw_plan(M, K, N, swg::device_sm_count()).ws_bytes;
   size_t total = 0;
@@ -608,7 +624,8 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
                       const void* fc, void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc, void* db_g,
                       void* db_fc, int64_t M, int64_t K, int64_t N, unsigned flags, void* workspace,
                       size_t workspace_bytes, swg_stream_t stream) {
-  if ((flags & ~(SWG_FUSED | SWG_ACCUMULATE | SWG_WS_DG_GIVEN)) != 0) return SWG_ERR_PARAM_INVALID;
+  if ((flags & ~(SWG_FUSED | SWG_ACCUMULATE | SWG_WS_DG_GIVEN | SWG_AUTO)) != 0) return SWG_ERR_PARAM_INVALID;
+  flags = resolve_auto(M, K, flags);
   const bool acc = (flags & SWG_ACCUMULATE) != 0;
   swg_status st = check_shape(M, K, N);
   if (st != SWG_OK) return st;

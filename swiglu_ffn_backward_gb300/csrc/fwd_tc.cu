@@ -12,8 +12,10 @@
 //                   4-deep ring, running across the CTA's tiles
 //   warp 1          TMEM allocation (512 columns = two accumulator buffers,
 //                   each g [128 x 128] | fc [128 x 128]); lane 0 issues
-//                   tcgen05.mma (M=128, N=128, K=16): each x step feeds both
-//                   products
+//                   tcgen05.mma (M=128, N=256, K=16): the W_g and W_fc tiles
+//                   sit in four consecutive 64-column MN-major chunks, so one
+//                   instruction per K step computes both products from one
+//                   read of the x tile
 //   warps 2-5       epilogue: drain the finished buffer while the tensor core
 //                   fills the other one: bias, SiLU, and per 32x32 block one
 //                   TMA store per output from a 64-byte-swizzled staging
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);  // A K-major, B MN-major
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, 2 * BN, 0, 1);  // A K-major, B = [W_g | W_fc] MN-major
       uint32_t gj = 0, it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++it) {
@@ -164,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-            const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024);
-            umma_bf16(d, ad, smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, acc);
-            umma_bf16(d + BN, ad, smem_desc(b_addr + 16384 + 2048 * k, 8192, 1024), idesc, acc);
+            // D[:, 0:128] = x W_g, D[:, 128:256] = x W_fc
+            umma_bf16(d, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024), idesc,
+                      acc);
           }
           umma_commit(&s.empty[st]);
         }

@@ -287,3 +287,16 @@ def test_host_path_binding_checks_buffers(swg):
         swg.swiglu_bwd_host(**dict(ins, dy=torch.zeros(M + 1, N, **bf)))
     with pytest.raises(TypeError):   # fp32 inputs
         swg.swiglu_bwd_host(**dict(ins, x=torch.zeros(M, K)))
+
+
+def test_auto_flag_resolves_like_the_measured_choice(swg):
+    """SWG_AUTO takes the fused chain for K <= 512 and M >= 32768, else the unfused one;
+    the workspace query resolves it the same way."""
+    from swiglu_ffn_backward_gb300 import _binding as b
+    q = b.lib.swiglu_bwd_workspace_size
+    for M, K, N, fused in ((220000, 512, 1024, True), (65537, 512, 1024, True), (4097, 512, 1024, False),
+                           (16384, 4096, 14336, False), (32767, 512, 1024, False)):
+        want = q(M, K, N, b.SWG_FUSED if fused else b.SWG_UNFUSED)
+        assert q(M, K, N, b.SWG_AUTO) == want, (M, K, N)
+        assert q(M, K, N, b.SWG_AUTO | b.SWG_ACCUMULATE) == q(M, K, N, (b.SWG_FUSED if fused else 0)
+                                                                | b.SWG_ACCUMULATE)

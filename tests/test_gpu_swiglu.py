@@ -228,3 +228,16 @@ def test_deterministic(fused):
     torch.cuda.synchronize()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("shape", [SWIGLU_CONFIGS["tail"][3], SWIGLU_CONFIGS["tail"][4]], ids=lambda s: s.name)
+def test_auto_chain_is_the_chosen_chain(shape):
+    """fused=None (SWG_AUTO) gives exactly the bits of the chain it selects: unfused at
+    M = 4097, fused at M = 65537 (K = 512)."""
+    swg = _swg()
+    inp = swiglu_inputs(shape, device="cuda")
+    a = swg.swiglu_bwd(**inp)
+    b = swg.swiglu_bwd(**inp, fused=shape.M >= 32768)
+    swg.swg_check()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
