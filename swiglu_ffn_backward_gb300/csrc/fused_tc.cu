@@ -7,58 +7,60 @@
 // recompute-instead-of-store principle stated in the Ascend C backward blog
 // post (Swish section: recompute sigma in the backward rather than keep it).
 //
-// Two kernels, both one CTA per SM with ten warps:
-//   warp 0 lane 0   TMA producer of the operand ring (W chunks, or x chunks)
-//   warp 1          TMEM allocation (512 columns); lane 0 issues tcgen05.mma
-//   warps 2-9       transform: load dy, g, fc straight from global memory into
-//                   registers (16-byte coalesced loads, one stage ahead of the
-//                   math, with an L2 prefetch of the tile a few stages further
-//                   ahead), compute dg, dfc in fp32 and store them as bf16 into
-//                   a ring of A-operand slots in the 128-byte-swizzled layout
-//                   the tensor cores read; then the epilogue, two warps per
-//                   32-lane TMEM quarter, one per 256-column accumulator half.
-//   The raw inputs never pass through shared memory: only the operand does.
+// Twelve warps per CTA, one CTA per SM, launched as a persistent wave (FX) or
+// one CTA per tile (FW):
+//   warp 0 lane 0   TMA producer of the operand ring (W chunks for FX, x chunks
+//                   for FW; 128-byte swizzle)
+//   warp 1          tensor-memory allocation (512 columns); lane 0 issues
+//                   tcgen05.mma (M = 128, N = 256, K = 16) and tcgen05.commit
+//   warp 2 lane 0   L2 prefetch of the raw dy, g, fc tiles a few stages ahead
+//                   of the transform, paced by the transform's progress count
+//   warp 3          idle
+//   warps 4-11      transform: load dy, g, fc straight from global memory into
+//                   registers (FX: three stages of registers, the loads running
+//                   two stages ahead of the math; FW: two), compute dg, dfc in
+//                   fp32 and store them as bf16 into a ring of A-operand slots
+//                   in the 128-byte-swizzled layout the tensor core reads; then
+//                   the epilogue.
+// Warpgroup 0 (warps 0-3) gives registers to the two transform warpgroups
+// (setmaxnreg): 48 per thread there, 224 in the transform (a block of twelve
+// warps is otherwise held to 168 per thread, and the FX transform wants more).
 //
-// fused x (FX): D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulators.
-//   Stages of 64 reduction columns. A = dg or dfc [128 m x 64 n] (K-major),
-//   B = W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries). Each dg element
-//   is computed once per 512 columns of dx (once when K <= 512); dg, dfc can
-//   also be written to HBM as optional outputs. Persistent: each CTA loops
-//   over its tiles, and a tile's epilogue waits until the next tile's first
-//   stages are in their A slots, so the tensor core restarts right after it.
+// fused x (FX): D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulator
+//   halves. Stages of 64 reduction columns n. A = dg or dfc [128 m x 64 n]
+//   (K-major), B = W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries).
+//   Persistent over m tiles: a tile's epilogue runs once the next tile's first
+//   stages are in their A slots, and it drains the low accumulator half first
+//   and releases it, so the next tile's first stages run their low-half MMAs
+//   while the high half is still being drained (their high-half MMAs follow).
 // fused w (FW): D = [dw_g^T ; dw_fc^T][n0:n0+64, k0:k0+512]: the A operand
 //   stacks 64 columns of dg over the same 64 columns of dfc (MN-major; the two
 //   8 KB halves of a slot are the two 64-element MN chunks, LBO = 8 KB), so one
 //   accumulator pair holds both outputs for all k. Stages of 64 rows of m;
-//   B = x [64 m x 256 k] (MN-major). The CTA owns a fixed band of 64 columns
-//   for its whole M range, so it also sums dg, dfc over its rows in registers
-//   (db column partials, one row per M split). The reduction over M is split
-//   into S chunks with fp32 partials and a fixed-order reduce.
-//
-// Operand sharing: the copy engine serves a bounded number of 128-byte rows
-// per clock per SM, and the operand ring (W in FX, x in FW) is the same for
-// several CTAs. CTAs are launched in clusters of CS that share it: CTAs of CS
-// consecutive m tiles (FX) or n tiles (FW). Each CTA loads 1/CS of every ring
-// entry with a cluster-multicast TMA copy that lands in all CS CTAs; an entry
-// is released only when all CS CTAs' MMAs are done with it (the release is a
-// multicast tcgen05.commit onto a barrier counting CS arrivals).
+//   B = x [64 m x 256 k] (MN-major, four 64 x 64 boxes). The CTA owns a fixed
+//   band of 64 columns for its whole M range, so it also sums dg, dfc over its
+//   rows in registers (db column partials, one row per M split). The reduction
+//   over M is split into S chunks with fp32 partials and a fixed-order reduce.
 //
 // Every mbarrier wait is bounded; a timeout sets the module status word,
-// stops issuing, drains the CTA's own TMA copies and MMAs, frees TMEM and
-// returns.
+// stops issuing, waits (bounded) for the work already issued, frees tensor
+// memory and returns.
 #include "swg_device.cuh"
 #include "swg_launch.h"
 
 namespace swg {
+
 namespace {
 
 enum FusedMode : int { kFX = 0, kFW = 1 };
 
-constexpr int kThreads = 320;
-constexpr int kXThreads = 256;  // transform / epilogue threads (warps 2-9)
-constexpr int kClusterX = 4;    // CTAs sharing each W chunk in the fused x kernel (measured: 3% over 2)
-constexpr int kClusterW = 4;    // CTAs sharing each x chunk in the fused w kernel
+constexpr int kThreads = 384;
+constexpr int kXWarp0 = 4;      // first transform warp
+constexpr int kXWarps = 8;
+constexpr int kCtlRegs = 48;    // registers per thread in warpgroup 0 after setmaxnreg
+constexpr int kXRegs = 224;     // registers per thread in the transform warpgroups
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSplitStages = 2;  // FX: stages whose low-half MMAs run before the high half is free
 
 template <int MODE>
 struct Cfg;
@@ -66,7 +68,7 @@ template <>
 struct Cfg<kFX> {
   static constexpr int kRows = 128;        // m rows of a stage's tile (64 columns of n)
   static constexpr int kAStages = 3;       // A-operand slots (dg + dfc, 2 x 16 KB each)
-  static constexpr int kEntryBytes = 32768;
+  static constexpr int kEntryBytes = 32768;  // W_g or W_fc [256 k x 64 n]
   static constexpr int kEntries = 4;
   static constexpr int kPrefetch = 8;      // stages prefetched into L2 ahead of the loads
 };
@@ -74,7 +76,7 @@ template <>
 struct Cfg<kFW> {
   static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
   static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
-  static constexpr int kEntryBytes = 32768;
+  static constexpr int kEntryBytes = 32768;  // x [64 m x 256 k]
   static constexpr int kEntries = 5;
   static constexpr int kPrefetch = 4;
 };
@@ -85,15 +87,17 @@ struct __align__(1024) FSmem {
   static constexpr int kHalf = C::kRows * 128;  // one 64-column bf16 tile (dg or dfc)
   uint8_t ring[C::kEntries][C::kEntryBytes];
   uint8_t aop[C::kAStages][2 * kHalf];          // [dg | dfc]
-  uint64_t a_full[C::kAStages];
-  uint64_t a_empty[C::kAStages];
-  uint64_t ring_full[C::kEntries];
-  uint64_t ring_empty[C::kEntries];
-  uint64_t accum;      // one phase per tile: the tile's MMAs are done
-  uint64_t tmem_free;  // one phase per tile: the epilogue has read the accumulator
+  uint64_t a_full[C::kAStages];      // the transform warps have written the slot
+  uint64_t a_empty[C::kAStages];     // the MMAs reading the slot are done
+  uint64_t ring_full[C::kEntries];   // the entry's copies have landed
+  uint64_t ring_empty[C::kEntries];  // the MMAs reading the entry are done
+  uint64_t accum;                    // one phase per tile: the tile's MMAs are done
+  uint64_t tmem_free[2];             // one phase per tile per accumulator half: the epilogue
+                                     // warps have read it
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   volatile uint32_t ring_issued, ring_consumed;
+  volatile uint32_t x_progress;      // stages the transform has produced (paces the prefetch warp)
 };
 
 struct FusedArgs {
@@ -113,32 +117,30 @@ struct FusedArgs {
   float* ws;       // [splits][2][K][N] dw partials (splits > 1)
   float* db_part;  // [splits][2N]
   int splits, kb_per, nkb_total, tiles_n;
-  int x3d;  // x entries come from one 3-D box (else 2-D boxes)
-  int cluster_tiles;  // work items of CS CTAs; cluster c takes c, c + nclusters, ...
+  int ntiles;         // work tiles; CTA c takes c, c + gridDim.x, ...
   int accumulate;     // FW: dw, db += this call's sums (one rounding of old + new)
-  int mtiles;         // FX: 128-row tiles of M
   long long wait_limit;  // cycles before a pipeline wait gives up
   int64_t stall_at;      // test injection: the producer stops before this ring entry (-1: never)
 };
 
-// One CTA's share of one cluster tile.
+// One CTA's work tile.
 struct Tile {
   int m0, n0, k0, kt, split, nst, kb_begin, nh, eps;
 };
 
-template <int MODE, int CS>
-__device__ __forceinline__ Tile tile_of(int ct, uint32_t crank, const FusedArgs& args) {
+template <int MODE>
+__device__ __forceinline__ Tile tile_of(int ct, const FusedArgs& args) {
   Tile t;
   t.m0 = t.n0 = t.split = t.kb_begin = 0;
   if (MODE == kFX) {
-    // cluster tile = CS consecutive m tiles at one 512-column block of K
+    // a 128-row m tile at one 512-column block of K
     t.kt = ct % args.tiles_k;
-    t.m0 = ((ct / args.tiles_k) * CS + static_cast<int>(crank)) * 128;
+    t.m0 = (ct / args.tiles_k) * 128;
     t.nst = (args.N + 63) / 64;  // stages: 64 columns of n each
   } else {
-    // cluster tile = CS consecutive 64-column bands of n, one K block, one M split
-    const int bands = args.tiles_n / CS;
-    t.n0 = ((ct % bands) * CS + static_cast<int>(crank)) * 64;
+    // a 64-column band of n, one K block, one M split
+    const int bands = args.tiles_n;
+    t.n0 = (ct % bands) * 64;
     const int rest = ct / bands;
     t.kt = rest % args.tiles_k;
     t.split = rest / args.tiles_k;
@@ -149,6 +151,33 @@ __device__ __forceinline__ Tile tile_of(int ct, uint32_t crank, const FusedArgs&
   t.nh = (args.K - t.k0) > 256 ? 2 : 1;             // 256-column accumulator halves in use
   t.eps = (MODE == kFX) ? 2 * t.nh : t.nh;          // ring entries per stage
   return t;
+}
+
+// FX entry order within a tile: the first J stages issue their low-half (h = 0)
+// entries first, then their high-half entries, so that their low-half MMAs can
+// run while the previous tile's high accumulator half is still being drained.
+struct EntryPos {
+  int i, p, h;
+};
+__device__ __forceinline__ EntryPos fx_entry(const Tile& tl, int j) {
+  const int J = tl.nh == 2 ? min(kSplitStages, tl.nst) : 0;
+  EntryPos r;
+  if (j < 2 * J) {
+    r.i = j >> 1;
+    r.p = j & 1;
+    r.h = 0;
+  } else if (j < 4 * J) {
+    r.i = (j - 2 * J) >> 1;
+    r.p = j & 1;
+    r.h = 1;
+  } else {
+    const int jj = j - 4 * J;
+    r.i = J + jj / tl.eps;
+    const int q = jj % tl.eps;
+    r.p = q / tl.nh;
+    r.h = q % tl.nh;
+  }
+  return r;
 }
 
 template <int MODE>
@@ -203,7 +232,7 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* v) {
                     pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
 }
 
-template <int MODE, int CS>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_g,
                  const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_b0,
@@ -221,24 +250,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const uint32_t crank = CS > 1 ? cluster_ctarank() : 0u;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CS) - 1u);
-  const int cluster = blockIdx.x / CS;
-  const int nclusters = gridDim.x / CS;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAS; ++i) {
-      mbar_init(&s.a_full[i], kXThreads);
+      mbar_init(&s.a_full[i], kXWarps);  // one arrival per transform warp
       mbar_init(&s.a_empty[i], 1);
     }
     for (int i = 0; i < kRE; ++i) {
       mbar_init(&s.ring_full[i], 1);
-      mbar_init(&s.ring_empty[i], CS);  // released by all CTAs of the cluster
+      mbar_init(&s.ring_empty[i], 1);
     }
     mbar_init(&s.accum, 1);
-    mbar_init(&s.tmem_free, kXThreads);
+    mbar_init(&s.tmem_free[0], kXWarps);
+    mbar_init(&s.tmem_free[1], kXWarps);
     s.abort_flag = 0u;
     s.ring_issued = s.ring_consumed = 0u;
+    s.x_progress = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_dy);
     tma_prefetch_desc(&tm_g);
@@ -253,70 +279,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CS > 1) cluster_sync();  // every peer's barriers are initialised before any multicast
   const uint32_t tmem = s.tmem_base;
+
+  if (warp < kXWarp0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs) : "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer
     if (lane == 0) {
       uint32_t gj = 0;  // ring entries issued, over all tiles
-      bool stopped = false;  // test injection: nothing more is issued
-      for (int ct = cluster; ct < args.cluster_tiles && !s.abort_flag && !stopped; ct += nclusters) {
-        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+      bool stop = false;
+      for (int ct = blockIdx.x; ct < args.ntiles && !stop; ct += gridDim.x) {
+        const Tile tl = tile_of<MODE>(ct, args);
         const int total = tl.nst * tl.eps;
-        for (int j = 0; j < total && !s.abort_flag; ++j, ++gj) {
-          if (static_cast<int64_t>(gj) == args.stall_at) {
-            stopped = true;
+        for (int j = 0; j < total; ++j, ++gj) {
+          if (s.abort_flag || static_cast<int64_t>(gj) == args.stall_at) {
+            stop = true;
             break;
           }
           const int e = gj % kRE;
           if (gj >= kRE && !mbar_wait(&s.ring_empty[e], ((gj / kRE) - 1) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
+            stop = true;
             break;
           }
-          const int i = j / tl.eps, q = j % tl.eps;
-          mbar_arrive_expect_tx(&s.ring_full[e], C::kEntryBytes);  // all CS slices land here
+          mbar_arrive_expect_tx(&s.ring_full[e], C::kEntryBytes);
           if (MODE == kFX) {
-            const int p = q / tl.nh, h = q % tl.nh;  // W_g / W_fc, k half
-            constexpr int kSliceRows = 256 / CS;
-            uint8_t* dst = s.ring[e] + crank * kSliceRows * 128;
-            const int kr = tl.k0 + 256 * h + static_cast<int>(crank) * kSliceRows;
-            if (CS > 1)
-              tma_load_2d_mc(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr, kMask);
-            else
-              tma_load_2d(dst, p ? &tm_b1 : &tm_b0, &s.ring_full[e], i * 64, kr);
+            const EntryPos ep = fx_entry(tl, j);
+            tma_load_2d(s.ring[e], ep.p ? &tm_b1 : &tm_b0, &s.ring_full[e], ep.i * 64, tl.k0 + 256 * ep.h);
           } else {
+            const int i = j / tl.eps, h = j % tl.eps;
             const int mrow = (tl.kb_begin + i) * 64;
-            const int kk = tl.k0 + 256 * q;
-            constexpr int kSliceChunks = 4 / CS;  // 64x64 blocks of the entry this CTA loads
-            const int c_begin = static_cast<int>(crank) * kSliceChunks;
-            uint8_t* dst = s.ring[e] + c_begin * 8192;
-            if (args.x3d) {
-              if (CS > 1)
-                tma_load_3d_mc(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin, kMask);
-              else
-                tma_load_3d(dst, &tm_b0, &s.ring_full[e], 0, mrow, kk / 64 + c_begin);
-            } else {
+            const int kk = tl.k0 + 256 * h;
+            // four 64 x 64 boxes: the entry's 64-column MN chunks (columns past K read as zeros)
 #pragma unroll
-              for (int c = 0; c < kSliceChunks; ++c) {
-                if (CS > 1)
-                  tma_load_2d_mc(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow, kMask);
-                else
-                  tma_load_2d(dst + c * 8192, &tm_b1, &s.ring_full[e], kk + 64 * (c_begin + c), mrow);
-              }
-            }
+            for (int cb = 0; cb < 4; ++cb)
+              tma_load_2d(s.ring[e] + cb * 8192, &tm_b0, &s.ring_full[e], kk + 64 * cb, mrow);
           }
           s.ring_issued = gj + 1;
         }
-      }
-      if (CS > 1 && !s.abort_flag) {
-        // the peers' last releases arrive on this CTA's barriers: see them land
-        // before this CTA can leave
-        for (uint32_t j = gj > static_cast<uint32_t>(kRE) ? gj - kRE : 0u; j < gj; ++j)
-          if (!mbar_wait(&s.ring_empty[j % kRE], (j / kRE) & 1, args.wait_limit)) {
-            flag_timeout(s, args.status);
-            break;
-          }
       }
     }
   } else if (warp == 1) {
@@ -325,72 +325,145 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, MODE == kFW, MODE == kFW);
       uint32_t gi = 0, gj = 0, tt = 0;  // A stages, ring entries, tiles consumed
       bool ok = true;
-      for (int ct = cluster; ct < args.cluster_tiles && ok; ct += nclusters, ++tt) {
-        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
-        if (tt > 0) {
-          // the previous tile's epilogue must have read the accumulator out
-          if (!mbar_wait(&s.tmem_free, (tt - 1) & 1, args.wait_limit)) {
-            flag_timeout(s, args.status);
-            break;
-          }
-          tc_fence_after();
+      // the MMAs of ring entry gj: stage i of the tile (A slot gi + i), product p, accumulator half h
+      auto consume = [&](int i, int p, int h) -> bool {
+        const int e = gj % kRE;
+        if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
+          flag_timeout(s, args.status);
+          return false;
         }
-        for (int i = 0; i < tl.nst && ok; ++i, ++gi) {
-          const int a = gi % kAS;
-          if (!mbar_wait(&s.a_full[a], (gi / kAS) & 1, args.wait_limit)) {
-            flag_timeout(s, args.status);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_slot = smem_u32(s.aop[a]);
-          for (int q = 0; q < tl.eps; ++q, ++gj) {
-            const int e = gj % kRE;
-            if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
-              flag_timeout(s, args.status);
-              ok = false;
-              break;
-            }
-            s.ring_consumed = gj + 1;
-            tc_fence_after();
-            const uint32_t b_addr = smem_u32(s.ring[e]);
-            if (MODE == kFX) {
-              const int p = q / tl.nh, h = q % tl.nh;
-              const uint32_t a_addr = a_slot + p * kHalf;  // dg or dfc
+        s.ring_consumed = gj + 1;
+        tc_fence_after();
+        const uint32_t b_addr = smem_u32(s.ring[e]);
+        const uint32_t a_slot = smem_u32(s.aop[(gi + i) % kAS]);
+        if (MODE == kFX) {
+          const uint32_t a_addr = a_slot + p * kHalf;  // dg or dfc
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024),
-                          smem_desc(b_addr + 32 * k, 16, 1024), idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
-            } else {
-              const int h = q;
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 32 * k, 16, 1024),
+                      idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
+        } else {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                umma_bf16(tmem + h * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
-                          smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
-            }
-            if (CS > 1)
-              umma_commit_mc(&s.ring_empty[e], kMask);  // release the entry in every CTA of the cluster
-            else
-              umma_commit(&s.ring_empty[e]);
-          }
-          umma_commit(&s.a_empty[a]);
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem + h * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
+                      smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
         }
+        umma_commit(&s.ring_empty[e]);
+        ++gj;
+        return true;
+      };
+      auto wait_a = [&](int i) -> bool {
+        const uint32_t g2 = gi + i;
+        if (!mbar_wait(&s.a_full[g2 % kAS], (g2 / kAS) & 1, args.wait_limit)) {
+          flag_timeout(s, args.status);
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
+      // the previous tile's epilogue has read accumulator half h out
+      auto wait_free = [&](int h) -> bool {
+        if (tt == 0) return true;
+        if (!mbar_wait(&s.tmem_free[h], (tt - 1) & 1, args.wait_limit)) {
+          flag_timeout(s, args.status);
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
+      for (int ct = blockIdx.x; ct < args.ntiles && ok; ct += gridDim.x, ++tt) {
+        const Tile tl = tile_of<MODE>(ct, args);
+        if (MODE == kFX) {
+          // the first J stages: low-half MMAs as soon as the low half is free, then
+          // their high-half MMAs once the high half is free too
+          const int J = tl.nh == 2 ? min(kSplitStages, tl.nst) : 0;
+          if (!wait_free(0)) break;
+          if (J == 0 && !wait_free(1)) break;
+          for (int i = 0; i < J && ok; ++i) {
+            ok = wait_a(i);
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 0);
+          }
+          if (ok && J > 0) ok = wait_free(1);
+          for (int i = 0; i < J && ok; ++i) {
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 1);
+            umma_commit(&s.a_empty[(gi + i) % kAS]);
+          }
+          for (int i = J; i < tl.nst && ok; ++i) {
+            ok = wait_a(i);
+            for (int q = 0; q < tl.eps && ok; ++q) ok = consume(i, q / tl.nh, q % tl.nh);
+            umma_commit(&s.a_empty[(gi + i) % kAS]);
+          }
+        } else {
+          if (!wait_free(0) || !wait_free(1)) break;
+          for (int i = 0; i < tl.nst && ok; ++i) {
+            ok = wait_a(i);
+            for (int h = 0; h < tl.eps && ok; ++h) ok = consume(i, 0, h);
+            umma_commit(&s.a_empty[(gi + i) % kAS]);
+          }
+        }
+        gi += tl.nst;
         umma_commit(&s.accum);  // this tile's accumulator is complete
       }
       // after a timeout the epilogue may have stopped waiting: see every MMA this thread
-      // issued complete before the CTA frees TMEM (tt accumulator phases were committed)
+      // issued complete before TMEM is freed (tt accumulator phases were committed)
       if (s.abort_flag && tt > 0) mbar_wait(&s.accum, (tt - 1) & 1, args.wait_limit);
     }
-  } else {
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ L2 prefetch of the raw tiles
+    if (lane == 0) {
+      int ntot = 0;
+      for (int ct = blockIdx.x; ct < args.ntiles; ct += gridDim.x) ntot += tile_of<MODE>(ct, args).nst;
+      int next = 0, tix = 0, in_tile = 0;
+      Tile tl = tile_of<MODE>(blockIdx.x, args);
+      uint32_t last = 0;
+      long long tlast = clock64();
+      while (next < ntot && !s.abort_flag) {
+        const uint32_t pr = s.x_progress;
+        if (pr != last) {
+          last = pr;
+          tlast = clock64();
+        }
+        if (next < static_cast<int>(pr) + C::kPrefetch + 1) {
+          if (MODE == kFX) {
+            const int p0 = in_tile * 64;
+            tma_prefetch_l2_2d(&tm_dy, p0, tl.m0);
+            tma_prefetch_l2_2d(&tm_g, p0, tl.m0);
+            tma_prefetch_l2_2d(&tm_fc, p0, tl.m0);
+          } else {
+            const int p1 = (tl.kb_begin + in_tile) * 64;
+            tma_prefetch_l2_2d(&tm_dy, tl.n0, p1);
+            tma_prefetch_l2_2d(&tm_g, tl.n0, p1);
+            tma_prefetch_l2_2d(&tm_fc, tl.n0, p1);
+          }
+          ++next;
+          if (++in_tile == tl.nst) {
+            in_tile = 0;
+            ++tix;
+            tl = tile_of<MODE>(blockIdx.x + tix * gridDim.x, args);
+          }
+        } else {
+          if (clock64() - tlast > args.wait_limit) break;  // the transform stopped making progress
+          __nanosleep(64);
+        }
+      }
+    }
+  } else if (warp >= kXWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kXRegs) : "memory");
     // ------------------------------------------------------------ transform
-    const int t = threadIdx.x - 64;  // 0..255
-    const int c = t & 7;             // 16-byte chunk of the 64-column tile (8 columns)
-    const int rg = t >> 3;           // row group 0..31; rows rg, rg + 32, ...
+    const int t = threadIdx.x - kXWarp0 * 32;  // 0..255
+    const int xw = warp - kXWarp0;             // transform warp 0..7
+    const int c = t & 7;                       // 16-byte chunk of the 64-column tile (8 columns)
+    const int rg = t >> 3;                     // row group 0..31; rows rg, rg + 32, ...
     const int64_t N64 = args.N;
     // A thread whose wait runs out stops computing ("dead") but keeps taking
     // part in the arrivals and the named barriers.
     bool dead = false;
 
+    // one arrival of this warp, after every lane's work before it
+    auto warp_arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
     // stores one stage's dg, dfc (8 columns x kRPT rows of this thread) into A slot a
     auto store_stage = [&](int a, int row0, int col, bool want_dg, const uint4 (&bdy)[kRPT],
                            const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT], float (&cg)[8], float (&cf)[8]) {
@@ -445,30 +518,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The CTA's stages form one stream over its tiles: stage st is stage
       // st % nst of the CTA's tile st / nst, and also the global A-stage index.
       // A tile's epilogue runs after the first kAS - 1 stages of the next tile
-      // are in their A slots, so the tensor core restarts as soon as the
-      // accumulator is drained; the staging buffer of the epilogue's TMA stores
+      // are in their A slots; the staging buffer of the epilogue's TMA stores
       // is the A slot of the finished tile's last stage, free once its MMAs are.
       const int nst = (args.N + 63) / 64;
-      const int ntiles = cluster < args.cluster_tiles ? (args.cluster_tiles - 1 - cluster) / nclusters + 1 : 0;
+      const int ntiles = static_cast<int>(blockIdx.x) < args.ntiles
+                             ? (args.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
       const int total = ntiles * nst;
       const int look = nst < kAS - 1 ? nst : kAS - 1;
-      auto tile_at = [&](int tix) { return tile_of<MODE, CS>(cluster + tix * nclusters, crank, args); };
+      auto tile_at = [&](int tix) { return tile_of<MODE>(blockIdx.x + tix * gridDim.x, args); };
       float ug[8], uf[8];  // column sums, unused here
 #pragma unroll
       for (int e = 0; e < 8; ++e) ug[e] = uf[e] = 0.0f;
+      uint4 zdy[kRPT], zg[kRPT], zfc[kRPT];
 
       auto load = [&](int st, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
         const bool valid = st < total;
         const int m0 = valid ? tile_at(st / nst).m0 : 0;
         load_rows(m0, (valid ? (st % nst) * 64 : 0) + c * 8, valid, bdy, bg, bfc);
-      };
-      auto prefetch = [&](int st) {
-        if (st < total) {
-          const int m0 = tile_at(st / nst).m0, p0 = (st % nst) * 64;
-          tma_prefetch_l2_2d(&tm_dy, p0, m0);
-          tma_prefetch_l2_2d(&tm_g, p0, m0);
-          tma_prefetch_l2_2d(&tm_fc, p0, m0);
-        }
       };
       auto process = [&](int st, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
         const int a = st % kAS;
@@ -478,9 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_stage(a, tl.m0, (st % nst) * 64 + c * 8, tl.kt == 0 && args.dg_out != nullptr, bdy, bg, bfc, ug,
                       uf);
         }
-        mbar_arrive(&s.a_full[a]);
+        warp_arrive(&s.a_full[a]);
+        if (t == 0) s.x_progress = static_cast<uint32_t>(st + 1);
       };
-      // tile tix's accumulator -> bf16 dx through staging buffer stg (an A slot)
+      // tile tix's accumulator -> bf16 dx through staging buffer stg (an A slot):
+      // the low half (columns 0-255) first, then the high half, each released to the
+      // MMA issuer as soon as every warp has read it
       auto epilogue = [&](int tix, int stg) {
         const Tile tl = tile_at(tix);
         bool acc_ok = false;
@@ -488,36 +558,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_ok = mbar_wait(&s.accum, tix & 1, args.wait_limit);
           if (!acc_ok) flag_timeout(s, args.status);
         }
-        const int q = warp & 3;         // TMEM lane quarter this warp may read
-        const int h = (warp - 2) >> 2;  // accumulator half this warp drains
+        const int q = warp & 3;   // TMEM lane quarter this warp may read
+        const int sub = xw >> 2;  // 128-column half of each accumulator half
         tc_fence_after();
         // tcgen05.ld is warp-collective: decide for the whole warp
-        if (h < tl.nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag)) {
+        const bool go = __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag);
+        int nb = 0;  // blocks stored by this warp (alternating 2 KB staging halves)
+        for (int h = 0; h < 2; ++h) {
+          if (go && h < tl.nh) {
 #pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + cc * 32, v);
-            tmem_ld_wait();
-            // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
-            // store (rows beyond M and columns beyond K are clipped by the copy engine)
-            uint8_t* buf = s.aop[stg] + (warp - 2) * 4096 + (cc & 1) * 2048;
-            if (cc >= 2) {
-              if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
-              __syncwarp();
-            }
-            const uint32_t sb = smem_u32(buf) + lane * 64;
+            for (int cc = 0; cc < 4; ++cc, ++nb) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + sub * 128 + cc * 32, v);
+              tmem_ld_wait();
+              // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
+              // store (rows beyond M and columns beyond K are clipped by the copy engine)
+              uint8_t* buf = s.aop[stg] + xw * 4096 + (nb & 1) * 2048;
+              if (nb >= 2) {
+                if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+                __syncwarp();
+              }
+              const uint32_t sb = smem_u32(buf) + lane * 64;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), pack8(v + 8 * j));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tm_out, buf, tl.k0 + h * 256 + cc * 32, tl.m0 + q * 32);
-              bulk_commit();
+              for (int j = 0; j < 4; ++j) sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), pack8(v + 8 * j));
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tm_out, buf, tl.k0 + h * 256 + sub * 128 + cc * 32, tl.m0 + q * 32);
+                bulk_commit();
+              }
             }
           }
+          tc_fence_before();
+          warp_arrive(&s.tmem_free[h]);  // this warp has read its part of half h
         }
-        tc_fence_before();
-        mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
         // the staging slot is written again by a later stage: every store has read it
         if (lane == 0) bulk_wait_read<0>();
         named_sync_transform();
@@ -527,29 +601,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tix >= 1 && st % nst + 1 == look) epilogue(tix - 1, (tix * nst - 1) % kAS);
       };
 
-      if (t == 0)
-        for (int p = 0; p <= C::kPrefetch; ++p) prefetch(p);
+      // three stages of registers: the loads of stages st + 1 and st + 2 are in
+      // flight while stage st is computed (and while an epilogue runs)
       load(0, xdy, xg, xfc);
-      for (int st = 0; st < total; st += 2) {
-        // two stages per iteration, alternating register buffers: the loads of the
-        // next stage are in flight while this stage is computed (and while an
-        // epilogue runs)
-        if (t == 0) prefetch(st + 1 + C::kPrefetch);
-        load(st + 1, ydy, yg, yfc);
+      load(1, ydy, yg, yfc);
+      for (int st = 0; st < total; st += 3) {
+        load(st + 2, zdy, zg, zfc);
         process(st, xdy, xg, xfc);
         after(st);
         if (st + 1 >= total) break;
-        if (t == 0) prefetch(st + 2 + C::kPrefetch);
-        load(st + 2, xdy, xg, xfc);
+        load(st + 3, xdy, xg, xfc);
         process(st + 1, ydy, yg, yfc);
         after(st + 1);
+        if (st + 2 >= total) break;
+        load(st + 4, ydy, yg, yfc);
+        process(st + 2, zdy, zg, zfc);
+        after(st + 2);
       }
       if (ntiles > 0) epilogue(ntiles - 1, (total - 1) % kAS);
       if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
     } else {
       uint32_t gi = 0, tt = 0;  // A stages, tiles produced
-      for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters, ++tt) {
-        const Tile tl = tile_of<MODE, CS>(ct, crank, args);
+      for (int ct = blockIdx.x; ct < args.ntiles; ct += gridDim.x, ++tt) {
+        const Tile tl = tile_of<MODE>(ct, args);
         const int n0 = tl.n0, k0 = tl.k0, kb_begin = tl.kb_begin, nst = tl.nst, nh = tl.nh, split = tl.split;
         const bool want_db = tl.kt == 0 && args.db_part != nullptr;
         float cg[8], cf[8];  // column sums over the CTA's whole M range
@@ -559,31 +633,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load = [&](int i, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
           load_rows((kb_begin + i) * 64, n0 + c * 8, i < nst, bdy, bg, bfc);
         };
-        auto prefetch = [&](int i) {
-          if (i < nst) {
-            const int p1 = (kb_begin + i) * 64;
-            tma_prefetch_l2_2d(&tm_dy, n0, p1);
-            tma_prefetch_l2_2d(&tm_g, n0, p1);
-            tma_prefetch_l2_2d(&tm_fc, n0, p1);
-          }
-        };
         auto process = [&](int i, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
           const uint32_t gs = gi + i;  // global A-stage index
           const int a = gs % kAS;
           acquire_slot(gs, a);
           if (!dead) store_stage(a, (kb_begin + i) * 64, n0 + c * 8, false, bdy, bg, bfc, cg, cf);
-          mbar_arrive(&s.a_full[a]);
+          warp_arrive(&s.a_full[a]);
+          if (t == 0) s.x_progress = gs + 1;
         };
 
-        if (t == 0)
-          for (int i = 0; i <= C::kPrefetch; ++i) prefetch(i);
+        // two stages per iteration, alternating register buffers: the loads of the
+        // next stage are in flight while this stage is computed
         load(0, xdy, xg, xfc);
         for (int i = 0; i < nst; i += 2) {
-          if (t == 0) prefetch(i + 1 + C::kPrefetch);
           load(i + 1, ydy, yg, yfc);
           process(i, xdy, xg, xfc);
           if (i + 1 >= nst) break;
-          if (t == 0) prefetch(i + 2 + C::kPrefetch);
           load(i + 2, xdy, xg, xfc);
           process(i + 1, ydy, yg, yfc);
         }
@@ -608,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_sync_transform();
           float* scratch = reinterpret_cast<float*>(s.aop[0]);  // [8 warps][8 chunks][16]
           if (lane < 8) {
-            float* pp = scratch + ((warp - 2) * 8 + c) * 16;
+            float* pp = scratch + (xw * 8 + c) * 16;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               pp[e] = cg[e];
@@ -633,8 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
         tc_fence_after();
-        const int r = q * 32 + lane;    // accumulator row (TMEM lane)
-        const int h = (warp - 2) >> 2;  // accumulator half this warp drains
+        const int r = q * 32 + lane;  // accumulator row (TMEM lane)
+        const int h = xw >> 2;        // accumulator half this warp drains
         // tcgen05.ld is warp-collective: decide for the whole warp
         if (h < nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag && nst > 0)) {
 #pragma unroll 1
@@ -671,7 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&s.tmem_free);  // this thread has read its part of the accumulator
+        warp_arrive(&s.tmem_free[0]);  // this warp has read its part of the accumulator
+        warp_arrive(&s.tmem_free[1]);
       }  // tile loop
     }
   }
@@ -687,7 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (CS > 1) cluster_sync();  // no CTA leaves while a peer may still write into it
 }
 
 template <int MODE>
@@ -695,36 +760,40 @@ constexpr size_t smem_bytes() {
   return sizeof(FSmem<MODE>) + 1024;
 }
 
-template <int MODE, int CS>
+template <int MODE>
 cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const CUtensorMap& out,
                    FusedArgs args, bool persistent) {
   constexpr size_t smem = smem_bytes<MODE>();
   static_assert(smem <= 232448, "fused kernel shared memory");
-  cudaError_t err = cudaFuncSetAttribute(fused_kernel<MODE, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static_assert(128 * kCtlRegs + 256 * kXRegs <= kThreads * 168, "setmaxnreg split exceeds a 168-register launch");
+  cudaError_t err = cudaFuncSetAttribute(fused_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  args.cluster_tiles = static_cast<int>(grid / CS);
-  if (persistent) {
-    // one resident wave of clusters, each looping over cluster tiles
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, fused_kernel<MODE, CS>, &cfg) == cudaSuccess &&
-        max_clusters > 0 && static_cast<unsigned>(max_clusters) * CS < grid)
-      cfg.gridDim = dim3(static_cast<unsigned>(max_clusters) * CS);
+  {
+    // setmaxnreg redistributes the block's launch registers: warpgroup 0 drops to
+    // kCtlRegs per thread, the two transform warpgroups rise to kXRegs. The sum must
+    // fit what the block was launched with, else an increase would wait forever:
+    // refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, fused_kernel<MODE>);
+    if (err != cudaSuccess) return err;
+    if (static_cast<long long>(fa.numRegs) * kThreads < 128LL * kCtlRegs + 256LL * kXRegs)
+      return cudaErrorInvalidValue;
   }
-  return cudaLaunchKernelEx(&cfg, fused_kernel<MODE, CS>, a, b, c, d, e, out, args);
+  args.ntiles = static_cast<int>(grid);
+  if (persistent) {
+    // one resident wave, each CTA looping over tiles
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<MODE>, kThreads, smem) ==
+            cudaSuccess &&
+        per_sm > 0) {
+      const unsigned wave = static_cast<unsigned>(per_sm * device_sm_count());
+      if (wave < grid) grid = wave;
+    }
+  }
+  fused_kernel<MODE><<<grid, kThreads, smem, stream>>>(a, b, c, d, e, out, args);
+  return cudaGetLastError();
 }
 
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -751,15 +820,13 @@ FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
 cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, const uint16_t* w_g,
                            const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
                            int64_t N, cudaStream_t stream) {
-  constexpr int CS = kClusterX;
   CUtensorMap mdy, mg, mfc, mw0, mw1, mdx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mdx, dx, K, M, static_cast<uint64_t>(K) * 2, 32, 32, 64)) return cudaErrorInvalidValue;
   // the raw tensors are only prefetched into L2 here, one stage's box at a time
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 128, 0) ||
-      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) ||
-      !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256 / CS) ||
-      !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256 / CS))
+      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256) ||
+      !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256))
     return cudaErrorInvalidValue;
   FusedArgs a{};
   a.M = static_cast<int>(M);
@@ -776,9 +843,8 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
   const Injection inj = take_injection(2);
   a.wait_limit = inj.wait_limit;
   a.stall_at = inj.stall_at;
-  const int64_t mclusters = ((M + 127) / 128 + CS - 1) / CS;  // tail CTAs run on zero-filled rows
-  return launch<kFX, CS>(static_cast<unsigned>(mclusters * CS * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, mdx, a,
-                         true);
+  const int64_t tiles = (M + 127) / 128 * a.tiles_k;
+  return launch<kFX>(static_cast<unsigned>(tiles), stream, mdy, mg, mfc, mw0, mw1, mdx, a, true);
 }
 
 namespace {
@@ -788,23 +854,13 @@ namespace {
 cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                              uint16_t* dw_g, uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, float* dw_part,
                              float* db_part, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
-  CUtensorMap mdy, mg, mfc, mx2, mx3;
+  CUtensorMap mdy, mg, mfc, mx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
+  // x as 64 x 64 boxes (64 columns of k, 64 rows of m): 8 KB MN-major chunks
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 64) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 64) ||
       !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 64) ||
-      !encode_tmap_2d_bf16(&mx2, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64))
+      !encode_tmap_2d_bf16(&mx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64))
     return cudaErrorInvalidValue;
-  constexpr int CS = kClusterW;
-  // x viewed as [K/64 chunks][M rows][64]: one box {64, 64 rows, 4/CS chunks} lands as
-  // 8 KB 64x64 blocks, the MN-major layout of (a slice of) one operand entry
-  int x3d = 0;
-  if (K % 64 == 0) {
-    const uint64_t dims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(K / 64)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
-    const uint32_t box[3] = {64, 64, 4 / CS};
-    x3d = encode_tmap_3d_bf16(&mx3, x, dims, strides, box, 128) ? 1 : 0;
-  }
-  if (!x3d) mx3 = mx2;
   FusedArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
@@ -821,13 +877,12 @@ cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16
   a.splits = static_cast<int>(plan.splits);
   a.kb_per = static_cast<int>(plan.kb_per);
   a.nkb_total = static_cast<int>((M + 63) / 64);
-  a.tiles_n = static_cast<int>(((N + 63) / 64 + CS - 1) / CS * CS);  // clusters of CS n tiles
-  a.x3d = x3d;
+  a.tiles_n = static_cast<int>((N + 63) / 64);
   a.accumulate = accumulate ? 1 : 0;
   a.wait_limit = kWaitLimitCycles;
   a.stall_at = -1;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
-  return launch<kFW, CS>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx3, mx2, mx2, a, false);
+  return launch<kFW>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx, mx, mx, a, false);
 }
 
 }  // namespace

@@ -1,11 +1,10 @@
-// w and x stages of the SwiGLU-FFN backward as tcgen05 (TMEM-accumulator) bf16
-// GEMMs fed by TMA.
+// w stage of the SwiGLU-FFN backward as a tcgen05 (TMEM-accumulator) bf16 GEMM
+// fed by TMA (the x stage is in xgemm_tc.cu), and the tensor-map, plan and
+// status-word helpers the other kernels share.
 //
 // Source: "PyPTO-Gym in practice: the fused SwiGLU backward operator",
-// "Algorithm overview and formulas" items 3-4 and the w/x rows of "Kernel
+// "Algorithm overview and formulas" item 3 and the w row of "Kernel
 // signatures":
-//   x stage: dx = dg W_g^T + dfc W_fc^T  -- one GEMM [dg | dfc] [W_g | W_fc]^T,
-//            reduction length 2N; the k loop walks (dg, W_g) then (dfc, W_fc).
 //   w stage: dw_g = x^T dg, dw_fc = x^T dfc -- one launch, the two outputs are
 //            two tile sets; the reduction runs over M and is split into S
 //            chunks whose fp32 partials a second kernel adds in a fixed order.
@@ -18,14 +17,11 @@
 // warps 2-5 read the 128x256 fp32 accumulator out of TMEM (each warp its own
 // 32-lane quarter) and store bf16 (or fp32 partials).
 //
-// Operand layouts (shared memory, 128-byte swizzle, written by TMA):
-//   x stage, K-major: A tile = 128 rows of dg/dfc x 64 reduction elements;
-//     B tile = 256 rows of W x 64 reduction elements; 8-row groups 1024 B
-//     apart (SBO), +32 B per K=16 step.
-//   w stage, MN-major: the reduction index m is the strided one. A tile =
-//     x[m0:m0+64, k0:k0+128] as two 64x64 boxes (8 KB apart = LBO, the stride
-//     between 64-element MN chunks), B tile = dg[m0:m0+64, n0:n0+256] as four
-//     boxes; 8-row k groups 1024 B apart (SBO), +2048 B per K=16 step.
+// Operand layouts (shared memory, 128-byte swizzle, written by TMA), MN-major:
+// the reduction index m is the strided one. A tile = x[m0:m0+64, k0:k0+128] as
+// two 64x64 boxes (8 KB apart = LBO, the stride between 64-element MN chunks),
+// B tile = dg[m0:m0+64, n0:n0+256] as four boxes; 8-row k groups 1024 B apart
+// (SBO), +2048 B per K=16 step.
 // Tails of M, K and N are zero-filled by TMA on load and masked on store.
 //
 // Every mbarrier wait is bounded; on timeout the kernel ORs a flag into the
@@ -52,7 +48,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 
-enum Mode : int { kModeX = 0, kModeW = 1 };
+enum Mode : int { kModeW = 1 };
 
 struct __align__(1024) Smem {
   uint8_t a[STAGES][A_BYTES];
@@ -69,18 +65,11 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct GemmArgs {
   int M, K, N;
-  // x stage
-  uint16_t* dx;
-  int tiles_k;  // dx column tiles
-  int nkb_half; // reduction blocks per half (ceil(N / 64))
-  // w stage
   uint16_t* dw[2];
   float* ws;
   int splits, kb_per, nkb_total;
   int tiles_kw, tiles_nw;  // dw tile grid per problem
   int accumulate;          // dw += this call's sums (one rounding of old + new)
-  long long wait_limit;    // cycles before a pipeline wait gives up
-  int stall_at;            // test injection: the producer stops before this k block (-1: never)
 };
 
 __device__ __forceinline__ void flag_timeout(Smem& s) {
@@ -99,26 +88,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- tile coordinates
-  int m0 = 0, n0 = 0, prob = 0, split = 0, kb_begin = 0, kb_end = 0;
-  if (MODE == kModeX) {
-    const int t = blockIdx.x;
-    n0 = (t % args.tiles_k) * BN;      // dx columns (index k of W)
-    m0 = (t / args.tiles_k) * BM;      // dx rows
-    kb_begin = 0;
-    kb_end = 2 * args.nkb_half;
-  } else {
-    int t = blockIdx.x;
-    const int nt = t % args.tiles_nw;
-    t /= args.tiles_nw;
-    const int kt = t % args.tiles_kw;
-    t /= args.tiles_kw;
-    prob = t % 2;
-    split = t / 2;
-    m0 = kt * BM;                      // dw rows (index k)
-    n0 = nt * BN;                      // dw columns (index n)
-    kb_begin = split * args.kb_per;
-    kb_end = min(args.nkb_total, kb_begin + args.kb_per);
-  }
+  int t = blockIdx.x;
+  const int nt = t % args.tiles_nw;
+  t /= args.tiles_nw;
+  const int kt = t % args.tiles_kw;
+  t /= args.tiles_kw;
+  const int prob = t % 2;
+  const int split = t / 2;
+  const int m0 = kt * BM;  // dw rows (index k)
+  const int n0 = nt * BN;  // dw columns (index n)
+  const int kb_begin = split * args.kb_per;
+  const int kb_end = min(args.nkb_total, kb_begin + args.kb_per);
   const int nkb = kb_end - kb_begin;
 
   if (threadIdx.x == 0) {
@@ -151,35 +131,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nkb; ++i) {
       const int st = i % STAGES;
       const int use = i / STAGES;
-      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, args.wait_limit)) {
+      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1)) {
         flag_timeout(s);
         break;
       }
-      if (s.abort_flag || i == args.stall_at) break;
+      if (s.abort_flag) break;
       mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
-      const int kb = kb_begin + i;
-      if (MODE == kModeX) {
-        const bool second = kb >= args.nkb_half;
-        const int r0 = (second ? kb - args.nkb_half : kb) * BK;  // reduction offset within N
-        tma_load_2d(s.a[st], second ? &tmA1 : &tmA0, &s.full[st], r0, m0);
-        tma_load_2d(s.b[st], second ? &tmB1 : &tmB0, &s.full[st], r0, n0);
-      } else {
-        const int mr = kb * BK;  // reduction rows of M
-        tma_load_2d(s.a[st], &tmA0, &s.full[st], m0, mr);
-        tma_load_2d(s.a[st] + 8192, &tmA0, &s.full[st], m0 + 64, mr);
-        const CUtensorMap* tb = prob ? &tmB1 : &tmB0;
+      const int mr = (kb_begin + i) * BK;  // reduction rows of M
+      tma_load_2d(s.a[st], &tmA0, &s.full[st], m0, mr);
+      tma_load_2d(s.a[st] + 8192, &tmA0, &s.full[st], m0 + 64, mr);
+      const CUtensorMap* tb = prob ? &tmB1 : &tmB0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tma_load_2d(s.b[st] + j * 8192, tb, &s.full[st], n0 + 64 * j, mr);
-      }
+      for (int j = 0; j < 4; ++j) tma_load_2d(s.b[st] + j * 8192, tb, &s.full[st], n0 + 64 * j, mr);
       issued = i + 1;
       s.issued = issued;
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, MODE == kModeW, MODE == kModeW);
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 1, 1);  // both operands MN-major
     for (int i = 0; i < nkb; ++i) {
       const int st = i % STAGES;
-      if (!mbar_wait(&s.full[st], (i / STAGES) & 1, args.wait_limit)) {
+      if (!mbar_wait(&s.full[st], (i / STAGES) & 1)) {
         flag_timeout(s);
         break;
       }
@@ -188,27 +160,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_addr = smem_u32(s.a[st]);
       const uint32_t b_addr = smem_u32(s.b[st]);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        uint64_t ad, bd;
-        if (MODE == kModeX) {
-          ad = smem_desc(a_addr + 32 * k, 16, 1024);
-          bd = smem_desc(b_addr + 32 * k, 16, 1024);
-        } else {
-          ad = smem_desc(a_addr + 2048 * k, 8192, 1024);
-          bd = smem_desc(b_addr + 2048 * k, 8192, 1024);
-        }
-        umma_bf16(tmem, ad, bd, idesc, (i > 0 || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < BK / 16; ++k)
+        umma_bf16(tmem, smem_desc(a_addr + 2048 * k, 8192, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024), idesc,
+                  (i > 0 || k > 0) ? 1u : 0u);
       umma_commit(&s.empty[st]);
     }
     umma_commit(&s.accum);
     // after a timeout the epilogue may have stopped waiting: see every MMA this thread
     // issued complete before the CTA frees TMEM
-    if (s.abort_flag) mbar_wait(&s.accum, 0, args.wait_limit);
+    if (s.abort_flag) mbar_wait(&s.accum, 0);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const bool ok = mbar_wait(&s.accum, 0, args.wait_limit);
+    const bool ok = mbar_wait(&s.accum, 0);
     if (!ok) flag_timeout(s);
     tc_fence_after();
     const int r = q * 32 + lane;  // accumulator row
@@ -221,20 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         const int row = m0 + r;
         const int col = n0 + c * 32;
-        if (MODE == kModeX) {
-          if (row < args.M) {
-            uint4* dst = reinterpret_cast<uint4*>(args.dx + static_cast<int64_t>(row) * args.K + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (col + 8 * j < args.K) {
-                dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-              }
-            }
-          }
-        } else {
+        {
           if (row < args.K) {
             if (args.splits == 1) {
               uint4* dst = reinterpret_cast<uint4*>(args.dw[prob] + static_cast<int64_t>(row) * args.N + col);
@@ -274,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && s.abort_flag) {
     // drain: TMA copies issued but never consumed must land before the CTA exits
     for (uint32_t i = s.consumed; i < s.issued; ++i) {
-      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1, args.wait_limit)) break;
+      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
     }
   }
   __syncthreads();
@@ -393,30 +344,6 @@ WPlan w_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
   return p;
 }
 
-cudaError_t launch_x_gemm(const uint16_t* dg, const uint16_t* dfc, const uint16_t* w_g, const uint16_t* w_fc,
-                          uint16_t* dx, int64_t M, int64_t K, int64_t N, cudaStream_t stream) {
-  CUtensorMap a0, a1, b0, b1;
-  const uint64_t rs = static_cast<uint64_t>(N) * 2;
-  if (!encode_tmap_2d_bf16(&a0, dg, N, M, rs, BK, BM) || !encode_tmap_2d_bf16(&a1, dfc, N, M, rs, BK, BM) ||
-      !encode_tmap_2d_bf16(&b0, w_g, N, K, rs, BK, BN) || !encode_tmap_2d_bf16(&b1, w_fc, N, K, rs, BK, BN))
-    return cudaErrorInvalidValue;
-  GemmArgs a{};
-  a.M = static_cast<int>(M);
-  a.K = static_cast<int>(K);
-  a.N = static_cast<int>(N);
-  a.dx = dx;
-  a.tiles_k = static_cast<int>((K + BN - 1) / BN);
-  a.nkb_half = static_cast<int>((N + BK - 1) / BK);
-  const Injection inj = take_injection(1);
-  a.wait_limit = inj.wait_limit;
-  a.stall_at = static_cast<int>(inj.stall_at);
-  const int64_t tiles = ((M + BM - 1) / BM) * a.tiles_k;
-  cudaError_t e = prepare_kernel<kModeX>();
-  if (e != cudaSuccess) return e;
-  tc_gemm_kernel<kModeX><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(a0, a1, b0, b1, a);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t* dfc, uint16_t* dw_g,
                           uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws, const WPlan& plan,
                           cudaStream_t stream, bool accumulate) {
@@ -438,8 +365,6 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
   a.tiles_kw = static_cast<int>((K + BM - 1) / BM);
   a.tiles_nw = static_cast<int>((N + BN - 1) / BN);
   a.accumulate = accumulate ? 1 : 0;
-  a.wait_limit = kWaitLimitCycles;
-  a.stall_at = -1;
   const int64_t ctas = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
   cudaError_t e = prepare_kernel<kModeW>();
   if (e != cudaSuccess) return e;
