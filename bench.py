@@ -255,7 +255,7 @@ def run_ours(args, rank, world):
     kernels = {
         "b_stage": dict(bound="hbm", work=10.0 * M * N + 4.0 * N, peak=pk["hbm"], unit="GB/s", src="b_stage.cu"),
         "w_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
-        "x_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="gemm_tc.cu"),
+        "x_gemm": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="xgemm_tc.cu"),
         "x_fused": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="fused_tc.cu"),
         "w_fused": dict(bound="tensor", work=gemm_flop, peak=pk["bf16"], unit="TFLOP/s", src="fused_tc.cu"),
     }
