@@ -309,8 +309,8 @@ swg_status act_grad(const void* grad, const void* x, swg_act act, void* grad_x,
  * All tensors share `dtype` (fp32 / fp16 / bf16), aligned to their element size
  * (SWG_ERR_UNSUPPORTED otherwise); 16-byte aligned groups take the bulk-copy
  * path, others plain loads. Math is fp32, sums in a fixed order (dgamma and
- * dbeta added over samples in fp64); each output is rounded once (RNE);
- * results are bitwise reproducible.
+ * dbeta: each sample's partials added in fp32, the samples in fp64); each
+ * output is rounded once (RNE); results are bitwise reproducible.
  * Errors: G < 1, C not a multiple of G, a negative size or a negative / NaN eps
  * -> SWG_ERR_PARAM_INVALID; N G >= 2^28 or N C HxW >= 2^60 -> SWG_ERR_UNSUPPORTED; x, dy or dx NULL
  * with N C HxW > 0 -> SWG_ERR_NULLPTR; outputs overlapping inputs or each other

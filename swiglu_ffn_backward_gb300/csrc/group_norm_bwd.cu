@@ -19,19 +19,24 @@
 //             sample variance: analysis and recommendations", 1983):
 //             sum(x - K), sum((x - K)^2), sum(gamma dy), sum(gamma dy (x - K)),
 //             and per channel sum(dy), sum(dy (x - K));
-//   exchange  the four group sums through distributed shared memory, added in
-//             cluster-rank order by every CTA (the same value in all of them);
-//             the coefficients are formed in fp32 (this part's FP64 rate is a
-//             small fraction of its FP32 rate, and this step is on every CTA's
-//             critical path);
-//   pass 2    dx = (rstd gamma_c) dy + c2 + c3 ((x - K) - d), d = mu - K, written
-//             over x in shared memory and stored with bulk copies part by part.
-// A slice longer than the shared-memory stage is taken stage by stage and read
-// again for pass 2. Tensors whose groups do not start on 16-byte boundaries
-// take plain loads and stores. dgamma, dbeta: the per-(sample, group, slice,
-// channel) partials and the per-(sample, group) d and rstd go to the
-// workspace; a second kernel adds them over samples and slices in a fixed
-// order in fp64, so every output is bitwise reproducible.
+//   exchange  the four group sums of every warp of every CTA, added in the same
+//             fixed order by every warp (the same value in all of them); the
+//             persistent kernel pushes them into each CTA's shared memory with
+//             st.async (an mbarrier counts the bytes in), the per-group kernel
+//             reads them through distributed shared memory after a cluster
+//             barrier; the coefficients are formed in fp32 (this part's FP64
+//             rate is a small fraction of its FP32 rate, and this step is on
+//             every CTA's critical path);
+//   pass 2    dx = (rstd gamma_c) dy + c3 (x - K) + c2', c2' = c2 - c3 d,
+//             d = mu - K, written over x in shared memory and stored with bulk
+//             copies.
+// Both passes work on element pairs with the packed fp32x2 operations. A slice
+// longer than the shared-memory stage is taken stage by stage and read again
+// for pass 2. Tensors whose groups do not start on 16-byte boundaries take
+// plain loads and stores. dgamma, dbeta: the per-(sample, group, slice,
+// channel, warp) partials and the per-(sample, group) d and rstd go to the
+// workspace; a second kernel adds each sample's partials in fp32 and the
+// samples in fp64, in a fixed order, so every output is bitwise reproducible.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,6 +50,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+static_assert((kThreads & (kThreads - 1)) == 0, "items are dealt to threads by residue");
 constexpr int kParts = 2;                  // bulk-copy parts per stage, one mbarrier each (measured: 2 over 4 and 1)
 constexpr int kStageBytes = 96 * 1024;     // largest x and dy stage (slices longer than it are streamed)
 constexpr int kSliceBytes = 48 * 1024;     // target x and dy bytes per CTA (measured: 48 KB over 24 and 12)
@@ -68,15 +74,27 @@ __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// a 16-byte vector of T <-> floats
-template <typename T>
-struct Vec16 {
-  static constexpr int kN = 16 / static_cast<int>(sizeof(T));
-  union {
-    uint4 u;
-    T e[kN];
-  };
-};
+// two adjacent 16-bit elements (one 32-bit word) <-> a float2; for fp32 a pair of words
+__device__ __forceinline__ float2 pair_f(uint32_t u, __half) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return __half22float2(h);
+}
+__device__ __forceinline__ float2 pair_f(uint32_t u, __nv_bfloat16) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t pair_t(float2 v, __half) {
+  const __half2 h = __floats2half2_rn(v.x, v.y);
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+__device__ __forceinline__ uint32_t pair_t(float2 v, __nv_bfloat16) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -89,54 +107,95 @@ __device__ __forceinline__ double warp_sum(double v) {
   return v;
 }
 
+// Thread t takes the items i = t (mod kThreads) of a slice in every channel segment, so the items of
+// a slice spread evenly over the warps whatever the segments' lengths: the first such item at or after s.
+__device__ __forceinline__ int first_of_class(int s) {
+  return s + ((static_cast<int>(threadIdx.x) - s) & (kThreads - 1));
+}
+
+// The 16-byte vectors of one word quadruple: the pass-1 and pass-2 loops work on element pairs with
+// the packed fp32x2 operations (__fadd2_rn, __ffma2_rn: one instruction for two lanes of fp32), so the
+// sums below hold the even and the odd elements of each pair in .x and .y.
+//
 // pass-1 sums over stage-local [s, e) of one channel (vectorised: s, e multiples of the vector)
 template <typename T, bool kVec>
-__device__ __forceinline__ void acc_range(const T* xs, const T* ds, int s, int e, float K, float& sx, float& sxx,
-                                          float& sd, float& se) {
+__device__ __forceinline__ void acc_range(const T* xs, const T* ds, int s, int e, float K, float2& sx, float2& sxx,
+                                          float2& sd, float2& se) {
   if (kVec) {
-    constexpr int V = Vec16<T>::kN;
-    for (int v = s / V + static_cast<int>(threadIdx.x); v < e / V; v += kThreads) {
-      Vec16<T> vx, vd;
-      vx.u = reinterpret_cast<const uint4*>(xs)[v];
-      vd.u = reinterpret_cast<const uint4*>(ds)[v];
+    constexpr int V = 16 / static_cast<int>(sizeof(T));
+    const float2 nK = make_float2(-K, -K);
+    for (int v = first_of_class(s / V); v < e / V; v += kThreads) {
+      const uint4 ux = reinterpret_cast<const uint4*>(xs)[v];
+      const uint4 ud = reinterpret_cast<const uint4*>(ds)[v];
+      const uint32_t wx[4] = {ux.x, ux.y, ux.z, ux.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+      if constexpr (sizeof(T) == 2) {
 #pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const float xk = to_f(vx.e[i]) - K, dv = to_f(vd.e[i]);
-        sx += xk;
-        sxx = fmaf(xk, xk, sxx);
-        sd += dv;
-        se = fmaf(dv, xk, se);
+        for (int i = 0; i < 4; ++i) {
+          const float2 xk = __fadd2_rn(pair_f(wx[i], T()), nK), dv = pair_f(wd[i], T());
+          sx = __fadd2_rn(sx, xk);
+          sxx = __ffma2_rn(xk, xk, sxx);
+          sd = __fadd2_rn(sd, dv);
+          se = __ffma2_rn(dv, xk, se);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 xk = __fadd2_rn(make_float2(__uint_as_float(wx[2 * i]), __uint_as_float(wx[2 * i + 1])), nK);
+          const float2 dv = make_float2(__uint_as_float(wd[2 * i]), __uint_as_float(wd[2 * i + 1]));
+          sx = __fadd2_rn(sx, xk);
+          sxx = __ffma2_rn(xk, xk, sxx);
+          sd = __fadd2_rn(sd, dv);
+          se = __ffma2_rn(dv, xk, se);
+        }
       }
     }
   } else {
-    for (int i = s + static_cast<int>(threadIdx.x); i < e; i += kThreads) {
+    for (int i = first_of_class(s); i < e; i += kThreads) {
       const float xk = to_f(xs[i]) - K, dv = to_f(ds[i]);
-      sx += xk;
-      sxx = fmaf(xk, xk, sxx);
-      sd += dv;
-      se = fmaf(dv, xk, se);
+      sx.x += xk;
+      sxx.x = fmaf(xk, xk, sxx.x);
+      sd.x += dv;
+      se.x = fmaf(dv, xk, se.x);
     }
   }
 }
 
-// pass 2 over stage-local [s, e) of one channel: dx = aj dy + c2 + c3 ((x - K) - d), written over x
+// pass 2 over stage-local [s, e) of one channel: dx = aj dy + c3 (x - K) + c2', c2' = c2 - c3 d, written
+// over x
 template <typename T, bool kVec>
 __device__ __forceinline__ void dx_range(T* xs, const T* ds, int s, int e, float K, float aj, float d, float c2,
                                          float c3) {
+  const float c2d = fmaf(-c3, d, c2);
   if (kVec) {
-    constexpr int V = Vec16<T>::kN;
-    for (int v = s / V + static_cast<int>(threadIdx.x); v < e / V; v += kThreads) {
-      Vec16<T> vx, vd, vo;
-      vx.u = reinterpret_cast<const uint4*>(xs)[v];
-      vd.u = reinterpret_cast<const uint4*>(ds)[v];
+    constexpr int V = 16 / static_cast<int>(sizeof(T));
+    const float2 nK = make_float2(-K, -K), a2 = make_float2(aj, aj), c3v = make_float2(c3, c3),
+                 c2v = make_float2(c2d, c2d);
+    for (int v = first_of_class(s / V); v < e / V; v += kThreads) {
+      const uint4 ux = reinterpret_cast<const uint4*>(xs)[v];
+      const uint4 ud = reinterpret_cast<const uint4*>(ds)[v];
+      const uint32_t wx[4] = {ux.x, ux.y, ux.z, ux.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+      uint32_t wo[4];
+      if constexpr (sizeof(T) == 2) {
 #pragma unroll
-      for (int i = 0; i < V; ++i)
-        vo.e[i] = from_f<T>(fmaf(aj, to_f(vd.e[i]), fmaf(c3, (to_f(vx.e[i]) - K) - d, c2)));
-      reinterpret_cast<uint4*>(xs)[v] = vo.u;
+        for (int i = 0; i < 4; ++i) {
+          const float2 xk = __fadd2_rn(pair_f(wx[i], T()), nK);
+          wo[i] = pair_t(__ffma2_rn(a2, pair_f(wd[i], T()), __ffma2_rn(c3v, xk, c2v)), T());
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 xk = __fadd2_rn(make_float2(__uint_as_float(wx[2 * i]), __uint_as_float(wx[2 * i + 1])), nK);
+          const float2 o = __ffma2_rn(a2, make_float2(__uint_as_float(wd[2 * i]), __uint_as_float(wd[2 * i + 1])),
+                                      __ffma2_rn(c3v, xk, c2v));
+          wo[2 * i] = __float_as_uint(o.x);
+          wo[2 * i + 1] = __float_as_uint(o.y);
+        }
+      }
+      reinterpret_cast<uint4*>(xs)[v] = make_uint4(wo[0], wo[1], wo[2], wo[3]);
     }
   } else {
-    for (int i = s + static_cast<int>(threadIdx.x); i < e; i += kThreads)
-      xs[i] = from_f<T>(fmaf(aj, to_f(ds[i]), fmaf(c3, (to_f(xs[i]) - K) - d, c2)));
+    for (int i = first_of_class(s); i < e; i += kThreads)
+      xs[i] = from_f<T>(fmaf(aj, to_f(ds[i]), fmaf(c3, to_f(xs[i]) - K, c2d)));
   }
 }
 
@@ -167,6 +226,18 @@ struct GnArgs {
 struct GnCoef {
   float d, c1, c2, c3;  // d = mu - K, c1 = rstd; dx = (c1 gamma_c) dy + c2 + c3 ((x - K) - d)
 };
+// the coefficients from the group sums v0 = sum(x - K), v1 = sum((x - K)^2), v2 = sum(gamma dy),
+// v3 = sum(gamma dy (x - K))
+__device__ __forceinline__ GnCoef make_coef(float v0, float v1, float v2, float v3, const GnArgs& a) {
+  GnCoef c;
+  c.d = v0 * a.inv_m;                                         // mu - K
+  const float var = fmaxf(fmaf(v1, a.inv_m, -c.d * c.d), 0.0f);  // biased
+  c.c1 = rsqrtf(var + a.eps);                                 // rstd
+  const float B = c.c1 * fmaf(-c.d, v2, v3);                  // sum gamma dy x_hat
+  c.c2 = -c.c1 * v2 * a.inv_m;
+  c.c3 = -c.c1 * c.c1 * B * a.inv_m;
+  return c;
+}
 __device__ __forceinline__ GnCoef cluster_coef(const float (*ws)[4], const GnArgs& a) {
   const int lane = threadIdx.x & 31;
   float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
@@ -180,26 +251,14 @@ __device__ __forceinline__ GnCoef cluster_coef(const float (*ws)[4], const GnArg
     v2 += t2;
     v3 += t3;
   }
-  v0 = warp_sum(v0);
-  v1 = warp_sum(v1);
-  v2 = warp_sum(v2);
-  v3 = warp_sum(v3);
-  GnCoef c;
-  c.d = v0 * a.inv_m;                                         // mu - K
-  const float var = fmaxf(fmaf(v1, a.inv_m, -c.d * c.d), 0.0f);  // biased
-  c.c1 = rsqrtf(var + a.eps);                                 // rstd
-  const float B = c.c1 * fmaf(-c.d, v2, v3);                  // sum gamma dy x_hat
-  c.c2 = -c.c1 * v2 * a.inv_m;
-  c.c3 = -c.c1 * c.c1 * B * a.inv_m;
-  return c;
+  return make_coef(warp_sum(v0), warp_sum(v1), warp_sum(v2), warp_sum(v3), a);
 }
 
 // channel j closes (ends, or the slice ends inside it): gamma-weight the thread's sums into the
 // group sums; the warp's channel partials go to the workspace
-template <typename T>
-__device__ __forceinline__ void close_channel(int j, const T* gam, float* part, float& sd, float& se, float& ga,
+__device__ __forceinline__ void close_channel(int j, float gj, float* part, float2& sd2, float2& se2, float& ga,
                                               float& ge) {
-  const float gj = gam != nullptr ? to_f(gam[j]) : 1.0f;
+  const float sd = sd2.x + sd2.y, se = se2.x + se2.y;
   ga = fmaf(gj, sd, ga);
   ge = fmaf(gj, se, ge);
   if (part != nullptr) {
@@ -210,8 +269,8 @@ __device__ __forceinline__ void close_channel(int j, const T* gam, float* part, 
       q[1] = E;
     }
   }
-  sd = 0.f;
-  se = 0.f;
+  sd2 = make_float2(0.f, 0.f);
+  se2 = make_float2(0.f, 0.f);
 }
 
 // One cluster per (sample, group); slices longer than the stage are streamed
@@ -282,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
   // Channels are tracked incrementally (no integer division in the loops): j is
   // the channel at stage-local position s, jend the stage-local end of j. The
   // open channel's sums stay in registers across stages.
-  float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f, sd = 0.f, se = 0.f;
+  float2 sx2 = make_float2(0.f, 0.f), sxx2 = sx2, sd = sx2, se = sx2;
+  float ga = 0.f, ge = 0.f;
   bool open = false;
   int j = 0;
   for (int64_t st = 0; st < nst; ++st) {
@@ -298,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
       const int s1 = min(clen, (p + 1) * plen);
       for (int s = p * plen; s < s1;) {
         const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
-        acc_range<T, kMode == kBulkVec>(xs, ds, s, e, K, sx, sxx, sd, se);
+        acc_range<T, kMode == kBulkVec>(xs, ds, s, e, K, sx2, sxx2, sd, se);
         open = true;
         if (e == jend) {
-          close_channel(j, gam, part, sd, se, ga, ge);
+          close_channel(j, gam != nullptr ? to_f(gam[j]) : 1.0f, part, sd, se, ga, ge);
           open = false;
           ++j;
           jend += a.hw;
@@ -310,11 +370,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
       }
     }
   }
-  if (open) close_channel(j, gam, part, sd, se, ga, ge);  // the slice ends inside channel j
+  if (open) close_channel(j, gam != nullptr ? to_f(gam[j]) : 1.0f, part, sd, se, ga, ge);  // the slice ends in j
 
   // ---------------------------------------------------------------- exchange
-  sx = warp_sum(sx);
-  sxx = warp_sum(sxx);
+  const float sx = warp_sum(sx2.x + sx2.y);
+  const float sxx = warp_sum(sxx2.x + sxx2.y);
   ga = warp_sum(ga);
   ge = warp_sum(ge);
   if (lane == 0) {
@@ -375,18 +435,78 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gn_bwd_kernel(const GnAr
   if (timed_out && a.status != nullptr) atomicOr(a.status, kStatusTimeout);
 }
 
-// Persistent, double-buffered form for groups whose slices fit two shared-memory
-// buffers (16-byte aligned groups): cluster c takes groups c, c + #clusters, ...
-// and, while it works on one group, the bulk copies of its next group's slices
-// fill the other buffer; the stores of dx drain behind. One cluster barrier per
-// group (the per-warp sums alternate between two slots) and one block barrier
-// (before the stores); no barrier in pass 1.
+// bounded wait on a local mbarrier whose phase completes on st.async writes of the cluster's CTAs:
+// acquire at cluster scope, so that those writes are visible after it
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const uint32_t ad = smem_u32(bar);
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(ad), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const long long t0 = clock64();
+  while (!try_once()) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+// the shared-memory address of `p` (a local object) in cluster CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// st.async into cluster CTA `rank` at the offset of `dst`, completing its bytes on that CTA's mbarrier
+// at the offset of `bar`
+__device__ __forceinline__ void st_async_f4(const void* dst, const uint64_t* bar, uint32_t rank, float v0, float v1,
+                                            float v2, float v3) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr(dst, rank)),
+               "f"(v0), "f"(v1), "f"(v2), "f"(v3), "r"(cluster_addr(bar, rank))
+               : "memory");
+}
+// The group's coefficients from the per-warp sums every CTA of the cluster pushed into this CTA's
+// slot (xs[rank][warp] = sum(x - K), sum((x - K)^2), sum(gamma dy), sum(gamma dy (x - K))); the same
+// lanes take the same (rank, warp) pairs in the same order in every warp and CTA.
+__device__ __forceinline__ GnCoef slot_coef(const float4 (*xs)[kWarps], const GnArgs& a) {
+  const int lane = threadIdx.x & 31;
+  float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+  for (int p = lane; p < a.S * kWarps; p += 32) {
+    const float4 t = xs[p / kWarps][p % kWarps];
+    v0 += t.x;
+    v1 += t.y;
+    v2 += t.z;
+    v3 += t.w;
+  }
+  return make_coef(warp_sum(v0), warp_sum(v1), warp_sum(v2), warp_sum(v3), a);
+}
+
+// Persistent, double-buffered form for groups whose slices fit two shared-memory buffers (16-byte
+// aligned groups): cluster c takes groups c, c + #clusters, ... (its iterations it = 0, 1, ...), group
+// it in buffer it & 1. While a group is worked on, the bulk copies of the next group fill the other
+// buffer: its dy half at once, its x half once the store of the previous group has read it (the
+// store reads only the x half). The next group's shift K and gammas are loaded during this group and
+// converted after it, so their latency is off the chain. Exchange: every warp pushes its four group
+// sums into slot it & 1 of every CTA of the cluster with st.async; the slot's mbarrier completes when
+// all S x 8 have landed, and each warp forms the coefficients from its own shared memory. A slot is
+// written again (for group it + 2) only after every CTA has pushed group it + 1, which each of its
+// warps does after reading slot it & 1 for group it: two slots suffice.
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a, int64_t items) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t bar[2][kParts];
-  __shared__ float wsum[2][kWarps][4];
+  __shared__ __align__(8) uint64_t bar[2][kParts];  // copies of buffer b landed
+  __shared__ __align__(8) uint64_t xbar[2];         // exchange slot s complete
+  __shared__ __align__(16) float4 xsum[2][kMaxCluster][kWarps];
 
+  // the dgamma/dbeta kernel after this one may be scheduled now: it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const int64_t ncl = gridDim.x / a.S;
@@ -396,55 +516,87 @@ __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a
   const int np = len > 0 ? (len + plen - 1) / plen : 0;
   const int j0 = len > 0 ? static_cast<int>(lo / a.hw) : 0;            // first channel of the slice
   const int64_t jend0 = (static_cast<int64_t>(j0) + 1) * a.hw - lo;     // slice-local end of channel j0
+  const int nch = len > 0 ? static_cast<int>((lo + len - 1) / a.hw) - j0 + 1 : 0;  // channels in the slice
+  const bool gl_ok = nch <= 32;  // their gammas are held one per lane
+  const uint32_t xbytes = static_cast<uint32_t>(a.S * kWarps * sizeof(float4));
   // buffer b: x at smem + 2 b slice, dy at smem + (2 b + 1) slice (elements of T)
   auto xbuf = [&](int b) { return reinterpret_cast<T*>(smem) + 2 * b * a.slice; };
   auto dbuf = [&](int b) { return reinterpret_cast<T*>(smem) + (2 * b + 1) * a.slice; };
   const T* X = static_cast<const T*>(a.x);
   const T* DY = static_cast<const T*>(a.dy);
+  const T* GAM = static_cast<const T*>(a.gamma);
   T* DX = static_cast<T*>(a.dx);
 
   if (tid == 0) {
     for (int b = 0; b < 2; ++b)
       for (int p = 0; p < kParts; ++p) mbar_init(&bar[b][p], 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(&xbar[0], xbytes);  // the first two groups
+    mbar_arrive_expect_tx(&xbar[1], xbytes);
   }
-  __syncthreads();
+  cluster_sync();  // every CTA's barriers are set before a peer writes to them
   uint32_t phase = 0;  // bit b * kParts + p: parity of the next completion of bar[b][p]
   bool timed_out = false;
 
-  auto issue = [&](int64_t item, int b) {  // thread 0: this CTA's slice of group `item` -> buffer b
+  // thread 0: this CTA's slice of group `item` -> buffer b, dy half (with the barriers' expected bytes
+  // for both halves) and x half
+  auto issue_dy = [&](int64_t item, int b) {
     const int64_t off = item * a.m + lo;
     for (int p = 0; p < np; ++p) {
       const int s0 = p * plen, s1 = min(len, s0 + plen);
       const uint32_t bytes = static_cast<uint32_t>((s1 - s0) * static_cast<int>(sizeof(T)));
       mbar_arrive_expect_tx(&bar[b][p], 2 * bytes);
-      bulk_g2s(xbuf(b) + s0, X + off + s0, bytes, &bar[b][p]);
       bulk_g2s(dbuf(b) + s0, DY + off + s0, bytes, &bar[b][p]);
     }
   };
+  auto issue_x = [&](int64_t item, int b) {
+    const int64_t off = item * a.m + lo;
+    for (int p = 0; p < np; ++p) {
+      const int s0 = p * plen, s1 = min(len, s0 + plen);
+      bulk_g2s(xbuf(b) + s0, X + off + s0, static_cast<uint32_t>((s1 - s0) * static_cast<int>(sizeof(T))),
+               &bar[b][p]);
+    }
+  };
+  auto gamma_raw = [&](int64_t item) -> T {  // lane i: gamma of channel j0 + i of group `item`
+    return (GAM != nullptr && gl_ok && lane < nch) ? GAM[(item % a.groups) * a.cg + j0 + lane] : from_f<T>(1.0f);
+  };
 
-  int64_t w = blockIdx.x / a.S;
+  int64_t w = blockIdx.x / a.S;  // this iteration's group
   float K = w < items ? to_f(X[w * a.m]) : 0.0f;
-  if (tid == 0 && w < items) issue(w, 0);
+  float gl = w < items ? to_f(gamma_raw(w)) : 1.0f;
+  if (tid == 0 && w < items) {
+    issue_dy(w, 0);
+    issue_x(w, 0);
+  }
   for (int it = 0; w < items; w += ncl, ++it) {
     const int b = it & 1;
     const int64_t wn = w + ncl;
-    float K_next = 0.0f;
+    // the next group: its shift and gammas now (converted after this group), its copies
+    T k_raw = from_f<T>(0.0f), g_raw = from_f<T>(1.0f);
     if (wn < items) {
-      K_next = to_f(X[wn * a.m]);  // used by the next group: its latency hides behind this one
+      k_raw = X[wn * a.m];
+      g_raw = gamma_raw(wn);
       if (tid == 0) {
-        bulk_wait_read<0>();  // the stores of the previous group have read buffer b ^ 1
-        issue(wn, b ^ 1);
+        issue_dy(wn, b ^ 1);  // the previous group's store reads only the x half of buffer b ^ 1
+        bulk_wait_read<0>();
+        issue_x(wn, b ^ 1);
       }
     }
     T* xs = xbuf(b);
     const T* ds = dbuf(b);
     const int g = static_cast<int>(w % a.groups);
-    const T* gam = a.gamma != nullptr ? static_cast<const T*>(a.gamma) + static_cast<int64_t>(g) * a.cg : nullptr;
+    const T* gam = GAM != nullptr ? GAM + static_cast<int64_t>(g) * a.cg : nullptr;
+    auto gamma_at = [&](int j) -> float {  // the same value in every lane
+      const float v = __shfl_sync(0xffffffffu, gl, (j - j0) & 31);
+      return gam == nullptr ? 1.0f : gl_ok ? v : to_f(gam[j]);
+    };
     float* part = a.part != nullptr ? a.part + (w * a.S + rank) * static_cast<int64_t>(a.cg) * kWarps * 2 : nullptr;
 
     // pass 1 (no block barrier: channel partials are per warp)
-    float sx = 0.f, sxx = 0.f, ga = 0.f, ge = 0.f, sd = 0.f, se = 0.f;
+    float2 sx2 = make_float2(0.f, 0.f), sxx2 = sx2, sd = sx2, se = sx2;
+    float ga = 0.f, ge = 0.f;
     {
       int j = j0;
       int64_t jend = jend0;
@@ -455,10 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a
         const int s1 = min(len, (p + 1) * plen);
         for (int s = p * plen; s < s1;) {
           const int e = static_cast<int>(min(static_cast<int64_t>(s1), jend));
-          acc_range<T, kVec>(xs, ds, s, e, K, sx, sxx, sd, se);
+          acc_range<T, kVec>(xs, ds, s, e, K, sx2, sxx2, sd, se);
           open = true;
           if (e == jend) {
-            close_channel(j, gam, part, sd, se, ga, ge);
+            close_channel(j, gamma_at(j), part, sd, se, ga, ge);
             open = false;
             ++j;
             jend += a.hw;
@@ -466,22 +618,17 @@ __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a
           s = e;
         }
       }
-      if (open) close_channel(j, gam, part, sd, se, ga, ge);
+      if (open) close_channel(j, gamma_at(j), part, sd, se, ga, ge);
     }
 
-    // exchange: one cluster barrier; every warp forms the coefficients itself
-    sx = warp_sum(sx);
-    sxx = warp_sum(sxx);
+    // exchange
+    const float sx = warp_sum(sx2.x + sx2.y), sxx = warp_sum(sxx2.x + sxx2.y);
     ga = warp_sum(ga);
     ge = warp_sum(ge);
-    if (lane == 0) {
-      wsum[b][warp][0] = sx;
-      wsum[b][warp][1] = sxx;
-      wsum[b][warp][2] = ga;
-      wsum[b][warp][3] = ge;
-    }
-    cluster_sync();
-    const GnCoef cf = cluster_coef(wsum[b], a);
+    if (lane < a.S) st_async_f4(&xsum[b][rank][warp], &xbar[b], static_cast<uint32_t>(lane), sx, sxx, ga, ge);
+    if (!mbar_wait_cluster(&xbar[b], static_cast<uint32_t>((it >> 1) & 1))) timed_out = true;
+    if (tid == 0 && wn + ncl < items) mbar_arrive_expect_tx(&xbar[b], xbytes);  // slot b again, for group it + 2
+    const GnCoef cf = slot_coef(xsum[b], a);
     if (a.stats != nullptr && rank == 0 && tid == 0) {
       a.stats[2 * w] = cf.d;
       a.stats[2 * w + 1] = cf.c1;
@@ -491,14 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a
     {
       int j = j0;
       int64_t jend = jend0;
-      float aj = cf.c1 * (gam != nullptr && len > 0 ? to_f(gam[j]) : 1.0f);
+      float aj = cf.c1 * (len > 0 ? gamma_at(j) : 1.0f);
       for (int s = 0; s < len;) {
         const int e = static_cast<int>(min(static_cast<int64_t>(len), jend));
         dx_range<T, kVec>(xs, ds, s, e, K, aj, cf.d, cf.c2, cf.c3);
         if (e == jend) {
           ++j;
           jend += a.hw;
-          if (j < a.cg) aj = cf.c1 * (gam != nullptr ? to_f(gam[j]) : 1.0f);
+          if (j < a.cg) aj = cf.c1 * gamma_at(j);
         }
         s = e;
       }
@@ -509,34 +656,52 @@ __global__ void __launch_bounds__(kThreads, 1) gn_bwd_pipe_kernel(const GnArgs a
         bulk_commit();
       }
     }
-    K = K_next;
+    K = to_f(k_raw);
+    gl = to_f(g_raw);
   }
-  cluster_sync();  // no CTA leaves while a peer may still read its sums
+  cluster_sync();  // no CTA leaves while a peer may still read from or write to it
   if (tid == 0) bulk_wait_read<0>();
   if (timed_out && a.status != nullptr) atomicOr(a.status, kStatusTimeout);
 }
 
-// dgamma_c = sum_n rstd_n sum_k,w (E - d_n D),  dbeta_c = sum_n sum_k,w D over the slices k that hold
-// channel c and the warps w; one warp per channel, a fixed order (bitwise reproducible)
+// dgamma_c = sum_n rstd_n (E_n - d_n D_n),  dbeta_c = sum_n D_n, with D_n, E_n the sums of channel c's
+// partials of sample n over the slices k that hold the channel and the warps w (in fp32, k then w in
+// order); the samples are added in fp64 (lane i takes n = i, i + 32, ..., then the warp adds its lanes
+// in a fixed tree): one warp per channel, bitwise reproducible. Launched as a programmatic dependent
+// of the GroupNorm kernel: griddepcontrol.wait returns once that kernel has completed and its writes
+// are visible (without the launch attribute it returns at once).
+constexpr int kParamThreads = 128;
 template <typename T>
-__global__ void __launch_bounds__(256) gn_param_kernel(const float* __restrict__ stats, const float* __restrict__ part,
-                                                       T* dgamma, T* dbeta, int64_t N, int C, int G, int cg, int S,
-                                                       int64_t hw, int64_t slice) {
+__global__ void __launch_bounds__(kParamThreads) gn_param_kernel(const float* __restrict__ stats,
+                                                                 const float* __restrict__ part, T* dgamma, T* dbeta,
+                                                                 int64_t N, int C, int G, int cg, int S, int64_t hw,
+                                                                 int64_t slice) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (c >= C) return;
   const int g = c / cg, j = c % cg;
   const int64_t k0 = (j * hw) / slice;
   const int64_t k1 = min(static_cast<int64_t>(S - 1), ((j + 1) * hw - 1) / slice);
-  const int64_t per = (k1 - k0 + 1) * kWarps;
   double sb = 0.0, sg = 0.0;
-  for (int64_t t = lane; t < N * per; t += 32) {
-    const int64_t n = t / per, r = t - n * per;
-    const int64_t k = k0 + r / kWarps, w = r % kWarps, grp = n * G + g;
-    const float* p = part + ((((grp * S + k) * cg + j) * kWarps) + w) * 2;
-    const double D = p[0], E = p[1];
-    sb += D;
-    sg += static_cast<double>(stats[2 * grp + 1]) * (E - static_cast<double>(stats[2 * grp]) * D);
+  for (int64_t n = lane; n < N; n += 32) {
+    const int64_t grp = n * G + g;
+    float D = 0.f, E = 0.f;
+    for (int64_t k = k0; k <= k1; ++k) {
+      // the channel's kWarps (sum dy, sum dy (x - K)) pairs of slice k: 16-byte aligned, two per float4
+      const float4* q = reinterpret_cast<const float4*>(part + ((grp * S + k) * cg + j) * kWarps * 2);
+#pragma unroll
+      for (int i = 0; i < kWarps / 2; ++i) {
+        const float4 v = q[i];
+        D += v.x;
+        E += v.y;
+        D += v.z;
+        E += v.w;
+      }
+    }
+    const float2 st = *reinterpret_cast<const float2*>(stats + 2 * grp);  // d, rstd
+    sb += static_cast<double>(D);
+    sg += static_cast<double>(st.y) * (static_cast<double>(E) - static_cast<double>(st.x) * static_cast<double>(D));
   }
   sb = warp_sum(sb);
   sg = warp_sum(sg);
@@ -656,10 +821,18 @@ cudaError_t run(const void* dy, const void* x, const void* gamma, void* dx, void
                               : launch_mode<T, kPlain>(a, N * G, stream);
   if (err != cudaSuccess || !params) return err;
   const int64_t threads = C * 32;
-  gn_param_kernel<T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-      a.stats, a.part, static_cast<T*>(dgamma), static_cast<T*>(dbeta), N, static_cast<int>(C),
-      static_cast<int>(G), a.cg, a.S, HxW, a.slice);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + kParamThreads - 1) / kParamThreads));
+  cfg.blockDim = dim3(kParamThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gn_param_kernel<T>, static_cast<const float*>(a.stats),
+                            static_cast<const float*>(a.part), static_cast<T*>(dgamma), static_cast<T*>(dbeta), N,
+                            static_cast<int>(C), static_cast<int>(G), a.cg, a.S, HxW, a.slice);
 }
 
 }  // namespace
