@@ -172,6 +172,12 @@ def run_ours(args, rank, world):
         from synth import SwigluShape
         shape = SwigluShape(f"pages_M{M}", M, K, N, shape.seed, shape.dist)
     inp = swiglu_inputs(shape, device=dev)
+    # the e2e leg's pinned host buffers, allocated before any other host memory comes and goes
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
+    for k, v in inp.items():
+        host_in[k].copy_(v)
+    host_out = {k: torch.empty(shp, dtype=torch.bfloat16, pin_memory=True)
+                for k, shp in (("dx", (M, K)), ("dw_g", (K, N)), ("dw_fc", (K, N)), ("db_g", (1, N)), ("db_fc", (1, N)))}
     bf = dict(dtype=torch.bfloat16, device=dev)
     dg = torch.empty((M, N), **bf)
     dfc = torch.empty((M, N), **bf)
@@ -454,9 +460,7 @@ def run_ours(args, rank, world):
     # backward from host buffers: chunked over M, copies overlapped with the
     # compute); beside it, the same work as PyTorch copies around the
     # device-resident swiglu_bwd call (copies, then compute, then copies).
-    host_in = {k: v.cpu().pin_memory() for k, v in inp.items()}
     outs = dict(dx=dx, dw_g=dw_g, dw_fc=dw_fc, db_g=db_g, db_fc=db_fc)
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
     ws_host = torch.empty(swg.swiglu_bwd_host_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
