@@ -17,10 +17,12 @@
 //                   instruction per K step computes both products from one
 //                   read of the x tile
 //   warps 2-5       epilogue: drain the finished buffer while the tensor core
-//                   fills the other one: bias, SiLU, and per 32x32 block one
-//                   TMA store per output from a 64-byte-swizzled staging
-//                   buffer (the copy engine clips rows beyond M and columns
-//                   beyond N)
+//                   fills the other one: bias (the tile's columns staged once
+//                   per tile in shared memory), SiLU, and per 32x32 block a
+//                   64-byte-swizzled staging buffer that the warp reads back
+//                   row-wise and stores with coalesced 16-byte global stores
+//                   (eight whole 64-byte row segments per instruction; rows
+//                   beyond M and columns beyond N are not written)
 // The CTA loops over output tiles [128 rows x 128 columns]; with K = 512 a
 // tile holds only eight K blocks, so the double-buffered accumulator is what
 // keeps the tensor core busy across tile boundaries.
@@ -47,6 +49,7 @@ struct __align__(1024) FwdSmem {
   uint8_t a[STAGES][A_BYTES];
   uint8_t b[STAGES][B_BYTES];
   uint8_t stage[kEpiThreads / 32][3][2048];  // per epilogue warp: g, fc, y blocks [32 rows x 32 columns]
+  uint4 bias[kEpiThreads / 32][2][16];       // per epilogue warp: the tile's b_g, b_fc columns (8 per uint4)
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];   // the tile's MMAs into this buffer are done
@@ -60,6 +63,7 @@ struct FwdArgs {
   int M, K, N;
   uint32_t* status;
   const uint16_t* bias[2]; // b_g, b_fc [N] or null
+  uint16_t* out[3];        // g, fc, y [M, N]
   int tiles, tiles_n, nkb;
 };
 
@@ -68,6 +72,16 @@ __device__ __forceinline__ void fwd_timeout(FwdSmem& s, uint32_t* status) {
   s.abort_flag = 1u;
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void stg128(uint16_t* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -75,9 +89,7 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
-               const __grid_constant__ CUtensorMap tm_wfc, const __grid_constant__ CUtensorMap tm_g,
-               const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_y,
-               const FwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_wfc, const FwdArgs args) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& s = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -98,9 +110,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_wg);
     tma_prefetch_desc(&tm_wfc);
-    tma_prefetch_desc(&tm_g);
-    tma_prefetch_desc(&tm_fc);
-    tma_prefetch_desc(&tm_y);
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -178,11 +187,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
-    bool dead = false, staged = false;
+    bool dead = false;
     uint32_t it = 0;
     for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++it) {
       const uint32_t buf = it & 1;
       const int n0 = (t % args.tiles_n) * BN, m0 = (t / args.tiles_n) * BM;
+      {
+        // the tile's biases: lane l < 16 loads b_g columns n0 + 8l .. n0 + 8l + 7, lane 16 + l the same of b_fc
+        // (zeros beyond N, where the store clips); read back below as warp-wide broadcasts
+        const int which = lane >> 4, cb = n0 + 8 * (lane & 15);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        const uint16_t* bp = which ? args.bias[1] : args.bias[0];
+        if (cb < args.N && bp != nullptr) v = __ldg(reinterpret_cast<const uint4*>(bp + cb));
+        __syncwarp();  // every lane has read the previous tile's biases
+        s.bias[warp - 2][which][lane & 15] = v;
+        __syncwarp();
+      }
       bool ready = false;
       if (!dead && !s.abort_flag) {
         ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1);
@@ -203,17 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(d + BN + c * 32, vf);
           tmem_ld_wait();
           const int col = n0 + c * 32;
-          if (staged) {
-            if (lane == 0) bulk_wait_read<0>();  // the previous stores have read the staging buffers
-            __syncwarp();
-          }
+          uint4 rg[4], rf[4], ry[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            uint4 bgv = make_uint4(0u, 0u, 0u, 0u), bfv = make_uint4(0u, 0u, 0u, 0u);
-            if (col + 8 * j < args.N) {  // columns beyond N: zeros, clipped by the store
-              if (args.bias[0] != nullptr) bgv = __ldg(reinterpret_cast<const uint4*>(args.bias[0] + col + 8 * j));
-              if (args.bias[1] != nullptr) bfv = __ldg(reinterpret_cast<const uint4*>(args.bias[1] + col + 8 * j));
-            }
+            const uint4 bgv = s.bias[warp - 2][0][c * 4 + j], bfv = s.bias[warp - 2][1][c * 4 + j];
             const uint32_t bgw[4] = {bgv.x, bgv.y, bgv.z, bgv.w};
             const uint32_t bfw[4] = {bfv.x, bfv.y, bfv.z, bfv.w};
             uint32_t og[4], of[4], oy[4];
@@ -230,27 +243,44 @@ __global__ void __launch_bounds__(kThreads, 1)
               of[e] = pack_bf16x2(f2.x, f2.y);
               oy[e] = pack_bf16x2(y2.x, y2.y);
             }
+            rg[j] = make_uint4(og[0], og[1], og[2], og[3]);
+            rf[j] = make_uint4(of[0], of[1], of[2], of[3]);
+            ry[j] = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+          }
+          __syncwarp();  // every lane has read the previous chunk back from the staging buffers
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
             // this lane's row of each 32x32 block, 64-byte swizzle: 16-byte chunk j ^ ((row >> 1) & 3)
             const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
-            sts128(stg + off, make_uint4(og[0], og[1], og[2], og[3]));
-            sts128(stg + 2048 + off, make_uint4(of[0], of[1], of[2], of[3]));
-            sts128(stg + 4096 + off, make_uint4(oy[0], oy[1], oy[2], oy[3]));
+            sts128(stg + off, rg[j]);
+            sts128(stg + 2048 + off, rf[j]);
+            sts128(stg + 4096 + off, ry[j]);
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_g, s.stage[warp - 2][0], col, m0 + q * 32);
-            tma_store_2d(&tm_fc, s.stage[warp - 2][1], col, m0 + q * 32);
-            tma_store_2d(&tm_y, s.stage[warp - 2][2], col, m0 + q * 32);
-            bulk_commit();
+          // read the blocks back row-wise and store them coalesced: lane l takes the 16-byte chunk l & 3 of
+          // rows (l >> 2) + 8 i, so that each store writes eight whole 64-byte row segments
+          {
+            const int k = lane & 3;
+            const bool col_ok = col + 8 * k < args.N;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i;
+              const int row = m0 + q * 32 + r;
+              const uint32_t off = r * 64 + ((k ^ ((r >> 1) & 3)) << 4);
+              const uint4 vg = lds128(stg + off), vf = lds128(stg + 2048 + off), vy = lds128(stg + 4096 + off);
+              if (row < args.M && col_ok) {
+                const size_t o = static_cast<size_t>(row) * args.N + col + 8 * k;
+                stg128(args.out[0] + o, vg);
+                stg128(args.out[1] + o, vf);
+                stg128(args.out[2] + o, vy);
+              }
+            }
           }
-          staged = true;
         }
       }
       tc_fence_before();
       mbar_arrive(&s.tmem_empty[buf]);  // this thread has read its rows of the buffer
     }
-    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
   }
 
   __syncthreads();
@@ -271,12 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16_t* w_fc, const uint16_t* b_g,
                             const uint16_t* b_fc, uint16_t* g, uint16_t* fc, uint16_t* y, int64_t M, int64_t K,
                             int64_t N, cudaStream_t stream) {
-  CUtensorMap mx, mwg, mwfc, mg, mfc, my;
+  CUtensorMap mx, mwg, mwfc;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mx, x, K, M, static_cast<uint64_t>(K) * 2, BK, BM) ||
-      !encode_tmap_2d_bf16(&mwg, w_g, N, K, rs, 64, BK) || !encode_tmap_2d_bf16(&mwfc, w_fc, N, K, rs, 64, BK) ||
-      !encode_tmap_2d_bf16(&mg, g, N, M, rs, 32, 32, 64) || !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 32, 32, 64) ||
-      !encode_tmap_2d_bf16(&my, y, N, M, rs, 32, 32, 64))
+      !encode_tmap_2d_bf16(&mwg, w_g, N, K, rs, 64, BK) || !encode_tmap_2d_bf16(&mwfc, w_fc, N, K, rs, 64, BK))
     return cudaErrorInvalidValue;
   FwdArgs a{};
   a.M = static_cast<int>(M);
@@ -285,6 +313,9 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   a.status = status_word_ptr();
   a.bias[0] = b_g;
   a.bias[1] = b_fc;
+  a.out[0] = g;
+  a.out[1] = fc;
+  a.out[2] = y;
   a.tiles_n = static_cast<int>((N + BN - 1) / BN);
   a.tiles = static_cast<int>(((M + BM - 1) / BM) * a.tiles_n);
   a.nkb = static_cast<int>((K + BK - 1) / BK);
@@ -295,7 +326,7 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   if (e != cudaSuccess) return e;
   int grid = device_sm_count();
   if (grid > a.tiles) grid = a.tiles;
-  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mx, mwg, mwfc, mg, mfc, my, a);
+  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mx, mwg, mwfc, a);
   return cudaGetLastError();
 }
 
