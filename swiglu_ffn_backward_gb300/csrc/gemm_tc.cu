@@ -11,11 +11,14 @@
 // bf16 operands, fp32 accumulation in TMEM, one bf16 rounding per output
 // ("Dtype conversion flow": matmul accumulates in fp32).
 //
-// CTA = 6 warps: warp 0 lane 0 issues TMA loads into a STAGES-deep ring of
-// shared-memory operand tiles; warp 1 owns the TMEM allocation and lane 0
-// issues tcgen05.mma (M=128, N=256, K=16 per instruction) and tcgen05.commit;
-// warps 2-5 read the 128x256 fp32 accumulator out of TMEM (each warp its own
-// 32-lane quarter) and store bf16 (or fp32 partials).
+// Persistent: one CTA per SM (6 warps) walks the tiles t, t + #CTAs, ... in an
+// order that keeps the tiles in flight on shared operands (w_tile). Warp 0 lane 0
+// issues TMA loads into a STAGES-deep ring of shared-memory operand tiles that
+// runs across tiles; warp 1 owns the TMEM allocation (two 256-column accumulator
+// buffers) and lane 0 issues tcgen05.mma (M=128, N=256, K=16 per instruction) and
+// tcgen05.commit; warps 2-5 read a finished 128x256 fp32 accumulator out of TMEM
+// (each warp its own 32-lane quarter) and store bf16 (or fp32 partials) while the
+// tensor core fills the other buffer.
 //
 // Operand layouts (shared memory, 128-byte swizzle, written by TMA), MN-major:
 // the reduction index m is the strided one. A tile = x[m0:m0+64, k0:k0+128] as
@@ -46,7 +49,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 512;  // two accumulator buffers of 256 columns
 
 enum Mode : int { kModeW = 1 };
 
@@ -55,7 +59,8 @@ struct __align__(1024) Smem {
   uint8_t b[STAGES][B_BYTES];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t accum;
+  uint64_t tmem_full[2];   // the tile's MMAs into this buffer are done
+  uint64_t tmem_empty[2];  // the epilogue has read this buffer out
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   volatile uint32_t issued;
@@ -69,6 +74,7 @@ struct GemmArgs {
   float* ws;
   int splits, kb_per, nkb_total;
   int tiles_kw, tiles_nw;  // dw tile grid per problem
+  int tiles;               // splits x 2 x tiles_kw x tiles_nw
   int accumulate;          // dw += this call's sums (one rounding of old + new)
 };
 
@@ -77,6 +83,37 @@ __device__ __forceinline__ void flag_timeout(Smem& s) {
   s.abort_flag = 1u;
 }
 
+struct WTile {
+  int split, prob, m0, n0, kb_begin, nkb;
+};
+
+// Tile t's coordinates. CTAs that run at the same time should share operands: within a (split,
+// problem) the dw column tiles go in groups of kGroupN, and inside a group the column index runs
+// fastest and the row index next, so the ~150 tiles in flight read about kGroupN dg column blocks
+// (each shared by every row tile among them) and a band of x column blocks (each shared by the
+// group's columns). With the column index fastest over all of N instead, every wave streamed all of
+// dg (at M = 16384, K = 4096, N = 14336: 15.8 GB read from DRAM per launch for 1.1 GB of inputs).
+__device__ __forceinline__ WTile w_tile(int t, const GemmArgs& args) {
+  constexpr int kGroupN = 8;
+  const int per_prob = args.tiles_kw * args.tiles_nw;
+  WTile w;
+  w.split = t / (2 * per_prob);
+  t -= w.split * 2 * per_prob;
+  w.prob = t / per_prob;
+  t -= w.prob * per_prob;
+  const int grp = t / (args.tiles_kw * kGroupN);
+  const int gsize = min(kGroupN, args.tiles_nw - grp * kGroupN);
+  const int within = t - grp * args.tiles_kw * kGroupN;
+  w.m0 = (within / gsize) * BM;                      // dw rows (index k)
+  w.n0 = (grp * kGroupN + within % gsize) * BN;      // dw columns (index n)
+  w.kb_begin = w.split * args.kb_per;
+  w.nkb = min(args.nkb_total, w.kb_begin + args.kb_per) - w.kb_begin;
+  return w;
+}
+
+// Persistent: one CTA per SM walks tiles t, t + #CTAs, ...; the accumulator is
+// double-buffered in TMEM (2 x 256 columns), so a tile's epilogue runs while the
+// tensor core accumulates the next one, and the operand ring runs across tiles.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -87,26 +124,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- tile coordinates
-  int t = blockIdx.x;
-  const int nt = t % args.tiles_nw;
-  t /= args.tiles_nw;
-  const int kt = t % args.tiles_kw;
-  t /= args.tiles_kw;
-  const int prob = t % 2;
-  const int split = t / 2;
-  const int m0 = kt * BM;  // dw rows (index k)
-  const int n0 = nt * BN;  // dw columns (index n)
-  const int kb_begin = split * args.kb_per;
-  const int kb_end = min(args.nkb_total, kb_begin + args.kb_per);
-  const int nkb = kb_end - kb_begin;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
-    mbar_init(&s.accum, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tmem_full[i], 1);
+      mbar_init(&s.tmem_empty[i], kEpiThreads);
+    }
     s.abort_flag = 0u;
     s.issued = 0u;
     s.consumed = 0u;
@@ -125,70 +151,108 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    uint32_t issued = 0;
-    for (int i = 0; i < nkb; ++i) {
-      const int st = i % STAGES;
-      const int use = i / STAGES;
-      if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1)) {
-        flag_timeout(s);
-        break;
-      }
-      if (s.abort_flag) break;
-      mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
-      const int mr = (kb_begin + i) * BK;  // reduction rows of M
-      tma_load_2d(s.a[st], &tmA0, &s.full[st], m0, mr);
-      tma_load_2d(s.a[st] + 8192, &tmA0, &s.full[st], m0 + 64, mr);
-      const CUtensorMap* tb = prob ? &tmB1 : &tmB0;
+    if (lane == 0) {
+      uint32_t gj = 0;  // ring entries issued, over all tiles
+      bool stop = false;
+      for (int t = blockIdx.x; t < args.tiles && !stop; t += gridDim.x) {
+        const WTile w = w_tile(t, args);
+        const CUtensorMap* tb = w.prob ? &tmB1 : &tmB0;
+        for (int i = 0; i < w.nkb; ++i, ++gj) {
+          const int st = gj % STAGES;
+          if (gj >= STAGES && !mbar_wait(&s.empty[st], ((gj / STAGES) - 1) & 1)) {
+            flag_timeout(s);
+            stop = true;
+            break;
+          }
+          if (s.abort_flag) {
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+          const int mr = (w.kb_begin + i) * BK;  // reduction rows of M
+          tma_load_2d(s.a[st], &tmA0, &s.full[st], w.m0, mr);
+          tma_load_2d(s.a[st] + 8192, &tmA0, &s.full[st], w.m0 + 64, mr);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tma_load_2d(s.b[st] + j * 8192, tb, &s.full[st], n0 + 64 * j, mr);
-      issued = i + 1;
-      s.issued = issued;
+          for (int j = 0; j < 4; ++j) tma_load_2d(s.b[st] + j * 8192, tb, &s.full[st], w.n0 + 64 * j, mr);
+          s.issued = gj + 1;
+        }
+      }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 1, 1);  // both operands MN-major
-    for (int i = 0; i < nkb; ++i) {
-      const int st = i % STAGES;
-      if (!mbar_wait(&s.full[st], (i / STAGES) & 1)) {
-        flag_timeout(s);
-        break;
-      }
-      s.consumed = i + 1;
-      tc_fence_after();
-      const uint32_t a_addr = smem_u32(s.a[st]);
-      const uint32_t b_addr = smem_u32(s.b[st]);
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 1, 1);  // both operands MN-major
+      uint32_t gj = 0, it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++it) {
+        const WTile w = w_tile(t, args);
+        const uint32_t buf = it & 1;
+        if (it >= 2) {
+          // the epilogue has read this buffer's previous tile out
+          if (!mbar_wait(&s.tmem_empty[buf], ((it >> 1) - 1) & 1)) {
+            flag_timeout(s);
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t d = tmem + buf * BN;
+        for (int i = 0; i < w.nkb; ++i, ++gj) {
+          const int st = gj % STAGES;
+          if (!mbar_wait(&s.full[st], (gj / STAGES) & 1)) {
+            flag_timeout(s);
+            ok = false;
+            break;
+          }
+          s.consumed = gj + 1;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(s.a[st]);
+          const uint32_t b_addr = smem_u32(s.b[st]);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k)
-        umma_bf16(tmem, smem_desc(a_addr + 2048 * k, 8192, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024), idesc,
-                  (i > 0 || k > 0) ? 1u : 0u);
-      umma_commit(&s.empty[st]);
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d, smem_desc(a_addr + 2048 * k, 8192, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024),
+                      idesc, (i > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&s.empty[st]);
+        }
+        umma_commit(&s.tmem_full[buf]);  // committed even after a timeout: the epilogue stops waiting
+      }
+      // after a timeout the epilogue may have stopped waiting: see every MMA this thread
+      // issued complete before TMEM is freed (the buffer of tile it - 1 was committed last)
+      if (s.abort_flag && it > 0) mbar_wait(&s.tmem_full[(it - 1) & 1], ((it - 1) >> 1) & 1);
     }
-    umma_commit(&s.accum);
-    // after a timeout the epilogue may have stopped waiting: see every MMA this thread
-    // issued complete before the CTA frees TMEM
-    if (s.abort_flag) mbar_wait(&s.accum, 0);
-  } else if (warp >= 2) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const bool ok = mbar_wait(&s.accum, 0);
-    if (!ok) flag_timeout(s);
-    tc_fence_after();
-    const int r = q * 32 + lane;  // accumulator row
-    // tcgen05.ld is warp-collective: decide for the whole warp
-    if (__all_sync(0xffffffffu, ok && !s.abort_flag && nkb > 0)) {
+    bool dead = false;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++it) {
+      const WTile w = w_tile(t, args);
+      const uint32_t buf = it & 1;
+      bool ready = false;
+      if (!dead && !s.abort_flag) {
+        ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1);
+        if (!ready) {
+          flag_timeout(s);
+          dead = true;
+        }
+      }
+      tc_fence_after();
+      const int r = q * 32 + lane;  // accumulator row
+      // tcgen05.ld is warp-collective: decide for the whole warp
+      if (__all_sync(0xffffffffu, ready && !s.abort_flag && w.nkb > 0)) {
+        const uint32_t d = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
-        tmem_ld_wait();
-        const int row = m0 + r;
-        const int col = n0 + c * 32;
-        {
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(d + c * 32, v);
+          tmem_ld_wait();
+          const int row = w.m0 + r;
+          const int col = w.n0 + c * 32;
           if (row < args.K) {
             if (args.splits == 1) {
-              uint4* dst = reinterpret_cast<uint4*>(args.dw[prob] + static_cast<int64_t>(row) * args.N + col);
+              uint16_t* dwp = w.prob ? args.dw[1] : args.dw[0];
+              uint4* dst = reinterpret_cast<uint4*>(dwp + static_cast<int64_t>(row) * args.N + col);
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 if (col + 8 * j < args.N) {
@@ -206,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             } else {
-              float* dst = args.ws + (static_cast<int64_t>(split * 2 + prob) * args.K + row) * args.N + col;
+              float* dst = args.ws + (static_cast<int64_t>(w.split * 2 + w.prob) * args.K + row) * args.N + col;
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 if (col + 4 * j < args.N) {
@@ -217,8 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&s.tmem_empty[buf]);  // this thread has read its rows of the buffer
     }
-    tc_fence_before();
   }
 
   __syncthreads();
@@ -365,10 +430,13 @@ cudaError_t launch_w_gemm(const uint16_t* x, const uint16_t* dg, const uint16_t*
   a.tiles_kw = static_cast<int>((K + BM - 1) / BM);
   a.tiles_nw = static_cast<int>((N + BN - 1) / BN);
   a.accumulate = accumulate ? 1 : 0;
-  const int64_t ctas = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
+  const int64_t tiles = static_cast<int64_t>(plan.splits) * 2 * a.tiles_kw * a.tiles_nw;
+  a.tiles = static_cast<int>(tiles);
   cudaError_t e = prepare_kernel<kModeW>();
   if (e != cudaSuccess) return e;
-  tc_gemm_kernel<kModeW><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(a0, a0, b0, b1, a);
+  int64_t grid = device_sm_count();
+  if (grid > tiles) grid = tiles;
+  tc_gemm_kernel<kModeW><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a0, a0, b0, b1, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.splits == 1) return e;
   return launch_w_split_reduce(static_cast<const float*>(ws), plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
