@@ -246,7 +246,8 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc,
  * db_fc; dg and dfc are not produced) with every tensor argument in HOST
  * memory, same shapes and layouts as swiglu_bwd. Page-locked host buffers
  * (cudaHostAlloc / cudaHostRegister) let the copies overlap: M is cut into
- * chunks of about 32768 rows; while one chunk is computed, the next chunk's
+ * chunks of 32768 rows or more and a short last one (at least 16384 rows);
+ * while one chunk is computed, the next chunk's
  * rows are copied in and the previous chunk's dx is copied out, on two
  * internal streams ordered against `stream` with events. dw and db are
  * reduced once over every chunk's fp32 partials (one rounding, as in

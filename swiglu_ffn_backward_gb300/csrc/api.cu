@@ -388,8 +388,8 @@ swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, cons
 }
 
 // ---------------------------------------------------------------- whole backward from host buffers
-// The fused backward with every tensor in host memory. M is cut into chunks of
-// at least kHostChunkRows rows; while chunk c is computed (dx, and the fused w
+// The fused backward with every tensor in host memory. M is cut into chunks
+// (equal ones, then a short last one); while chunk c is computed (dx, and the fused w
 // stage's fp32 split partials into chunk c's own slots), chunk c + 1's rows are
 // copied in on one internal stream and chunk c - 1's dx is copied out on
 // another, each chunk's device buffers alternating between two sets. One
@@ -402,6 +402,7 @@ swg_status swiglu_bwd_w_fused(const void* x, const void* dy, const void* g, cons
 namespace {
 
 constexpr int64_t kHostChunkRows = 32768;
+constexpr int64_t kMinLastRows = 16384;
 
 struct HostPlan {
   int64_t chunks, rows;  // chunk count, rows per chunk (multiple of 64; the last may be shorter)
@@ -411,10 +412,12 @@ struct HostPlan {
 
 HostPlan host_plan(int64_t M, int64_t K, int64_t N, int sms) {
   HostPlan p{};
-  // floor(M / kHostChunkRows) chunks (at most 256) of equal 64-row multiples: every chunk, the last
-  // included, keeps at least 16K rows, so each one splits over M (its partials path needs two splits)
+  // floor(M / kHostChunkRows) chunks (at most 256): all but the last of one 64-row multiple, the
+  // last as short as allowed (kMinLastRows to kMinLastRows + 64 (chunks - 1) rows), so that little
+  // compute and dx copy-out is left after the last rows have come in. Every chunk keeps at least 16K
+  // rows, so each one splits over M (its partials path needs two splits).
   p.chunks = M >= 2 * kHostChunkRows ? std::min<int64_t>(M / kHostChunkRows, 256) : (M > 0 ? 1 : 0);
-  p.rows = p.chunks > 0 ? (((M + p.chunks - 1) / p.chunks) + 63) / 64 * 64 : 0;
+  p.rows = p.chunks > 1 ? (M - kMinLastRows) / (p.chunks - 1) / 64 * 64 : (M + 63) / 64 * 64;
   size_t off = 0;
   p.off_w = off;
   off += align256(static_cast<size_t>(2 * K * N) * 2);

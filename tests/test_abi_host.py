@@ -261,10 +261,11 @@ def test_host_path_workspace_follows_the_chunk_plan(swg, M):
     # outputs | partials of every chunk (or the fused w stage's own workspace for one chunk)
     K, N, sms = 512, 1024, 148
     chunks = min(M // 32768, 256) if M >= 65536 else (1 if M > 0 else 0)
-    rows = ((((M + chunks - 1) // chunks) + 63) // 64) * 64 if chunks else 0
+    # equal chunks of a 64-row multiple, then the shortest last chunk the partials path allows
+    rows = (M - 16384) // (chunks - 1) // 64 * 64 if chunks > 1 else (M + 63) // 64 * 64
     if chunks > 1:
         last = M - (chunks - 1) * rows
-        assert 16384 <= last <= rows  # every chunk splits over M
+        assert 16384 <= last <= min(rows, 16384 + 64 * (chunks - 1))  # every chunk splits over M
     total = _al256(2 * K * N * 2) + 2 * _al256(rows * (K + 3 * N) * 2) + 2 * _al256(rows * K * 2)
     total += _al256((2 * K * N + 2 * N) * 2)
     if chunks > 1:

@@ -10,6 +10,7 @@ first failure has already run every other test; it also passes on its own.
 import pytest
 import torch
 
+import oracle
 from synth import SWIGLU_CONFIGS, swiglu_inputs
 
 from ._parity import assert_all, compare, to_f64
@@ -27,7 +28,8 @@ def test_noalloc_rejects_shapes_beyond_the_array():
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice():
-    """Two calls in a row, on different inputs and sizes, each against swiglu_bwd_b."""
+    """Two calls in a row, on different inputs and sizes, each against the fp64 oracle's b stage and
+    bit for bit against swiglu_bwd_b."""
     import swiglu_ffn_backward_gb300 as swg
     for shape in (SWIGLU_CONFIGS["tail"][3], SWIGLU_CONFIGS["tail"][2]):  # M=4097, then M=1025
         inp = swiglu_inputs(shape, device="cuda")
@@ -35,7 +37,8 @@ def test_noalloc_matches_workspace_entry_point_twice():
         got = swg.swiglu_bwd_b_noalloc(inp["dy"], inp["g"], inp["fc"])
         swg.swg_check()
         names = ("dg", "dfc", "db_g", "db_fc")
-        assert_all([compare(n, gt, to_f64(rf)) for n, gt, rf in zip(names, got, ref)])
+        expect = oracle.swiglu_bwd_b(to_f64(inp["dy"]), to_f64(inp["g"]), to_f64(inp["fc"]))
+        assert_all([compare(n, gt, ex) for n, gt, ex in zip(names, got, expect)])
         for gt, rf in zip(got, ref):  # same kernel, same plan: the same bits
             assert torch.equal(gt, rf)
 
