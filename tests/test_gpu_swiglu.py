@@ -241,3 +241,28 @@ def test_auto_chain_is_the_chosen_chain(shape):
     swg.swg_check()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.gpu
+def test_w_stage_many_tiles_per_cta():
+    """The w GEMM with more dw tiles than CTAs (K = 2048, N = 2560: 2 x 16 x 10 = 320 tiles of 128 x 256
+    and no M split at M = 384): each persistent CTA takes two or three tiles through both TMEM
+    accumulators, and the column tiles form a group of eight and a short group of two. Against the
+    w-stage oracle on the GPU's own dg, dfc, then once more in accumulate mode on top of the result."""
+    swg = _swg()
+    shape = SwigluShape("w_many_tiles", 384, 2048, 2560, 7, "tail")
+    inp = swiglu_inputs(shape, device="cuda")
+    dg, dfc, _, _ = swg.swiglu_bwd_b(inp["dy"], inp["g"], inp["fc"])
+    dw_g, dw_fc = swg.swiglu_bwd_w(inp["x"], dg, dfc)
+    swg.swg_check()
+    h = _np(inp)
+    rdwg, rdwfc = oracle.swiglu_bwd_w(h["x"], to_f64(dg), to_f64(dfc))
+    assert_all([compare("dw_g", dw_g, rdwg), compare("dw_fc", dw_fc, rdwfc)])
+    # the same call through swiglu_bwd's accumulate mode adds a second copy of the sums onto dw
+    outs = swg.swiglu_bwd(**inp, fused=False)
+    base = {k: v.clone() for k, v in outs.items()}
+    swg.swiglu_bwd(**inp, fused=False, accumulate=True, out=outs)
+    swg.swg_check()
+    for k in ("dw_g", "dw_fc"):
+        ref = 2.0 * to_f64(base[k])
+        assert_all([compare(k, outs[k], ref)])
