@@ -37,7 +37,9 @@
 //   stacks 64 columns of dg over the same 64 columns of dfc (MN-major; the two
 //   8 KB halves of a slot are the two 64-element MN chunks, LBO = 8 KB), so one
 //   accumulator pair holds both outputs for all k. Stages of 64 rows of m;
-//   B = x [64 m x 256 k] (MN-major, four 64 x 64 boxes). The CTA owns a fixed
+//   B = x [64 m x 256 k] per accumulator half (MN-major, four 64 x 64 boxes),
+//   one 64 KB ring entry per stage holding both halves, so the MMA issuer
+//   checks one x barrier and one A barrier per eight MMAs. The CTA owns a fixed
 //   band of 64 columns for its whole M range, so it also sums dg, dfc over its
 //   rows in registers (db column partials, one row per M split). The reduction
 //   over M is split into S chunks with fp32 partials and a fixed-order reduce.
@@ -75,9 +77,9 @@ struct Cfg<kFX> {
 template <>
 struct Cfg<kFW> {
   static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
-  static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
-  static constexpr int kEntryBytes = 32768;  // x [64 m x 256 k]
-  static constexpr int kEntries = 5;
+  static constexpr int kAStages = 2;       // A-operand slots (dg | dfc stacked, 16 KB each)
+  static constexpr int kEntryBytes = 65536;  // x [64 m x 512 k]: one stage, both accumulator halves
+  static constexpr int kEntries = 3;
   static constexpr int kPrefetch = 4;
 };
 
@@ -149,7 +151,7 @@ __device__ __forceinline__ Tile tile_of(int ct, const FusedArgs& args) {
   }
   t.k0 = t.kt * 512;
   t.nh = (args.K - t.k0) > 256 ? 2 : 1;             // 256-column accumulator halves in use
-  t.eps = (MODE == kFX) ? 2 * t.nh : t.nh;          // ring entries per stage
+  t.eps = (MODE == kFX) ? 2 * t.nh : 1;             // ring entries per stage
   return t;
 }
 
@@ -302,18 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(&s.ring_full[e], C::kEntryBytes);
+          // FW: one 32 KB half per accumulator half in use
+          mbar_arrive_expect_tx(&s.ring_full[e], MODE == kFX ? C::kEntryBytes : tl.nh * 32768u);
           if (MODE == kFX) {
             const EntryPos ep = fx_entry(tl, j);
             tma_load_2d(s.ring[e], ep.p ? &tm_b1 : &tm_b0, &s.ring_full[e], ep.i * 64, tl.k0 + 256 * ep.h);
           } else {
-            const int i = j / tl.eps, h = j % tl.eps;
-            const int mrow = (tl.kb_begin + i) * 64;
-            const int kk = tl.k0 + 256 * h;
-            // four 64 x 64 boxes: the entry's 64-column MN chunks (columns past K read as zeros)
+            const int mrow = (tl.kb_begin + j) * 64;
+            // per accumulator half, four 64 x 64 boxes: 64-column MN chunks (columns past K read as zeros)
+            for (int h = 0; h < tl.nh; ++h)
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb)
-              tma_load_2d(s.ring[e] + cb * 8192, &tm_b0, &s.ring_full[e], kk + 64 * cb, mrow);
+              for (int cb = 0; cb < 4; ++cb)
+                tma_load_2d(s.ring[e] + h * 32768 + cb * 8192, &tm_b0, &s.ring_full[e], tl.k0 + 256 * h + 64 * cb,
+                            mrow);
           }
           s.ring_issued = gj + 1;
         }
@@ -325,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, MODE == kFW, MODE == kFW);
       uint32_t gi = 0, gj = 0, tt = 0;  // A stages, ring entries, tiles consumed
       bool ok = true;
-      // the MMAs of ring entry gj: stage i of the tile (A slot gi + i), product p, accumulator half h
+      // the MMAs of ring entry gj: stage i of the tile (A slot gi + i); FX: product p, accumulator
+      // half h; FW: both products at once, h = the accumulator halves in use
       auto consume = [&](int i, int p, int h) -> bool {
         const int e = gj % kRE;
         if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
@@ -343,10 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 32 * k, 16, 1024),
                       idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
         } else {
+          for (int hh = 0; hh < h; ++hh)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + h * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
-                      smem_desc(b_addr + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(tmem + hh * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
+                        smem_desc(b_addr + hh * 32768 + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&s.ring_empty[e]);
         ++gj;
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_free(0) || !wait_free(1)) break;
           for (int i = 0; i < tl.nst && ok; ++i) {
             ok = wait_a(i);
-            for (int h = 0; h < tl.eps && ok; ++h) ok = consume(i, 0, h);
+            if (ok) ok = consume(i, 0, tl.nh);
             umma_commit(&s.a_empty[(gi + i) % kAS]);
           }
         }
