@@ -537,19 +537,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 8; ++e) ug[e] = uf[e] = 0.0f;
       uint4 zdy[kRPT], zg[kRPT], zfc[kRPT];
 
-      auto load = [&](int st, uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
-        const bool valid = st < total;
-        const int m0 = valid ? tile_at(st / nst).m0 : 0;
-        load_rows(m0, (valid ? (st % nst) * 64 : 0) + c * 8, valid, bdy, bg, bfc);
+      // a position in the CTA's stage stream: stage index, stage within its tile, tile index,
+      // and the tile's first row and K block, advanced without divisions
+      struct Cur {
+        int st, sit, tix, m0, kt;
       };
-      auto process = [&](int st, const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
+      auto advance = [&](Cur& p) {
+        ++p.st;
+        if (++p.sit == nst) {
+          p.sit = 0;
+          ++p.tix;
+          if (p.st < total) {
+            const Tile tl = tile_at(p.tix);
+            p.m0 = tl.m0;
+            p.kt = tl.kt;
+          }
+        }
+      };
+      const Tile tl0 = tile_at(0);
+      Cur lc{0, 0, 0, tl0.m0, tl0.kt};  // the next stage to load
+      Cur pc = lc;                       // the next stage to transform
+      auto load = [&](uint4 (&bdy)[kRPT], uint4 (&bg)[kRPT], uint4 (&bfc)[kRPT]) {
+        const bool valid = lc.st < total;
+        load_rows(valid ? lc.m0 : 0, (valid ? lc.sit * 64 : 0) + c * 8, valid, bdy, bg, bfc);
+        advance(lc);
+      };
+      auto process = [&](const uint4 (&bdy)[kRPT], const uint4 (&bg)[kRPT], const uint4 (&bfc)[kRPT]) {
+        const int st = pc.st;
         const int a = st % kAS;
         acquire_slot(static_cast<uint32_t>(st), a);
-        if (!dead) {
-          const Tile tl = tile_at(st / nst);
-          store_stage(a, tl.m0, (st % nst) * 64 + c * 8, tl.kt == 0 && args.dg_out != nullptr, bdy, bg, bfc, ug,
-                      uf);
-        }
+        if (!dead)
+          store_stage(a, pc.m0, pc.sit * 64 + c * 8, pc.kt == 0 && args.dg_out != nullptr, bdy, bg, bfc, ug, uf);
         warp_arrive(&s.a_full[a]);
         if (t == 0) s.x_progress = static_cast<uint32_t>(st + 1);
       };
@@ -601,27 +619,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait_read<0>();
         named_sync_transform();
       };
-      auto after = [&](int st) {
-        const int tix = st / nst;
-        if (tix >= 1 && st % nst + 1 == look) epilogue(tix - 1, (tix * nst - 1) % kAS);
+      auto after = [&]() {
+        if (pc.tix >= 1 && pc.sit + 1 == look) epilogue(pc.tix - 1, (pc.tix * nst - 1) % kAS);
+        advance(pc);
       };
 
       // three stages of registers: the loads of stages st + 1 and st + 2 are in
       // flight while stage st is computed (and while an epilogue runs)
-      load(0, xdy, xg, xfc);
-      load(1, ydy, yg, yfc);
+      load(xdy, xg, xfc);
+      load(ydy, yg, yfc);
       for (int st = 0; st < total; st += 3) {
-        load(st + 2, zdy, zg, zfc);
-        process(st, xdy, xg, xfc);
-        after(st);
+        load(zdy, zg, zfc);
+        process(xdy, xg, xfc);
+        after();
         if (st + 1 >= total) break;
-        load(st + 3, xdy, xg, xfc);
-        process(st + 1, ydy, yg, yfc);
-        after(st + 1);
+        load(xdy, xg, xfc);
+        process(ydy, yg, yfc);
+        after();
         if (st + 2 >= total) break;
-        load(st + 4, ydy, yg, yfc);
-        process(st + 2, zdy, zg, zfc);
-        after(st + 2);
+        load(ydy, yg, yfc);
+        process(zdy, zg, zfc);
+        after();
       }
       if (ntiles > 0) epilogue(ntiles - 1, (total - 1) % kAS);
       if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
