@@ -7,42 +7,46 @@
 // recompute-instead-of-store principle stated in the Ascend C backward blog
 // post (Swish section: recompute sigma in the backward rather than keep it).
 //
-// Twelve warps per CTA, one CTA per SM, launched as a persistent wave (FX) or
-// one CTA per tile (FW):
+// Twelve warps per CTA, one CTA per SM:
 //   warp 0 lane 0   TMA producer of the operand ring (W chunks for FX, x chunks
 //                   for FW; 128-byte swizzle)
 //   warp 1          tensor-memory allocation (512 columns); lane 0 issues
-//                   tcgen05.mma (M = 128, N = 256, K = 16) and tcgen05.commit
+//                   tcgen05.mma (K = 16) and tcgen05.commit (FW: in the pair's
+//                   leader only)
 //   warp 2 lane 0   L2 prefetch of the raw dy, g, fc tiles a few stages ahead
 //                   of the transform, paced by the transform's progress count
 //   warp 3          idle
 //   warps 4-11      transform: load dy, g, fc straight from global memory into
-//                   registers (FX: three stages of registers, the loads running
-//                   two stages ahead of the math; FW: two), compute dg, dfc in
-//                   fp32 and store them as bf16 into a ring of A-operand slots
-//                   in the 128-byte-swizzled layout the tensor core reads; then
-//                   the epilogue.
+//                   registers (three stages of registers: the loads run two
+//                   stages ahead of the math), compute dg, dfc in fp32 and store
+//                   them as bf16 into a ring of A-operand slots in the 128-byte-
+//                   swizzled layout the tensor core reads; then the epilogue.
 // Warpgroup 0 (warps 0-3) gives registers to the two transform warpgroups
 // (setmaxnreg): 48 per thread there, 224 in the transform (a block of twelve
 // warps is otherwise held to 168 per thread, and the FX transform wants more).
 //
-// fused x (FX): D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulator
-//   halves. Stages of 64 reduction columns n. A = dg or dfc [128 m x 64 n]
-//   (K-major), B = W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries).
-//   Persistent over m tiles: a tile's epilogue runs once the next tile's first
-//   stages are in their A slots, and it drains the low accumulator half first
-//   and releases it, so the next tile's first stages run their low-half MMAs
-//   while the high half is still being drained (their high-half MMAs follow).
-// fused w (FW): D = [dw_g^T ; dw_fc^T][n0:n0+64, k0:k0+512]: the A operand
-//   stacks 64 columns of dg over the same 64 columns of dfc (MN-major; the two
-//   8 KB halves of a slot are the two 64-element MN chunks, LBO = 8 KB), so one
-//   accumulator pair holds both outputs for all k. Stages of 64 rows of m;
-//   B = x [64 m x 256 k] per accumulator half (MN-major, four 64 x 64 boxes),
-//   one 64 KB ring entry per stage holding both halves, so the MMA issuer
-//   checks one x barrier and one A barrier per eight MMAs. The CTA owns a fixed
-//   band of 64 columns for its whole M range, so it also sums dg, dfc over its
-//   rows in registers (db column partials, one row per M split). The reduction
-//   over M is split into S chunks with fp32 partials and a fixed-order reduce.
+// fused x (FX): one CTA per MMA (M = 128, N = 256), persistent over m tiles.
+//   D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulator halves. Stages
+//   of 64 reduction columns n. A = dg or dfc [128 m x 64 n] (K-major), B =
+//   W_g / W_fc chunks [256 k x 64 n] (32 KB ring entries). A tile's epilogue
+//   runs once the next tile's first stages are in their A slots, and it drains
+//   the low accumulator half first and releases it, so the next tile's first
+//   stages run their low-half MMAs while the high half is still being drained.
+// fused w (FW): CTA pairs (clusters of 2); one tcgen05.mma.cta_group::2
+//   (M = 256, N = 256) spans both SMs. Each CTA owns a 64-column band of n:
+//   D = [dw_g^T ; dw_fc^T][n0:n0+64, k0:k0+512] in its own tensor memory, with
+//   an A operand stacking 64 columns of dg over the same 64 columns of dfc
+//   (MN-major; the two 8 KB halves of a slot are the two 64-element MN chunks,
+//   LBO = 8 KB) that it forms itself. B = x [64 m x 256 k] per accumulator half
+//   (MN-major), split along N: each CTA copies its 128 columns of k into its own
+//   shared memory, one 32 KB ring entry per stage holding both halves, so every
+//   SM streams half of x. The even CTA (the leader) issues the MMAs; its
+//   barriers collect both CTAs' arrivals and copies, and each release is
+//   committed to the barriers of both, so the leader checks one x barrier and
+//   one A barrier per eight pair MMAs. Stages of 64 rows of m. Each CTA sums its
+//   dg, dfc columns over its rows in registers (db column partials, one row per
+//   M split). The reduction over M is split into S chunks with fp32 partials
+//   and a fixed-order reduce.
 //
 // Every mbarrier wait is bounded; a timeout sets the module status word,
 // stops issuing, waits (bounded) for the work already issued, frees tensor
@@ -57,6 +61,7 @@ namespace {
 enum FusedMode : int { kFX = 0, kFW = 1 };
 
 constexpr int kThreads = 384;
+constexpr int kXThreads = 256;  // transform / epilogue threads (warps 4-11)
 constexpr int kXWarp0 = 4;      // first transform warp
 constexpr int kXWarps = 8;
 constexpr int kCtlRegs = 48;    // registers per thread in warpgroup 0 after setmaxnreg
@@ -68,6 +73,7 @@ template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kFX> {
+  static constexpr int kPair = 1;          // CTAs per MMA: single-CTA tcgen05.mma
   static constexpr int kRows = 128;        // m rows of a stage's tile (64 columns of n)
   static constexpr int kAStages = 3;       // A-operand slots (dg + dfc, 2 x 16 KB each)
   static constexpr int kEntryBytes = 32768;  // W_g or W_fc [256 k x 64 n]
@@ -76,10 +82,11 @@ struct Cfg<kFX> {
 };
 template <>
 struct Cfg<kFW> {
+  static constexpr int kPair = 2;          // CTAs per MMA: a cta_group::2 pair (M = 256)
   static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
-  static constexpr int kAStages = 2;       // A-operand slots (dg | dfc stacked, 16 KB each)
-  static constexpr int kEntryBytes = 65536;  // x [64 m x 512 k]: one stage, both accumulator halves
-  static constexpr int kEntries = 3;
+  static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
+  static constexpr int kEntryBytes = 65536 / kPair;  // x [64 m x 2 x 128 k]: this CTA's half of a stage
+  static constexpr int kEntries = 5;
   static constexpr int kPrefetch = 4;
 };
 
@@ -89,13 +96,13 @@ struct __align__(1024) FSmem {
   static constexpr int kHalf = C::kRows * 128;  // one 64-column bf16 tile (dg or dfc)
   uint8_t ring[C::kEntries][C::kEntryBytes];
   uint8_t aop[C::kAStages][2 * kHalf];          // [dg | dfc]
-  uint64_t a_full[C::kAStages];      // the transform warps have written the slot
+  uint64_t a_full[C::kAStages];      // leader: both CTAs' transform warps have written the slot
   uint64_t a_empty[C::kAStages];     // the MMAs reading the slot are done
-  uint64_t ring_full[C::kEntries];   // the entry's copies have landed
+  uint64_t ring_full[C::kEntries];   // leader: both CTAs' halves of the entry have landed
   uint64_t ring_empty[C::kEntries];  // the MMAs reading the entry are done
   uint64_t accum;                    // one phase per tile: the tile's MMAs are done
-  uint64_t tmem_free[2];             // one phase per tile per accumulator half: the epilogue
-                                     // warps have read it
+  uint64_t tmem_free[2];             // leader, one phase per tile per accumulator half: both
+                                     // CTAs' epilogues have read it
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   volatile uint32_t ring_issued, ring_consumed;
@@ -119,30 +126,31 @@ struct FusedArgs {
   float* ws;       // [splits][2][K][N] dw partials (splits > 1)
   float* db_part;  // [splits][2N]
   int splits, kb_per, nkb_total, tiles_n;
-  int ntiles;         // work tiles; CTA c takes c, c + gridDim.x, ...
+  int cluster_tiles;  // pair tiles; cluster c takes c, c + nclusters, ...
   int accumulate;     // FW: dw, db += this call's sums (one rounding of old + new)
   long long wait_limit;  // cycles before a pipeline wait gives up
   int64_t stall_at;      // test injection: the producer stops before this ring entry (-1: never)
 };
 
-// One CTA's work tile.
+// One CTA's share of one pair tile.
 struct Tile {
   int m0, n0, k0, kt, split, nst, kb_begin, nh, eps;
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile tile_of(int ct, const FusedArgs& args) {
+__device__ __forceinline__ Tile tile_of(int ct, uint32_t crank, const FusedArgs& args) {
+  constexpr int kPair = Cfg<MODE>::kPair;
   Tile t;
   t.m0 = t.n0 = t.split = t.kb_begin = 0;
   if (MODE == kFX) {
-    // a 128-row m tile at one 512-column block of K
+    // pair tile = 2 consecutive 128-row m tiles at one 512-column block of K
     t.kt = ct % args.tiles_k;
-    t.m0 = (ct / args.tiles_k) * 128;
+    t.m0 = ((ct / args.tiles_k) * kPair + static_cast<int>(crank)) * 128;
     t.nst = (args.N + 63) / 64;  // stages: 64 columns of n each
   } else {
-    // a 64-column band of n, one K block, one M split
-    const int bands = args.tiles_n;
-    t.n0 = (ct % bands) * 64;
+    // pair tile = 2 consecutive 64-column bands of n, one K block, one M split
+    const int bands = args.tiles_n / kPair;
+    t.n0 = ((ct % bands) * kPair + static_cast<int>(crank)) * 64;
     const int rest = ct / bands;
     t.kt = rest % args.tiles_k;
     t.split = rest / args.tiles_k;
@@ -203,6 +211,85 @@ __device__ __forceinline__ void named_sync_transform() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// ---- pair primitives
+// shared::cluster address of the location at the local offset p in CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// the u32 at the local offset p in the shared memory of CTA `rank`
+__device__ __forceinline__ uint32_t ld_cluster_u32(const volatile uint32_t* p, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr(const_cast<const uint32_t*>(p), rank))
+               : "memory");
+  return v;
+}
+// arrive once on an mbarrier of another CTA of the cluster, given by its shared::cluster
+// address. The data the arrival announces is consumed through the async proxy (the
+// tensor core reads this CTA's own shared memory; the writer fences its stores to the
+// async proxy first), so the default release at CTA scope suffices.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait with cluster-scope acquire: the barrier collects arrivals of both CTAs
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, long long limit) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(a, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+// 2-D / 3-D tiled load into this CTA's shared memory, completion counted on the
+// pair leader's mbarrier (shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem of both CTAs] (+)= A * B over the pair (M = 256 split 128/128, B split along N)
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive once on the mbarrier at `bar` (shared::cluster address) when every pair MMA
+// this thread issued so far is done
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
 // dg, dfc for 8 elements; adds them to the column sums
 __device__ __forceinline__ void grad8_sum(const uint4& dy, const uint4& g, const uint4& fc, uint4& dg, uint4& dfc,
                                           float (&sg)[8], float (&sf)[8]) {
@@ -242,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const FusedArgs args) {
   using S = FSmem<MODE>;
   using C = Cfg<MODE>;
+  constexpr int kPair = C::kPair;
   constexpr int kAS = C::kAStages;
   constexpr int kRE = C::kEntries;
   constexpr int kRows = C::kRows;
@@ -252,9 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  const uint32_t crank = kPair == 2 ? cluster_ctarank() : 0u;  // rank in the pair (FX: no cluster)
+  const bool leader = crank == 0;
+  const int cluster = blockIdx.x / kPair;
+  const int nclusters = gridDim.x / kPair;
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAS; ++i) {
-      mbar_init(&s.a_full[i], kXWarps);  // one arrival per transform warp
+      mbar_init(&s.a_full[i], kPair * kXWarps);
       mbar_init(&s.a_empty[i], 1);
     }
     for (int i = 0; i < kRE; ++i) {
@@ -262,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.ring_empty[i], 1);
     }
     mbar_init(&s.accum, 1);
-    mbar_init(&s.tmem_free[0], kXWarps);
-    mbar_init(&s.tmem_free[1], kXWarps);
+    mbar_init(&s.tmem_free[0], kPair * kXWarps);
+    mbar_init(&s.tmem_free[1], kPair * kXWarps);
     s.abort_flag = 0u;
     s.ring_issued = s.ring_consumed = 0u;
     s.x_progress = 0u;
@@ -275,62 +368,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_b1);
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (kPair == 2) {
+      tmem_alloc_pair(&s.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&s.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kPair == 2) cluster_sync();  // both CTAs' barriers are initialised before any remote arrival or copy
   const uint32_t tmem = s.tmem_base;
 
   if (warp < kXWarp0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs) : "memory");
 
   if (warp == 0) {
-    // ------------------------------------------------------------ operand producer
+    // ------------------------------------------------------------ operand producer (both CTAs)
     if (lane == 0) {
       uint32_t gj = 0;  // ring entries issued, over all tiles
-      bool stop = false;
-      for (int ct = blockIdx.x; ct < args.ntiles && !stop; ct += gridDim.x) {
-        const Tile tl = tile_of<MODE>(ct, args);
+      bool stopped = false;
+      for (int ct = cluster; ct < args.cluster_tiles && !s.abort_flag && !stopped; ct += nclusters) {
+        const Tile tl = tile_of<MODE>(ct, crank, args);
         const int total = tl.nst * tl.eps;
-        for (int j = 0; j < total; ++j, ++gj) {
-          if (s.abort_flag || static_cast<int64_t>(gj) == args.stall_at) {
-            stop = true;
+        for (int j = 0; j < total && !s.abort_flag; ++j, ++gj) {
+          if (static_cast<int64_t>(gj) == args.stall_at) {
+            stopped = true;
             break;
           }
           const int e = gj % kRE;
           if (gj >= kRE && !mbar_wait(&s.ring_empty[e], ((gj / kRE) - 1) & 1, args.wait_limit)) {
             flag_timeout(s, args.status);
-            stop = true;
             break;
           }
-          // FW: one 32 KB half per accumulator half in use
-          mbar_arrive_expect_tx(&s.ring_full[e], MODE == kFX ? C::kEntryBytes : tl.nh * 32768u);
+          // the leader's barrier counts both halves of the entry
+          if (leader) mbar_arrive_expect_tx(&s.ring_full[e], MODE == kFX ? kPair * C::kEntryBytes : tl.nh * 32768u);
+          const uint32_t full = kPair == 2 ? cluster_addr(&s.ring_full[e], 0) : 0u;
           if (MODE == kFX) {
             const EntryPos ep = fx_entry(tl, j);
-            tma_load_2d(s.ring[e], ep.p ? &tm_b1 : &tm_b0, &s.ring_full[e], ep.i * 64, tl.k0 + 256 * ep.h);
+            const int kr = tl.k0 + 256 * ep.h + (256 / kPair) * static_cast<int>(crank);
+            if (kPair == 2)
+              tma_load_2d_pair(s.ring[e], ep.p ? &tm_b1 : &tm_b0, full, ep.i * 64, kr);
+            else
+              tma_load_2d(s.ring[e], ep.p ? &tm_b1 : &tm_b0, &s.ring_full[e], ep.i * 64, kr);
           } else {
             const int mrow = (tl.kb_begin + j) * 64;
-            // per accumulator half, four 64 x 64 boxes: 64-column MN chunks (columns past K read as zeros)
-            for (int h = 0; h < tl.nh; ++h)
+            for (int h = 0; h < tl.nh; ++h) {
+              const int kk = tl.k0 + 256 * h + (256 / kPair) * static_cast<int>(crank);
+              uint8_t* dst = s.ring[e] + h * (32768 / kPair);
 #pragma unroll
-              for (int cb = 0; cb < 4; ++cb)
-                tma_load_2d(s.ring[e] + h * 32768 + cb * 8192, &tm_b0, &s.ring_full[e], tl.k0 + 256 * h + 64 * cb,
-                            mrow);
+              for (int cbox = 0; cbox < 4 / kPair; ++cbox) {
+                if (kPair == 2)
+                  tma_load_2d_pair(dst + cbox * 8192, &tm_b0, full, kk + 64 * cbox, mrow);
+                else
+                  tma_load_2d(dst + cbox * 8192, &tm_b0, &s.ring_full[e], kk + 64 * cbox, mrow);
+              }
+            }
           }
           s.ring_issued = gj + 1;
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, MODE == kFW, MODE == kFW);
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128 * kPair, 256, MODE == kFW, MODE == kFW);
       uint32_t gi = 0, gj = 0, tt = 0;  // A stages, ring entries, tiles consumed
       bool ok = true;
-      // the MMAs of ring entry gj: stage i of the tile (A slot gi + i); FX: product p, accumulator
-      // half h; FW: both products at once, h = the accumulator halves in use
-      auto consume = [&](int i, int p, int h) -> bool {
+      // a release goes to the barrier at the same offset in both CTAs
+      auto commit2 = [&](uint64_t* bar) {
+        if (kPair == 2) {
+          umma_commit_pair(cluster_addr(bar, 0));
+          umma_commit_pair(cluster_addr(bar, 1));
+        } else {
+          umma_commit(bar);
+        }
+      };
+      auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
+        if (kPair == 2)
+          umma_pair(d, ad, bd, idesc, acc);
+        else
+          umma_bf16(d, ad, bd, idesc, acc);
+      };
+      auto consume = [&](int i, int p, int h, int nh_unused) -> bool {
+        (void)nh_unused;
         const int e = gj % kRE;
         if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
           flag_timeout(s, args.status);
@@ -344,16 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = a_slot + p * kHalf;  // dg or dfc
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 32 * k, 16, 1024),
-                      idesc, (i > 0 || p > 0 || k > 0) ? 1u : 0u);
+            mma(tmem + h * 256, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 32 * k, 16, 1024),
+                (i > 0 || p > 0 || k > 0) ? 1u : 0u);
         } else {
-          for (int hh = 0; hh < h; ++hh)
+          for (int hh = 0; hh < h; ++hh)  // h: the halves in use
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + hh * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
-                        smem_desc(b_addr + hh * 32768 + 2048 * k, 8192, 1024), idesc, (i > 0 || k > 0) ? 1u : 0u);
+              mma(tmem + hh * 256, smem_desc(a_slot + 2048 * k, kHalf, 1024),
+                  smem_desc(b_addr + hh * (32768 / kPair) + 2048 * k, 8192, 1024), (i > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(&s.ring_empty[e]);
+        commit2(&s.ring_empty[e]);
         ++gj;
         return true;
       };
@@ -376,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return true;
       };
-      for (int ct = blockIdx.x; ct < args.ntiles && ok; ct += gridDim.x, ++tt) {
-        const Tile tl = tile_of<MODE>(ct, args);
+      for (int ct = cluster; ct < args.cluster_tiles && ok; ct += nclusters, ++tt) {
+        const Tile tl = tile_of<MODE>(ct, 0u, args);
         if (MODE == kFX) {
           // the first J stages: low-half MMAs as soon as the low half is free, then
           // their high-half MMAs once the high half is free too
@@ -386,40 +508,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (J == 0 && !wait_free(1)) break;
           for (int i = 0; i < J && ok; ++i) {
             ok = wait_a(i);
-            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 0);
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 0, 0);
           }
           if (ok && J > 0) ok = wait_free(1);
           for (int i = 0; i < J && ok; ++i) {
-            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 1);
-            umma_commit(&s.a_empty[(gi + i) % kAS]);
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 1, 0);
+            commit2(&s.a_empty[(gi + i) % kAS]);
           }
           for (int i = J; i < tl.nst && ok; ++i) {
             ok = wait_a(i);
-            for (int q = 0; q < tl.eps && ok; ++q) ok = consume(i, q / tl.nh, q % tl.nh);
-            umma_commit(&s.a_empty[(gi + i) % kAS]);
+            for (int q = 0; q < tl.eps && ok; ++q) ok = consume(i, q / tl.nh, q % tl.nh, 0);
+            commit2(&s.a_empty[(gi + i) % kAS]);
           }
         } else {
           if (!wait_free(0) || !wait_free(1)) break;
           for (int i = 0; i < tl.nst && ok; ++i) {
             ok = wait_a(i);
-            if (ok) ok = consume(i, 0, tl.nh);
-            umma_commit(&s.a_empty[(gi + i) % kAS]);
+            if (ok) ok = consume(i, 0, tl.nh, 0);
+            commit2(&s.a_empty[(gi + i) % kAS]);
           }
         }
         gi += tl.nst;
-        umma_commit(&s.accum);  // this tile's accumulator is complete
+        commit2(&s.accum);  // this tile's accumulators (both CTAs) are complete
       }
-      // after a timeout the epilogue may have stopped waiting: see every MMA this thread
-      // issued complete before TMEM is freed (tt accumulator phases were committed)
+      // after a timeout the epilogues may have stopped waiting: see every MMA this thread
+      // issued complete before tensor memory is freed (tt accumulator phases were committed)
       if (s.abort_flag && tt > 0) mbar_wait(&s.accum, (tt - 1) & 1, args.wait_limit);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ L2 prefetch of the raw tiles
     if (lane == 0) {
       int ntot = 0;
-      for (int ct = blockIdx.x; ct < args.ntiles; ct += gridDim.x) ntot += tile_of<MODE>(ct, args).nst;
+      for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters) ntot += tile_of<MODE>(ct, crank, args).nst;
       int next = 0, tix = 0, in_tile = 0;
-      Tile tl = tile_of<MODE>(blockIdx.x, args);
+      Tile tl = tile_of<MODE>(cluster, crank, args);
       uint32_t last = 0;
       long long tlast = clock64();
       while (next < ntot && !s.abort_flag) {
@@ -444,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++in_tile == tl.nst) {
             in_tile = 0;
             ++tix;
-            tl = tile_of<MODE>(blockIdx.x + tix * gridDim.x, args);
+            tl = tile_of<MODE>(cluster + tix * nclusters, crank, args);
           }
         } else {
           if (clock64() - tlast > args.wait_limit) break;  // the transform stopped making progress
@@ -454,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kXWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kXRegs) : "memory");
-    // ------------------------------------------------------------ transform
+    // ------------------------------------------------------------ transform (both CTAs)
     const int t = threadIdx.x - kXWarp0 * 32;  // 0..255
     const int xw = warp - kXWarp0;             // transform warp 0..7
     const int c = t & 7;                       // 16-byte chunk of the 64-column tile (8 columns)
@@ -464,10 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // part in the arrivals and the named barriers.
     bool dead = false;
 
-    // one arrival of this warp, after every lane's work before it
-    auto warp_arrive = [&](uint64_t* bar) {
+    // arrival of this warp on a barrier of the pair leader (after its lanes' work)
+    auto warp_arrive_leader = [&](uint64_t* bar) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
+      if (lane == 0) {
+        if (kPair == 1 || leader)
+          mbar_arrive(bar);
+        else
+          mbar_arrive_remote(cluster_addr(bar, 0));
+      }
     };
     // stores one stage's dg, dfc (8 columns x kRPT rows of this thread) into A slot a
     auto store_stage = [&](int a, int row0, int col, bool want_dg, const uint4 (&bdy)[kRPT],
@@ -517,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (s.abort_flag) dead = true;
     };
-    uint4 xdy[kRPT], xg[kRPT], xfc[kRPT], ydy[kRPT], yg[kRPT], yfc[kRPT];
+    uint4 xdy[kRPT], xg[kRPT], xfc[kRPT], ydy[kRPT], yg[kRPT], yfc[kRPT], zdy[kRPT], zg[kRPT], zfc[kRPT];
 
     if constexpr (MODE == kFX) {
       // The CTA's stages form one stream over its tiles: stage st is stage
@@ -526,16 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // are in their A slots; the staging buffer of the epilogue's TMA stores
       // is the A slot of the finished tile's last stage, free once its MMAs are.
       const int nst = (args.N + 63) / 64;
-      const int ntiles = static_cast<int>(blockIdx.x) < args.ntiles
-                             ? (args.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                             : 0;
+      const int ntiles = cluster < args.cluster_tiles ? (args.cluster_tiles - 1 - cluster) / nclusters + 1 : 0;
       const int total = ntiles * nst;
       const int look = nst < kAS - 1 ? nst : kAS - 1;
-      auto tile_at = [&](int tix) { return tile_of<MODE>(blockIdx.x + tix * gridDim.x, args); };
+      auto tile_at = [&](int tix) { return tile_of<MODE>(cluster + tix * nclusters, crank, args); };
       float ug[8], uf[8];  // column sums, unused here
 #pragma unroll
       for (int e = 0; e < 8; ++e) ug[e] = uf[e] = 0.0f;
-      uint4 zdy[kRPT], zg[kRPT], zfc[kRPT];
 
       // a position in the CTA's stage stream: stage index, stage within its tile, tile index,
       // and the tile's first row and K block, advanced without divisions
@@ -568,12 +692,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         acquire_slot(static_cast<uint32_t>(st), a);
         if (!dead)
           store_stage(a, pc.m0, pc.sit * 64 + c * 8, pc.kt == 0 && args.dg_out != nullptr, bdy, bg, bfc, ug, uf);
-        warp_arrive(&s.a_full[a]);
+        warp_arrive_leader(&s.a_full[a]);
         if (t == 0) s.x_progress = static_cast<uint32_t>(st + 1);
       };
       // tile tix's accumulator -> bf16 dx through staging buffer stg (an A slot):
       // the low half (columns 0-255) first, then the high half, each released to the
-      // MMA issuer as soon as every warp has read it
+      // leader as soon as it has been read
       auto epilogue = [&](int tix, int stg) {
         const Tile tl = tile_at(tix);
         bool acc_ok = false;
@@ -581,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_ok = mbar_wait(&s.accum, tix & 1, args.wait_limit);
           if (!acc_ok) flag_timeout(s, args.status);
         }
-        const int q = warp & 3;   // TMEM lane quarter this warp may read
-        const int sub = xw >> 2;  // 128-column half of each accumulator half
+        const int q = warp & 3;    // TMEM lane quarter this warp may read
+        const int sub = xw >> 2;   // 128-column half of each accumulator half
         tc_fence_after();
         // tcgen05.ld is warp-collective: decide for the whole warp
         const bool go = __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag);
@@ -613,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_fence_before();
-          warp_arrive(&s.tmem_free[h]);  // this warp has read its part of half h
+          warp_arrive_leader(&s.tmem_free[h]);  // this warp has read its part of half h
         }
         // the staging slot is written again by a later stage: every store has read it
         if (lane == 0) bulk_wait_read<0>();
@@ -645,8 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
     } else {
       uint32_t gi = 0, tt = 0;  // A stages, tiles produced
-      for (int ct = blockIdx.x; ct < args.ntiles; ct += gridDim.x, ++tt) {
-        const Tile tl = tile_of<MODE>(ct, args);
+      for (int ct = cluster; ct < args.cluster_tiles; ct += nclusters, ++tt) {
+        const Tile tl = tile_of<MODE>(ct, crank, args);
         const int n0 = tl.n0, k0 = tl.k0, kb_begin = tl.kb_begin, nst = tl.nst, nh = tl.nh, split = tl.split;
         const bool want_db = tl.kt == 0 && args.db_part != nullptr;
         float cg[8], cf[8];  // column sums over the CTA's whole M range
@@ -661,19 +785,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int a = gs % kAS;
           acquire_slot(gs, a);
           if (!dead) store_stage(a, (kb_begin + i) * 64, n0 + c * 8, false, bdy, bg, bfc, cg, cf);
-          warp_arrive(&s.a_full[a]);
+          warp_arrive_leader(&s.a_full[a]);
           if (t == 0) s.x_progress = gs + 1;
         };
 
-        // two stages per iteration, alternating register buffers: the loads of the
-        // next stage are in flight while this stage is computed
         load(0, xdy, xg, xfc);
-        for (int i = 0; i < nst; i += 2) {
-          load(i + 1, ydy, yg, yfc);
+        load(1, ydy, yg, yfc);
+        for (int i = 0; i < nst; i += 3) {
+          load(i + 2, zdy, zg, zfc);
           process(i, xdy, xg, xfc);
           if (i + 1 >= nst) break;
-          load(i + 2, xdy, xg, xfc);
+          load(i + 3, xdy, xg, xfc);
           process(i + 1, ydy, yg, yfc);
+          if (i + 2 >= nst) break;
+          load(i + 4, ydy, yg, yfc);
+          process(i + 2, zdy, zg, zfc);
         }
 
         gi += nst;
@@ -721,8 +847,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
         tc_fence_after();
-        const int r = q * 32 + lane;  // accumulator row (TMEM lane)
-        const int h = xw >> 2;        // accumulator half this warp drains
+        const int r = q * 32 + lane;    // accumulator row (TMEM lane)
+        const int h = xw >> 2;          // accumulator half this warp drains
         // tcgen05.ld is warp-collective: decide for the whole warp
         if (h < nh && __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag && nst > 0)) {
 #pragma unroll 1
@@ -759,22 +885,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        warp_arrive(&s.tmem_free[0]);  // this warp has read its part of the accumulator
-        warp_arrive(&s.tmem_free[1]);
+        warp_arrive_leader(&s.tmem_free[0]);  // this warp has read its part of the accumulator
+        warp_arrive_leader(&s.tmem_free[1]);
       }  // tile loop
     }
   }
 
   __syncthreads();
-  if (threadIdx.x == 0 && s.abort_flag) {
-    // drain: ring copies issued but never waited on must land before the CTA exits
-    for (uint32_t i = s.ring_consumed; i < s.ring_issued; ++i)
-      if (!mbar_wait(&s.ring_full[i % kRE], (i / kRE) & 1, args.wait_limit)) break;
+  if (kPair == 2) cluster_sync();  // both CTAs are done with their roles: no more remote arrivals or commits
+  if (leader && threadIdx.x == 0) {
+    const uint32_t peer_abort = kPair == 2 ? ld_cluster_u32(&s.abort_flag, 1) : 0u;
+    if (s.abort_flag || peer_abort) {
+      // drain: copies (of either CTA) that complete on this CTA's barriers must land
+      // before any CTA exits
+      const uint32_t peer_issued = kPair == 2 ? ld_cluster_u32(&s.ring_issued, 1) : 0u;
+      const uint32_t issued = s.ring_issued > peer_issued ? s.ring_issued : peer_issued;
+      for (uint32_t i = s.ring_consumed; i < issued; ++i)
+        if (!mbar_wait(&s.ring_full[i % kRE], (i / kRE) & 1, args.wait_limit)) break;
+    }
   }
+  if (kPair == 2) cluster_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (kPair == 2)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -787,6 +924,7 @@ template <int MODE>
 cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const CUtensorMap& out,
                    FusedArgs args, bool persistent) {
+  constexpr int kPair = Cfg<MODE>::kPair;
   constexpr size_t smem = smem_bytes<MODE>();
   static_assert(smem <= 232448, "fused kernel shared memory");
   static_assert(128 * kCtlRegs + 256 * kXRegs <= kThreads * 168, "setmaxnreg split exceeds a 168-register launch");
@@ -804,19 +942,43 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
     if (static_cast<long long>(fa.numRegs) * kThreads < 128LL * kCtlRegs + 256LL * kXRegs)
       return cudaErrorInvalidValue;
   }
-  args.ntiles = static_cast<int>(grid);
-  if (persistent) {
-    // one resident wave, each CTA looping over tiles
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<MODE>, kThreads, smem) ==
-            cudaSuccess &&
-        per_sm > 0) {
-      const unsigned wave = static_cast<unsigned>(per_sm * device_sm_count());
-      if (wave < grid) grid = wave;
+  args.cluster_tiles = static_cast<int>(grid / kPair);
+  if constexpr (kPair == 1) {
+    if (persistent) {
+      // one resident wave, each CTA looping over tiles
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<MODE>, kThreads, smem) ==
+              cudaSuccess &&
+          per_sm > 0) {
+        const unsigned wave = static_cast<unsigned>(per_sm * device_sm_count());
+        if (wave < grid) grid = wave;
+      }
     }
+    fused_kernel<MODE><<<grid, kThreads, smem, stream>>>(a, b, c, d, e, out, args);
+    return cudaGetLastError();
+  } else {
+    // clusters of two CTAs: the pair that one cta_group::2 MMA spans
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (persistent) {
+      // one resident wave of pairs, each looping over pair tiles
+      int max_clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, fused_kernel<MODE>, &cfg) == cudaSuccess &&
+          max_clusters > 0 && static_cast<unsigned>(max_clusters) * kPair < grid)
+        cfg.gridDim = dim3(static_cast<unsigned>(max_clusters) * kPair);
+    }
+    return cudaLaunchKernelEx(&cfg, fused_kernel<MODE>, a, b, c, d, e, out, args);
   }
-  fused_kernel<MODE><<<grid, kThreads, smem, stream>>>(a, b, c, d, e, out, args);
-  return cudaGetLastError();
 }
 
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -843,13 +1005,15 @@ FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
 cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, const uint16_t* w_g,
                            const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
                            int64_t N, cudaStream_t stream) {
+  constexpr int kPair = Cfg<kFX>::kPair;
   CUtensorMap mdy, mg, mfc, mw0, mw1, mdx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mdx, dx, K, M, static_cast<uint64_t>(K) * 2, 32, 32, 64)) return cudaErrorInvalidValue;
   // the raw tensors are only prefetched into L2 here, one stage's box at a time
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 128, 0) ||
-      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256) ||
-      !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256))
+      !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) ||
+      !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256 / kPair) ||
+      !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256 / kPair))
     return cudaErrorInvalidValue;
   FusedArgs a{};
   a.M = static_cast<int>(M);
@@ -866,8 +1030,9 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
   const Injection inj = take_injection(2);
   a.wait_limit = inj.wait_limit;
   a.stall_at = inj.stall_at;
-  const int64_t tiles = (M + 127) / 128 * a.tiles_k;
-  return launch<kFX>(static_cast<unsigned>(tiles), stream, mdy, mg, mfc, mw0, mw1, mdx, a, true);
+  const int64_t mpairs = ((M + 127) / 128 + kPair - 1) / kPair;  // tail CTAs run on zero-filled rows
+  return launch<kFX>(static_cast<unsigned>(mpairs * kPair * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, mdx, a,
+                     true);
 }
 
 namespace {
@@ -877,6 +1042,7 @@ namespace {
 cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                              uint16_t* dw_g, uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, float* dw_part,
                              float* db_part, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+  constexpr int kPair = Cfg<kFW>::kPair;
   CUtensorMap mdy, mg, mfc, mx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   // x as 64 x 64 boxes (64 columns of k, 64 rows of m): 8 KB MN-major chunks
@@ -900,7 +1066,7 @@ cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16
   a.splits = static_cast<int>(plan.splits);
   a.kb_per = static_cast<int>(plan.kb_per);
   a.nkb_total = static_cast<int>((M + 63) / 64);
-  a.tiles_n = static_cast<int>((N + 63) / 64);
+  a.tiles_n = static_cast<int>(((N + 63) / 64 + kPair - 1) / kPair * kPair);  // pairs of 64-column bands
   a.accumulate = accumulate ? 1 : 0;
   a.wait_limit = kWaitLimitCycles;
   a.stall_at = -1;
