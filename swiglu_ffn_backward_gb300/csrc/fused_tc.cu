@@ -40,13 +40,14 @@
 //   LBO = 8 KB) that it forms itself. B = x [64 m x 256 k] per accumulator half
 //   (MN-major), split along N: each CTA copies its 128 columns of k into its own
 //   shared memory, one 32 KB ring entry per stage holding both halves, so every
-//   SM streams half of x. The even CTA (the leader) issues the MMAs; its
-//   barriers collect both CTAs' arrivals and copies, and each release is
-//   committed to the barriers of both, so the leader checks one x barrier and
-//   one A barrier per eight pair MMAs. Stages of 64 rows of m. Each CTA sums its
-//   dg, dfc columns over its rows in registers (db column partials, one row per
-//   M split). The reduction over M is split into S chunks with fp32 partials
-//   and a fixed-order reduce.
+//   SM streams half of x. The even CTA (the leader) issues the MMAs. One
+//   barrier per stage slot (four slots, each an x entry and an A slot)
+//   collects the stage's copies of both CTAs and the arrivals of both CTAs'
+//   transform warps, and one release per stage is committed to the barriers of
+//   both CTAs, so the leader checks one barrier per eight pair MMAs. Stages of
+//   64 rows of m. Each CTA sums its dg, dfc columns over its rows in registers
+//   (db column partials, one row per M split). The reduction over M is split
+//   into S chunks with fp32 partials and a fixed-order reduce.
 //
 // Every mbarrier wait is bounded; a timeout sets the module status word,
 // stops issuing, waits (bounded) for the work already issued, frees tensor
@@ -86,7 +87,7 @@ struct Cfg<kFW> {
   static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
   static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
   static constexpr int kEntryBytes = 65536 / kPair;  // x [64 m x 2 x 128 k]: this CTA's half of a stage
-  static constexpr int kEntries = 5;
+  static constexpr int kEntries = 4;       // = kAStages: entry i and A slot i form stage slot i
   static constexpr int kPrefetch = 4;
 };
 
@@ -96,10 +97,11 @@ struct __align__(1024) FSmem {
   static constexpr int kHalf = C::kRows * 128;  // one 64-column bf16 tile (dg or dfc)
   uint8_t ring[C::kEntries][C::kEntryBytes];
   uint8_t aop[C::kAStages][2 * kHalf];          // [dg | dfc]
-  uint64_t a_full[C::kAStages];      // leader: both CTAs' transform warps have written the slot
-  uint64_t a_empty[C::kAStages];     // the MMAs reading the slot are done
-  uint64_t ring_full[C::kEntries];   // leader: both CTAs' halves of the entry have landed
-  uint64_t ring_empty[C::kEntries];  // the MMAs reading the entry are done
+  uint64_t a_full[C::kAStages];      // FX: the transform warps have written the slot
+  uint64_t a_empty[C::kAStages];     // FX: the MMAs reading the slot are done
+  uint64_t ring_full[C::kEntries];   // the entry's copies have landed (FW, leader: both CTAs'
+                                     // halves, and both CTAs' transform warps wrote A slot i)
+  uint64_t ring_empty[C::kEntries];  // the MMAs reading the entry (FW: and A slot i) are done
   uint64_t accum;                    // one phase per tile: the tile's MMAs are done
   uint64_t tmem_free[2];             // leader, one phase per tile per accumulator half: both
                                      // CTAs' epilogues have read it
@@ -351,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.a_empty[i], 1);
     }
     for (int i = 0; i < kRE; ++i) {
-      mbar_init(&s.ring_full[i], 1);
+      // FW: the stage's x copies and both CTAs' A slots complete one barrier
+      mbar_init(&s.ring_full[i], MODE == kFW ? 1 + kPair * kXWarps : 1);
       mbar_init(&s.ring_empty[i], 1);
     }
     mbar_init(&s.accum, 1);
@@ -523,9 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           if (!wait_free(0) || !wait_free(1)) break;
           for (int i = 0; i < tl.nst && ok; ++i) {
-            ok = wait_a(i);
-            if (ok) ok = consume(i, 0, tl.nh, 0);
-            commit2(&s.a_empty[(gi + i) % kAS]);
+            ok = consume(i, 0, tl.nh, 0);
           }
         }
         gi += tl.nst;
@@ -638,7 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // waits for A slot a to be released by the MMAs of stage st - kAS
     auto acquire_slot = [&](uint32_t st, int a) {
-      if (!dead && st >= kAS && !mbar_wait(&s.a_empty[a], ((st / kAS) - 1) & 1, args.wait_limit)) {
+      uint64_t* eb = MODE == kFW ? &s.ring_empty[a] : &s.a_empty[a];
+      if (!dead && st >= kAS && !mbar_wait(eb, ((st / kAS) - 1) & 1, args.wait_limit)) {
         flag_timeout(s, args.status);
         dead = true;
       }
@@ -785,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int a = gs % kAS;
           acquire_slot(gs, a);
           if (!dead) store_stage(a, (kb_begin + i) * 64, n0 + c * 8, false, bdy, bg, bfc, cg, cf);
-          warp_arrive_leader(&s.a_full[a]);
+          warp_arrive_leader(&s.ring_full[a]);
           if (t == 0) s.x_progress = gs + 1;
         };
 
@@ -926,6 +928,7 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
                    FusedArgs args, bool persistent) {
   constexpr int kPair = Cfg<MODE>::kPair;
   constexpr size_t smem = smem_bytes<MODE>();
+  static_assert(MODE == kFX || Cfg<kFW>::kEntries == Cfg<kFW>::kAStages, "fw slots");
   static_assert(smem <= 232448, "fused kernel shared memory");
   static_assert(128 * kCtlRegs + 256 * kXRegs <= kThreads * 168, "setmaxnreg split exceeds a 168-register launch");
   cudaError_t err = cudaFuncSetAttribute(fused_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
