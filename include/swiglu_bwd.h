@@ -226,9 +226,15 @@ swg_status swiglu_fwd(const void* x, const void* w_g, const void* w_fc,
  * flags: SWG_UNFUSED, SWG_FUSED or SWG_AUTO, optionally | SWG_ACCUMULATE.
  * dg, dfc are optional outputs: pass NULL to skip them. With SWG_UNFUSED and
  * NULL dg/dfc, the workspace holds them (4*M*N bytes more). With SWG_FUSED the
- * call runs swiglu_bwd_x_fused then swiglu_bwd_w_fused: the w and x GEMMs
- * compute dg, dfc tile by tile in shared memory from dy, g, fc; their operands
- * are the bf16 roundings of the fp32 dg, dfc, exactly as in the unfused chain.
+ * call runs the work of swiglu_bwd_w_fused and swiglu_bwd_x_fused: the w and x
+ * GEMMs compute dg, dfc tile by tile in shared memory from dy, g, fc; their
+ * operands are the bf16 roundings of the fp32 dg, dfc, exactly as in the
+ * unfused chain. When the w stage leaves SMs free and the x stage needs more
+ * than one wave of tiles, the x stage's last tiles run beside the w stage on a
+ * library-owned side stream (forked from and joined back into `stream` within
+ * the call, so the call stays ordered on `stream` and can be captured in a CUDA
+ * graph) and the rest after it; every output is bit-identical to the two stage
+ * calls.
  * Workspace: swiglu_bwd_workspace_size(M, K, N, flags) bytes; with non-NULL
  * dg/dfc the smaller figure swiglu_bwd_workspace_size(M, K, N, flags |
  * SWG_WS_DG_GIVEN) suffices. */

@@ -603,6 +603,8 @@ swg_status swiglu_bwd_host(const void* x, const void* w_g, const void* w_fc, con
 // fused 0.80 ms, unfused 1.07 ms; K = 512, M = 65537: 0.285 vs 0.346 ms;
 // K = 512, M <= 4097: fused slower (fixed costs of its two persistent
 // launches); K = 4096, N = 14336, M = 16384: fused 6.85 ms, unfused 5.48 ms.
+namespace {
+
 bool auto_fused(int64_t M, int64_t K) { return K <= 512 && M >= 32768; }
 
 unsigned resolve_auto(int64_t M, int64_t K, unsigned flags) {
@@ -610,6 +612,59 @@ unsigned resolve_auto(int64_t M, int64_t K, unsigned flags) {
   flags &= ~(SWG_AUTO | SWG_FUSED);
   return auto_fused(M, K) ? (flags | SWG_FUSED) : flags;
 }
+
+// The fused chain's x-stage work split: when the w stage occupies fewer CTAs than the GPU has
+// SMs, the x stage's last side_tiles tiles run on side_ctas CTAs beside the w stage and the
+// other main_tiles tiles in one persistent wave after it. The side share is what makes the
+// main part one wave round shorter (main_tiles = (rounds - 1) * SMs), and it is taken only when
+// its own rounds fit well inside the w stage. By operand volume a w-stage CTA does the work of
+// kb_per / (2 * ceil(N / 64)) x-stage tiles (a 64-row stage of one band against a 128-row tile
+// over all bands); in time it takes about three quarters of that (measured at K = 512,
+// N = 1024: 382 stages against 8.8 tiles). The side rounds may use 0.6 of the volume figure,
+// about 80% of the w stage's time.
+struct FxSplit {
+  int64_t main_tiles = 0, side_tiles = 0;
+  int side_ctas = 0;
+};
+FxSplit fx_split(int64_t M, int64_t K, int64_t N, const swg::FwPlan& plan, int sms) {
+  FxSplit sp;
+  const int64_t tiles = swg::fused_x_tiles(M, K);
+  sp.main_tiles = tiles;
+  const int64_t idle = sms - swg::fused_w_ctas(K, N, plan);
+  const int64_t rounds = (tiles + sms - 1) / sms;
+  if (idle <= 0 || rounds < 2) return sp;
+  const int64_t main = (rounds - 1) * sms, side = tiles - main;
+  const int64_t side_rounds = (side + idle - 1) / idle;
+  const int64_t nst = (N + 63) / 64;
+  if (side_rounds * 2 * nst * 5 > plan.kb_per * 3) return sp;
+  sp.main_tiles = main;
+  sp.side_tiles = side;
+  sp.side_ctas = static_cast<int>(idle);
+  return sp;
+}
+
+// the side stream of the fused chain and its fork / join events (per device, created once;
+// the enqueue of one call holds the lock)
+struct SideStream {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+cudaError_t side_stream(int dev, SideStream** out) {
+  SideStream& h = g_side[dev];
+  if (h.side == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  *out = &h;
+  return cudaSuccess;
+}
+
+}  // namespace
 
 size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags) {
   if (M <= 0 || K <= 0 || N <= 0) return 0;
@@ -667,17 +722,42 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
 
   uint8_t* wp = static_cast<uint8_t*>(workspace);
   if (flags & SWG_FUSED) {
-    const swg::FwPlan fplan = swg::fw_plan(M, K, N, swg::device_sm_count());
-    cudaError_t e = swg::launch_fused_x(
-        static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
-        static_cast<const uint16_t*>(w_g), static_cast<const uint16_t*>(w_fc), static_cast<uint16_t*>(dx),
-        static_cast<uint16_t*>(dg), static_cast<uint16_t*>(dfc), M, K, N, s);
-    if (e != cudaSuccess) return SWG_ERR_CUDA;
-    e = swg::launch_fused_w(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
-                            static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
-                            static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
-                            static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, wp, fplan, s,
-                            acc);
+    const int sms = swg::device_sm_count();
+    const swg::FwPlan fplan = swg::fw_plan(M, K, N, sms);
+    const FxSplit sp = fx_split(M, K, N, fplan, sms);
+    auto fx = [&](cudaStream_t cs, int64_t t0, int64_t t1, int ctas) {
+      return swg::launch_fused_x(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(g),
+                                 static_cast<const uint16_t*>(fc), static_cast<const uint16_t*>(w_g),
+                                 static_cast<const uint16_t*>(w_fc), static_cast<uint16_t*>(dx),
+                                 static_cast<uint16_t*>(dg), static_cast<uint16_t*>(dfc), M, K, N, cs, t0, t1, ctas);
+    };
+    auto fw = [&]() {
+      return swg::launch_fused_w(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
+                                 static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+                                 static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
+                                 static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), M, K, N, wp, fplan,
+                                 s, acc);
+    };
+    if (sp.side_tiles == 0) {
+      cudaError_t e = fx(s, 0, -1, 0);
+      if (e == cudaSuccess) e = fw();
+      return cuda_status(e);
+    }
+    // the w stage leaves SMs free: the last x-stage tiles run there at the same time, on a
+    // side stream ordered after everything before this call, and the caller's stream waits
+    // for them at the end; the other x-stage tiles follow the w stage in one persistent wave
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SWG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    SideStream* ss = nullptr;
+    if (side_stream(dev, &ss) != cudaSuccess) return SWG_ERR_CUDA;
+    cudaError_t e = cudaEventRecord(ss->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->side, ss->fork, 0);
+    if (e == cudaSuccess) e = fw();
+    if (e == cudaSuccess) e = fx(ss->side, sp.main_tiles, sp.main_tiles + sp.side_tiles, sp.side_ctas);
+    if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->side);
+    if (e == cudaSuccess) e = fx(s, 0, sp.main_tiles, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);
     return cuda_status(e);
   }
   uint16_t* dgp = static_cast<uint16_t*>(dg);

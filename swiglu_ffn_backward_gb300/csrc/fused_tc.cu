@@ -128,6 +128,7 @@ struct FusedArgs {
   float* ws;       // [splits][2][K][N] dw partials (splits > 1)
   float* db_part;  // [splits][2N]
   int splits, kb_per, nkb_total, tiles_n;
+  int tile0;          // FX: the first m tile of this launch (tiles tile0 + ct)
   int cluster_tiles;  // pair tiles; cluster c takes c, c + nclusters, ...
   int accumulate;     // FW: dw, db += this call's sums (one rounding of old + new)
   long long wait_limit;  // cycles before a pipeline wait gives up
@@ -145,9 +146,11 @@ __device__ __forceinline__ Tile tile_of(int ct, uint32_t crank, const FusedArgs&
   Tile t;
   t.m0 = t.n0 = t.split = t.kb_begin = 0;
   if (MODE == kFX) {
-    // pair tile = 2 consecutive 128-row m tiles at one 512-column block of K
-    t.kt = ct % args.tiles_k;
-    t.m0 = ((ct / args.tiles_k) * kPair + static_cast<int>(crank)) * 128;
+    // a 128-row m tile at one 512-column block of K
+    static_assert(Cfg<kFX>::kPair == 1, "FX runs on single-CTA MMAs");
+    const int c2 = ct + args.tile0;
+    t.kt = c2 % args.tiles_k;
+    t.m0 = (c2 / args.tiles_k) * 128;
     t.nst = (args.N + 63) / 64;  // stages: 64 columns of n each
   } else {
     // pair tile = 2 consecutive 64-column bands of n, one K block, one M split
@@ -925,7 +928,7 @@ constexpr size_t smem_bytes() {
 template <int MODE>
 cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const CUtensorMap& out,
-                   FusedArgs args, bool persistent) {
+                   FusedArgs args, bool persistent, int max_ctas = 0) {
   constexpr int kPair = Cfg<MODE>::kPair;
   constexpr size_t smem = smem_bytes<MODE>();
   static_assert(MODE == kFX || Cfg<kFW>::kEntries == Cfg<kFW>::kAStages, "fw slots");
@@ -957,6 +960,7 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
         if (wave < grid) grid = wave;
       }
     }
+    if (max_ctas > 0 && grid > static_cast<unsigned>(max_ctas)) grid = static_cast<unsigned>(max_ctas);
     fused_kernel<MODE><<<grid, kThreads, smem, stream>>>(a, b, c, d, e, out, args);
     return cudaGetLastError();
   } else {
@@ -1007,16 +1011,14 @@ FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
 
 cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, const uint16_t* w_g,
                            const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
-                           int64_t N, cudaStream_t stream) {
-  constexpr int kPair = Cfg<kFX>::kPair;
+                           int64_t N, cudaStream_t stream, int64_t tile_begin, int64_t tile_end, int max_ctas) {
   CUtensorMap mdy, mg, mfc, mw0, mw1, mdx;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mdx, dx, K, M, static_cast<uint64_t>(K) * 2, 32, 32, 64)) return cudaErrorInvalidValue;
   // the raw tensors are only prefetched into L2 here, one stage's box at a time
   if (!encode_tmap_2d_bf16(&mdy, dy, N, M, rs, 64, 128, 0) || !encode_tmap_2d_bf16(&mg, g, N, M, rs, 64, 128, 0) ||
       !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 64, 128, 0) ||
-      !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256 / kPair) ||
-      !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256 / kPair))
+      !encode_tmap_2d_bf16(&mw0, w_g, N, K, rs, 64, 256) || !encode_tmap_2d_bf16(&mw1, w_fc, N, K, rs, 64, 256))
     return cudaErrorInvalidValue;
   FusedArgs a{};
   a.M = static_cast<int>(M);
@@ -1033,9 +1035,19 @@ cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t
   const Injection inj = take_injection(2);
   a.wait_limit = inj.wait_limit;
   a.stall_at = inj.stall_at;
-  const int64_t mpairs = ((M + 127) / 128 + kPair - 1) / kPair;  // tail CTAs run on zero-filled rows
-  return launch<kFX>(static_cast<unsigned>(mpairs * kPair * a.tiles_k), stream, mdy, mg, mfc, mw0, mw1, mdx, a,
-                     true);
+  const int64_t tiles = fused_x_tiles(M, K);
+  if (tile_end < 0 || tile_end > tiles) tile_end = tiles;
+  if (tile_begin < 0 || tile_begin >= tile_end) return cudaSuccess;  // nothing in the range
+  a.tile0 = static_cast<int>(tile_begin);
+  return launch<kFX>(static_cast<unsigned>(tile_end - tile_begin), stream, mdy, mg, mfc, mw0, mw1, mdx, a, true,
+                     max_ctas);
+}
+
+int64_t fused_x_tiles(int64_t M, int64_t K) { return (M + 127) / 128 * ((K + 511) / 512); }
+
+int64_t fused_w_ctas(int64_t K, int64_t N, const FwPlan& plan) {
+  constexpr int kPair = Cfg<kFW>::kPair;
+  return plan.splits * ((K + 511) / 512) * (((N + 63) / 64 + kPair - 1) / kPair * kPair);
 }
 
 namespace {

@@ -95,10 +95,16 @@ struct FwPlan {
 };
 // ws_bytes = split-M dw partials (when splits > 1) + db partials [splits][2N], 256-B aligned parts
 FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms);
-// dx (and optionally dg, dfc) from dy, g, fc, W
+// dx (and optionally dg, dfc) from dy, g, fc, W: the work tiles [tile_begin, tile_end) (tile t = m rows
+// 128 (t / tk) onwards at K block t % tk, tk = ceil(K / 512); tile_end < 0: to the last one) on one
+// persistent wave of at most max_ctas CTAs (0: as many as fit)
 cudaError_t launch_fused_x(const uint16_t* dy, const uint16_t* g, const uint16_t* fc, const uint16_t* w_g,
                            const uint16_t* w_fc, uint16_t* dx, uint16_t* dg, uint16_t* dfc, int64_t M, int64_t K,
-                           int64_t N, cudaStream_t stream);
+                           int64_t N, cudaStream_t stream, int64_t tile_begin = 0, int64_t tile_end = -1,
+                           int max_ctas = 0);
+int64_t fused_x_tiles(int64_t M, int64_t K);
+// CTAs of one fused w-stage launch under a plan
+int64_t fused_w_ctas(int64_t K, int64_t N, const FwPlan& plan);
 // dw and db from x, dy, g, fc; ws holds the split-M dw partials, then the db partials
 cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                            uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,

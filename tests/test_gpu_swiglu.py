@@ -266,3 +266,58 @@ def test_w_stage_many_tiles_per_cta():
     for k in ("dw_g", "dw_fc"):
         ref = 2.0 * to_f64(base[k])
         assert_all([compare(k, outs[k], ref)])
+
+
+@pytest.mark.gpu
+def test_fused_chain_side_split_matches_stage_calls():
+    """At M = 100000, K = 512, N = 1024 the fused whole-backward call runs the x stage's last tiles
+    beside the w stage (the w stage leaves SMs free and the x stage needs six waves): every output
+    must equal the two stage calls' bit for bit. The outputs start filled with a value no result
+    takes, so a tile the split left out would show."""
+    swg = _swg()
+    shape = SwigluShape("split_M100000", 100000, 512, 1024, 11, "pages")
+    inp = swiglu_inputs(shape, device="cuda")
+    M, K, N = shape.M, shape.K, shape.N
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), **bf)
+    swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"], dx)
+    dwg, dwfc = torch.empty((K, N), **bf), torch.empty((K, N), **bf)
+    dbg, dbfc = torch.empty((1, N), **bf), torch.empty((1, N), **bf)
+    ws = torch.empty(max(swg.swiglu_bwd_w_fused_workspace_size(M, K, N), 16), dtype=torch.uint8, device="cuda")
+    swg.swiglu_bwd_w_fused(inp["x"], inp["dy"], inp["g"], inp["fc"], dwg, dwfc, dbg, dbfc, workspace=ws)
+    out = {"dx": torch.full((M, K), 3.0e38, **bf), "dw_g": torch.full((K, N), 3.0e38, **bf),
+           "dw_fc": torch.full((K, N), 3.0e38, **bf), "db_g": torch.full((1, N), 3.0e38, **bf),
+           "db_fc": torch.full((1, N), 3.0e38, **bf)}
+    swg.swiglu_bwd(**inp, fused=True, return_dg=False, out=out)
+    swg.swg_check()
+    for name, ref in (("dx", dx), ("dw_g", dwg), ("dw_fc", dwfc), ("db_g", dbg), ("db_fc", dbfc)):
+        assert torch.equal(out[name], ref), name
+
+
+@pytest.mark.gpu
+def test_fused_chain_side_split_in_cuda_graph():
+    """The side stream of the fused whole-backward call joins a CUDA graph capture and rejoins the
+    captured stream: a replay gives the eager call's outputs bit for bit."""
+    swg = _swg()
+    shape = SwigluShape("split_M100000", 100000, 512, 1024, 12, "pages")
+    inp = swiglu_inputs(shape, device="cuda")
+    eager = swg.swiglu_bwd(**inp, fused=True, return_dg=False)
+    swg.swg_check()
+    out = {k: torch.empty_like(v) for k, v in eager.items()}
+    ws = torch.empty(max(swg.swiglu_bwd_workspace_size(shape.M, shape.K, shape.N, swg.SWG_FUSED), 16), dtype=torch.uint8,
+                     device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm the call up outside the capture
+        swg.swiglu_bwd(**inp, fused=True, return_dg=False, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        swg.swiglu_bwd(**inp, fused=True, return_dg=False, out=out, workspace=ws)
+    for v in out.values():
+        v.fill_(3.0e38)
+    graph.replay()
+    torch.cuda.synchronize()
+    swg.swg_check()
+    for k, v in eager.items():
+        assert torch.equal(out[k], v), k
