@@ -247,6 +247,12 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc,
                       unsigned flags, void* workspace, size_t workspace_bytes,
                       swg_stream_t stream);
 
+/* The number of kernels one swiglu_bwd(..., M, K, N, flags, ...) call launches
+ * on the current device: 0 for a call that launches none (M == 0 clears its
+ * outputs with memsets; K or N == 0; invalid arguments). Launches nothing; for
+ * launch accounting and profiling. */
+int swiglu_bwd_kernel_count(int64_t M, int64_t K, int64_t N, unsigned flags);
+
 /* ---- whole fused backward from host buffers ------------------------------------
  * The whole backward of swiglu_bwd(..., SWG_FUSED, ...) (dx, dw_g, dw_fc, db_g,
  * db_fc; dg and dfc are not produced) with every tensor argument in HOST

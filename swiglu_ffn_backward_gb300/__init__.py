@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     swiglu_bwd_b_workspace_size,
     swiglu_bwd_host,
     swiglu_bwd_host_workspace_size,
+    swiglu_bwd_kernel_count,
     swiglu_bwd_w,
     swiglu_bwd_w_workspace_size,
     swiglu_bwd_workspace_size,

@@ -41,7 +41,7 @@ EXPORTS = (
     "swiglu_bwd_b_workspace_size", "swiglu_bwd_b",
     "swiglu_bwd_w_workspace_size", "swiglu_bwd_w",
     "swiglu_bwd_x",
-    "swiglu_bwd_workspace_size", "swiglu_bwd",
+    "swiglu_bwd_workspace_size", "swiglu_bwd", "swiglu_bwd_kernel_count",
     "swish_grad",
     "swiglu_bwd_b_noalloc",
     "swiglu_bwd_x_fused",
@@ -98,6 +98,8 @@ def _load() -> ctypes.CDLL:
     lib.act_grad.restype = st
     lib.swiglu_bwd_workspace_size.argtypes = [I64, I64, I64, U]
     lib.swiglu_bwd_workspace_size.restype = SZ
+    lib.swiglu_bwd_kernel_count.argtypes = [I64, I64, I64, U]
+    lib.swiglu_bwd_kernel_count.restype = ctypes.c_int
     lib.swiglu_bwd.argtypes = [P] * 13 + [I64, I64, I64, U, P, SZ, P]
     lib.swiglu_bwd.restype = st
     lib.swish_grad.argtypes = [P, P, ctypes.POINTER(ctypes.c_float), P, I64, ctypes.c_int, P]
@@ -266,6 +268,11 @@ def swiglu_bwd_b_workspace_size(M: int, N: int) -> int:
 
 def swiglu_bwd_w_workspace_size(M: int, K: int, N: int) -> int:
     return lib.swiglu_bwd_w_workspace_size(M, K, N)
+
+
+def swiglu_bwd_kernel_count(M: int, K: int, N: int, flags: int = SWG_UNFUSED) -> int:
+    """How many kernels one swiglu_bwd call with these sizes and flags launches on the current device."""
+    return lib.swiglu_bwd_kernel_count(M, K, N, flags)
 
 
 def swiglu_bwd_workspace_size(M: int, K: int, N: int, flags: int = SWG_UNFUSED) -> int:

@@ -678,6 +678,21 @@ size_t swiglu_bwd_workspace_size(int64_t M, int64_t K, int64_t N, unsigned flags
   return total;
 }
 
+int swiglu_bwd_kernel_count(int64_t M, int64_t K, int64_t N, unsigned flags) {
+  if ((flags & ~(SWG_FUSED | SWG_ACCUMULATE | SWG_WS_DG_GIVEN | SWG_AUTO)) != 0) return 0;
+  if (check_shape(M, K, N) != SWG_OK || M <= 0 || K == 0 || N == 0) return 0;
+  flags = resolve_auto(M, K, flags);
+  const int sms = swg::device_sm_count();
+  if (flags & SWG_FUSED) {
+    const swg::FwPlan fplan = swg::fw_plan(M, K, N, sms);
+    const FxSplit sp = fx_split(M, K, N, fplan, sms);
+    // x stage (one or two launches), w stage, its dw split reduce, its db reduce
+    return (sp.side_tiles > 0 ? 2 : 1) + 1 + (fplan.splits > 1 ? 1 : 0) + 1;
+  }
+  // b stage and its db reduce, w GEMM and its split reduce, x GEMM
+  return 2 + 1 + (swg::w_plan(M, K, N, sms).splits > 1 ? 1 : 0) + 1;
+}
+
 swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const void* dy, const void* g,
                       const void* fc, void* dg, void* dfc, void* dx, void* dw_g, void* dw_fc, void* db_g,
                       void* db_fc, int64_t M, int64_t K, int64_t N, unsigned flags, void* workspace,
