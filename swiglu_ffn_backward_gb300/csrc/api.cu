@@ -686,8 +686,8 @@ int swiglu_bwd_kernel_count(int64_t M, int64_t K, int64_t N, unsigned flags) {
   if (flags & SWG_FUSED) {
     const swg::FwPlan fplan = swg::fw_plan(M, K, N, sms);
     const FxSplit sp = fx_split(M, K, N, fplan, sms);
-    // x stage (one or two launches), w stage, its dw split reduce, its db reduce
-    return (sp.side_tiles > 0 ? 2 : 1) + 1 + (fplan.splits > 1 ? 1 : 0) + 1;
+    // x stage (one or two launches), w stage, its dw and db reductions (one launch)
+    return (sp.side_tiles > 0 ? 2 : 1) + 1 + 1;
   }
   // b stage and its db reduce, w GEMM and its split reduce, x GEMM
   return 2 + 1 + (swg::w_plan(M, K, N, sms).splits > 1 ? 1 : 0) + 1;

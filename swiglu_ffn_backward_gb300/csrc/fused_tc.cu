@@ -990,6 +990,54 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
 
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// The w stage's two reductions in one launch. Blocks [0, dw_blocks) add the dw split partials
+// ws[s][p][k][n] in split order in fp32 and round once to bf16 (with accumulate, the old dw value
+// joins the fp32 sum before the rounding); the other blocks add the db partials db_part[s][2N] in
+// fp64 -- per column the splits s = r, r + 32, ... summed for each r < 32, those 32 sums then added
+// in order -- and round once to bf16. The same arithmetic as the separate dw and db reduces.
+__global__ void __launch_bounds__(256) fw_reduce_kernel(const float4* __restrict__ ws, int splits,
+                                                        int64_t per_prob4, uint2* __restrict__ dw_g,
+                                                        uint2* __restrict__ dw_fc, const float* __restrict__ db_part,
+                                                        int64_t N, uint16_t* __restrict__ db_g,
+                                                        uint16_t* __restrict__ db_fc, int accumulate,
+                                                        int dw_blocks) {
+  if (static_cast<int>(blockIdx.x) < dw_blocks) {
+    const int64_t total4 = 2 * per_prob4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
+         i += static_cast<int64_t>(dw_blocks) * blockDim.x) {
+      float4 acc = ws[i];
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 v = ws[static_cast<int64_t>(sp) * total4 + i];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      uint2* dst = i < per_prob4 ? dw_g + i : dw_fc + (i - per_prob4);
+      if (accumulate) {
+        const uint2 old = *dst;
+        *dst = make_uint2(add_pack_bf16x2(acc.x, acc.y, old.x), add_pack_bf16x2(acc.z, acc.w, old.y));
+      } else {
+        *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      }
+    }
+    return;
+  }
+  const int64_t two_n = 2 * N;
+  const int64_t j = static_cast<int64_t>(static_cast<int>(blockIdx.x) - dw_blocks) * blockDim.x + threadIdx.x;
+  if (j >= two_n) return;
+  double t = 0.0;
+  for (int r = 0; r < 32 && r < splits; ++r) {
+    double sr = 0.0;
+    for (int sp = r; sp < splits; sp += 32) sr += static_cast<double>(db_part[static_cast<int64_t>(sp) * two_n + j]);
+    t += sr;
+  }
+  uint16_t* dst = j < N ? db_g + j : db_fc + (j - N);
+  if (accumulate) t += static_cast<double>(__uint_as_float(static_cast<uint32_t>(*dst) << 16));
+  const __nv_bfloat16 b = __double2bfloat16(t);
+  *dst = *reinterpret_cast<const uint16_t*>(&b);
+}
+
 }  // namespace
 
 FwPlan fw_plan(int64_t M, int64_t K, int64_t N, int num_sms) {
@@ -1099,11 +1147,16 @@ cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t
   float* db_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(dw_bytes));
   cudaError_t e = launch_fw_kernel(x, dy, g, fc, dw_g, dw_fc, M, K, N, dw_part, db_part, plan, stream, accumulate);
   if (e != cudaSuccess) return e;
-  if (plan.splits > 1) {
-    e = launch_w_split_reduce(dw_part, plan.splits, K, N, dw_g, dw_fc, stream, accumulate);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_db_reduce(db_part, plan.splits, N, db_g, db_fc, stream, accumulate);
+  // both reductions in one launch (with one split the kernel wrote dw itself)
+  const int64_t per_prob4 = K * N / 4;
+  int64_t dw_blocks = plan.splits > 1 ? (2 * per_prob4 + 255) / 256 : 0;
+  if (dw_blocks > 4096) dw_blocks = 4096;
+  const int64_t db_blocks = (2 * N + 255) / 256;
+  fw_reduce_kernel<<<static_cast<unsigned>(dw_blocks + db_blocks), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(dw_part), static_cast<int>(plan.splits), per_prob4,
+      reinterpret_cast<uint2*>(dw_g), reinterpret_cast<uint2*>(dw_fc), db_part, N, db_g, db_fc, accumulate ? 1 : 0,
+      static_cast<int>(dw_blocks));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fused_w_partials(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
