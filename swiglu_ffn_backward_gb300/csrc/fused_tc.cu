@@ -79,7 +79,7 @@ struct Cfg<kFX> {
   static constexpr int kAStages = 3;       // A-operand slots (dg + dfc, 2 x 16 KB each)
   static constexpr int kEntryBytes = 32768;  // W_g or W_fc [256 k x 64 n]
   static constexpr int kEntries = 4;
-  static constexpr int kPrefetch = 8;      // stages prefetched into L2 ahead of the loads
+  static constexpr int kPrefetch = 4;      // stages prefetched into L2 ahead of the loads
 };
 template <>
 struct Cfg<kFW> {
