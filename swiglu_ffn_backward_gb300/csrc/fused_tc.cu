@@ -62,7 +62,6 @@ namespace {
 enum FusedMode : int { kFX = 0, kFW = 1 };
 
 constexpr int kThreads = 384;
-constexpr int kXThreads = 256;  // transform / epilogue threads (warps 4-11)
 constexpr int kXWarp0 = 4;      // first transform warp
 constexpr int kXWarps = 8;
 constexpr int kCtlRegs = 48;    // registers per thread in warpgroup 0 after setmaxnreg
@@ -457,8 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           umma_bf16(d, ad, bd, idesc, acc);
       };
-      auto consume = [&](int i, int p, int h, int nh_unused) -> bool {
-        (void)nh_unused;
+      auto consume = [&](int i, int p, int h) -> bool {
         const int e = gj % kRE;
         if (!mbar_wait(&s.ring_full[e], (gj / kRE) & 1, args.wait_limit)) {
           flag_timeout(s, args.status);
@@ -514,22 +512,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (J == 0 && !wait_free(1)) break;
           for (int i = 0; i < J && ok; ++i) {
             ok = wait_a(i);
-            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 0, 0);
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 0);
           }
           if (ok && J > 0) ok = wait_free(1);
           for (int i = 0; i < J && ok; ++i) {
-            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 1, 0);
+            for (int p = 0; p < 2 && ok; ++p) ok = consume(i, p, 1);
             commit2(&s.a_empty[(gi + i) % kAS]);
           }
           for (int i = J; i < tl.nst && ok; ++i) {
             ok = wait_a(i);
-            for (int q = 0; q < tl.eps && ok; ++q) ok = consume(i, q / tl.nh, q % tl.nh, 0);
+            for (int q = 0; q < tl.eps && ok; ++q) ok = consume(i, q / tl.nh, q % tl.nh);
             commit2(&s.a_empty[(gi + i) % kAS]);
           }
         } else {
           if (!wait_free(0) || !wait_free(1)) break;
           for (int i = 0; i < tl.nst && ok; ++i) {
-            ok = consume(i, 0, tl.nh, 0);
+            ok = consume(i, 0, tl.nh);
           }
         }
         gi += tl.nst;
