@@ -236,27 +236,6 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(const volatile uint32_t* p, u
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait with cluster-scope acquire: the barrier collects arrivals of both CTAs
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, long long limit) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_cluster(a, parity)) {
-    if (clock64() - t0 > limit) return false;
-  }
-  return true;
-}
 // 2-D / 3-D tiled load into this CTA's shared memory, completion counted on the
 // pair leader's mbarrier (shared::cluster address)
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1) {
