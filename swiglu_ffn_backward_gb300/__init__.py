@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     status_string,
     swg_check,
     swg_inject_stall,
+    SWG_INJECT_FUSED_W,
     SWG_INJECT_FUSED_X,
     SWG_INJECT_X_GEMM,
     swiglu_bwd,

@@ -233,6 +233,18 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(const volatile uint32_t* p, u
 // address. The data the arrival announces is consumed through the async proxy (the
 // tensor core reads this CTA's own shared memory; the writer fences its stores to the
 // async proxy first), so the default release at CTA scope suffices.
+// has the phase with the given parity completed? (a non-blocking look)
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -568,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool dead = false;
 
     // arrival of this warp on a barrier of the pair leader (after its lanes' work)
-    auto warp_arrive_leader = [&](uint64_t* bar) {
+    auto warp_arrive_leader = [&](uint64_t* bar, bool may = true) {
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && may) {
         if (kPair == 1 || leader)
           mbar_arrive(bar);
         else
@@ -767,7 +779,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int a = gs % kAS;
           acquire_slot(gs, a);
           if (!dead) store_stage(a, (kb_begin + i) * 64, n0 + c * 8, false, bdy, bg, bfc, cg, cf);
-          warp_arrive_leader(&s.ring_full[a]);
+          // The slot's barrier also counts the producer's copies. A warp whose wait ran out (lane 0
+          // decides) arrives only where the slot's previous use was released: that use's phase
+          // completed, so this arrival falls into the phase of stage gs, and an arrival can never
+          // overrun a phase that a missing copy left open.
+          const bool may = lane != 0 || !dead || gs < static_cast<uint32_t>(kAS) ||
+                           mbar_test(smem_u32(&s.ring_empty[a]), ((gs / kAS) - 1) & 1);
+          warp_arrive_leader(&s.ring_full[a], may);
           if (t == 0) s.x_progress = gs + 1;
         };
 
@@ -1108,8 +1126,9 @@ cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16
   a.nkb_total = static_cast<int>((M + 63) / 64);
   a.tiles_n = static_cast<int>(((N + 63) / 64 + kPair - 1) / kPair * kPair);  // pairs of 64-column bands
   a.accumulate = accumulate ? 1 : 0;
-  a.wait_limit = kWaitLimitCycles;
-  a.stall_at = -1;
+  const Injection inj = take_injection(3);
+  a.wait_limit = inj.wait_limit;
+  a.stall_at = inj.stall_at;
   const int64_t ctas = plan.splits * a.tiles_k * a.tiles_n;
   return launch<kFW>(static_cast<unsigned>(ctas), stream, mdy, mg, mfc, mx, mx, mx, a, false);
 }

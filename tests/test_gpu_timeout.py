@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from synth import SWIGLU_CONFIGS, swiglu_inputs
+from synth import SWIGLU_CONFIGS, SwigluShape, swiglu_inputs
 
 from ._parity import assert_all, compare, to_f64
 
@@ -30,6 +30,7 @@ def test_injection_arguments_are_checked():
     assert b.lib.swg_inject_stall(b.SWG_INJECT_X_GEMM, 1, 100) == b.SWG_ERR_PARAM_INVALID
     # arming and disarming touches host state only
     assert b.lib.swg_inject_stall(b.SWG_INJECT_FUSED_X, 3, LIMIT) == b.SWG_OK
+    assert b.lib.swg_inject_stall(b.SWG_INJECT_FUSED_W, 0, LIMIT) == b.SWG_OK
     assert b.lib.swg_inject_stall(0, 0, 0) == b.SWG_OK
 
 
@@ -75,4 +76,26 @@ def test_fused_x_wait_runs_out(entry):
     h = {k: to_f64(v) for k, v in inp.items()}
     rdx = oracle.swiglu_bwd_x(to_f64(out["dg"]), to_f64(out["dfc"]), h["w_g"], h["w_fc"])
     assert_all([compare("dx", out["dx"], rdx)])
+    torch.cuda.synchronize()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("entry", [0, 1, 3])
+def test_fused_w_wait_runs_out(entry):
+    """The fused w kernel runs on CTA pairs (M=2048 K=64 N=128: four M-splits of one pair of
+    64-column bands, eight stages per CTA, four stage slots). Both CTAs' producers stop before the
+    entry; the leader's MMA wait runs out; the transform warps' waits for the slots of the stages
+    four on run out too, and those warps arrive only on slots whose previous use was released; both
+    CTAs meet at the final cluster barrier. A normal call afterwards passes."""
+    swg = _swg()
+    shape = SwigluShape("fw_stall_M2048", 2048, 64, 128, 9, "tail")
+    inp = swiglu_inputs(shape, device="cuda")
+    swg.swg_inject_stall(swg.SWG_INJECT_FUSED_W, entry, LIMIT)
+    swg.swiglu_bwd_w_fused(inp["x"], inp["dy"], inp["g"], inp["fc"])
+    _expect_timeout(swg)
+    out = swg.swiglu_bwd(**inp, fused=True)
+    swg.swg_check()
+    h = {k: to_f64(v) for k, v in inp.items()}
+    rdwg, rdwfc = oracle.swiglu_bwd_w(h["x"], to_f64(out["dg"]), to_f64(out["dfc"]))
+    assert_all([compare("dw_g", out["dw_g"], rdwg), compare("dw_fc", out["dw_fc"], rdwfc)])
     torch.cuda.synchronize()
