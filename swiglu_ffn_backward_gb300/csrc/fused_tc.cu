@@ -7,7 +7,7 @@
 // recompute-instead-of-store principle stated in the Ascend C backward blog
 // post (Swish section: recompute sigma in the backward rather than keep it).
 //
-// Twelve warps per CTA, one CTA per SM:
+// One CTA per SM: warpgroup 0 and the transform warps (FX: sixteen, FW: eight).
 //   warp 0 lane 0   TMA producer of the operand ring (W chunks for FX, x chunks
 //                   for FW; 128-byte swizzle)
 //   warp 1          tensor-memory allocation (512 columns); lane 0 issues
@@ -16,14 +16,17 @@
 //   warp 2 lane 0   L2 prefetch of the raw dy, g, fc tiles a few stages ahead
 //                   of the transform, paced by the transform's progress count
 //   warp 3          idle
-//   warps 4-11      transform: load dy, g, fc straight from global memory into
-//                   registers (three stages of registers: the loads run two
-//                   stages ahead of the math), compute dg, dfc in fp32 and store
-//                   them as bf16 into a ring of A-operand slots in the 128-byte-
-//                   swizzled layout the tensor core reads; then the epilogue.
-// Warpgroup 0 (warps 0-3) gives registers to the two transform warpgroups
-// (setmaxnreg): 48 per thread there, 224 in the transform (a block of twelve
-// warps is otherwise held to 168 per thread, and the FX transform wants more).
+//   warps 4-        transform: load dy, g, fc straight from global memory into
+//                   registers (FX: two stages of registers, the loads running a
+//                   stage ahead of the math; FW: three), compute dg, dfc in fp32
+//                   and store them as bf16 into a ring of A-operand slots in the
+//                   128-byte-swizzled layout the tensor core reads; then the
+//                   epilogue.
+// Warpgroup 0 gives registers to the transform warpgroups (setmaxnreg): 48 per
+// thread there; FX's sixteen transform warps rise from the 96 a 640-thread
+// block is launched with to 104, FW's eight from 168 to 224. Sixteen FX warps
+// of two rows per stage with two register stages measured slightly faster than
+// eight of four rows with three.
 //
 // fused x (FX): one CTA per MMA (M = 128, N = 256), persistent over m tiles.
 //   D = dx[m0:m0+128, k0:k0+512] in two 256-column accumulator halves. Stages
@@ -61,11 +64,8 @@ namespace {
 
 enum FusedMode : int { kFX = 0, kFW = 1 };
 
-constexpr int kThreads = 384;
 constexpr int kXWarp0 = 4;      // first transform warp
-constexpr int kXWarps = 8;
 constexpr int kCtlRegs = 48;    // registers per thread in warpgroup 0 after setmaxnreg
-constexpr int kXRegs = 224;     // registers per thread in the transform warpgroups
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSplitStages = 2;  // FX: stages whose low-half MMAs run before the high half is free
 
@@ -73,6 +73,10 @@ template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kFX> {
+  static constexpr int kXWarps = 16;       // transform warps
+  static constexpr int kThreads = 640;
+  static constexpr int kLaunchRegs = 96;   // registers per thread at launch (65536 / 640, rounded down to 8)
+  static constexpr int kXRegs = 104;       // transform warps after setmaxnreg
   static constexpr int kPair = 1;          // CTAs per MMA: single-CTA tcgen05.mma
   static constexpr int kRows = 128;        // m rows of a stage's tile (64 columns of n)
   static constexpr int kAStages = 3;       // A-operand slots (dg + dfc, 2 x 16 KB each)
@@ -82,6 +86,10 @@ struct Cfg<kFX> {
 };
 template <>
 struct Cfg<kFW> {
+  static constexpr int kXWarps = 8;
+  static constexpr int kThreads = 384;
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kXRegs = 224;
   static constexpr int kPair = 2;          // CTAs per MMA: a cta_group::2 pair (M = 256)
   static constexpr int kRows = 64;         // m rows of a stage (64 columns of n)
   static constexpr int kAStages = 4;       // A-operand slots (dg | dfc stacked, 16 KB each)
@@ -211,8 +219,9 @@ __device__ __forceinline__ uint4 ldg_stream(const uint16_t* p) {
                : "l"(p));
   return v;
 }
+template <int XW>
 __device__ __forceinline__ void named_sync_transform() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * XW) : "memory");
 }
 
 // ---- pair primitives
@@ -317,7 +326,7 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* v) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_g,
                  const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_b0,
                  const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_out,
@@ -329,7 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kRE = C::kEntries;
   constexpr int kRows = C::kRows;
   constexpr int kHalf = S::kHalf;
-  constexpr int kRPT = kRows / 32;  // rows per transform thread per stage
+  constexpr int kXWarps = C::kXWarps;
+  constexpr int kRS = kXWarps * 4;     // row stride: transform threads per 8-column chunk
+  constexpr int kRPT = kRows / kRS;    // rows per transform thread per stage
   extern __shared__ uint8_t smem_raw[];
   S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -379,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
 
   if (warp < kXWarp0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs) : "memory");
+  static_assert(kRows % kRS == 0, "rows per transform thread");
 
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer (both CTAs)
@@ -568,12 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kXWarp0) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kXRegs) : "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kXRegs) : "memory");
     // ------------------------------------------------------------ transform (both CTAs)
-    const int t = threadIdx.x - kXWarp0 * 32;  // 0..255
-    const int xw = warp - kXWarp0;             // transform warp 0..7
+    const int t = threadIdx.x - kXWarp0 * 32;  // 0 .. 32 kXWarps - 1
+    const int xw = warp - kXWarp0;             // transform warp
     const int c = t & 7;                       // 16-byte chunk of the 64-column tile (8 columns)
-    const int rg = t >> 3;                     // row group 0..31; rows rg, rg + 32, ...
+    const int rg = t >> 3;                     // row group; rows rg, rg + kRS, ...
     const int64_t N64 = args.N;
     // A thread whose wait runs out stops computing ("dead") but keeps taking
     // part in the arrivals and the named barriers.
@@ -596,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sdf = sdg + kHalf;
 #pragma unroll
       for (int q = 0; q < kRPT; ++q) {
-        const int row = rg + 32 * q;  // row within the tile
+        const int row = rg + kRS * q;  // row within the tile
         // 128-byte swizzle: the 16-byte chunk index is XORed with row & 7
         const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
         uint4 odg, odfc;
@@ -618,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          uint4 (&bfc)[kRPT]) {
 #pragma unroll
       for (int q = 0; q < kRPT; ++q) {
-        const int row = row0 + rg + 32 * q;
+        const int row = row0 + rg + kRS * q;
         if (valid && row < args.M && col < args.N) {  // tails read as zeros
           const int64_t o = static_cast<int64_t>(row) * N64 + col;
           bdy[q] = ldg_stream(args.dy + o);
@@ -700,7 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!acc_ok) flag_timeout(s, args.status);
         }
         const int q = warp & 3;    // TMEM lane quarter this warp may read
-        const int sub = xw >> 2;   // 128-column half of each accumulator half
+        // the warps of a lane quarter split each 256-column accumulator half into kSubW-column parts
+        constexpr int kSubW = 256 / (kXWarps / 4);
+        constexpr int kStgBufs = (2 * kHalf / kXWarps) / 2048;  // 2 KB staging blocks per warp
+        static_assert(kStgBufs >= 1, "staging");
+        const int sub = xw >> 2;
         tc_fence_after();
         // tcgen05.ld is warp-collective: decide for the whole warp
         const bool go = __all_sync(0xffffffffu, !dead && acc_ok && !s.abort_flag);
@@ -708,15 +724,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           if (go && h < tl.nh) {
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc, ++nb) {
+            for (int cc = 0; cc < kSubW / 32; ++cc, ++nb) {
               uint32_t v[32];
-              tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + sub * 128 + cc * 32, v);
+              tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 256 + sub * kSubW + cc * 32, v);
               tmem_ld_wait();
               // this warp's 32 x 32 block -> a 64-byte-swizzled staging buffer -> one TMA
               // store (rows beyond M and columns beyond K are clipped by the copy engine)
-              uint8_t* buf = s.aop[stg] + xw * 4096 + (nb & 1) * 2048;
-              if (nb >= 2) {
-                if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+              uint8_t* buf = s.aop[stg] + xw * (2048 * kStgBufs) + (nb % kStgBufs) * 2048;
+              if (nb >= kStgBufs) {
+                if (lane == 0) bulk_wait_read<kStgBufs - 1>();  // the store that used this buffer has read it
                 __syncwarp();
               }
               const uint32_t sb = smem_u32(buf) + lane * 64;
@@ -725,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tm_out, buf, tl.k0 + h * 256 + sub * 128 + cc * 32, tl.m0 + q * 32);
+                tma_store_2d(&tm_out, buf, tl.k0 + h * 256 + sub * kSubW + cc * 32, tl.m0 + q * 32);
                 bulk_commit();
               }
             }
@@ -735,28 +751,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the staging slot is written again by a later stage: every store has read it
         if (lane == 0) bulk_wait_read<0>();
-        named_sync_transform();
+        named_sync_transform<kXWarps>();
       };
       auto after = [&]() {
         if (pc.tix >= 1 && pc.sit + 1 == look) epilogue(pc.tix - 1, (pc.tix * nst - 1) % kAS);
         advance(pc);
       };
 
-      // three stages of registers: the loads of stages st + 1 and st + 2 are in
-      // flight while stage st is computed (and while an epilogue runs)
+      // two stages of registers: the loads of stage st + 1 are in flight while stage
+      // st is computed (and while an epilogue runs)
       load(xdy, xg, xfc);
-      load(ydy, yg, yfc);
-      for (int st = 0; st < total; st += 3) {
-        load(zdy, zg, zfc);
+      for (int st = 0; st < total; st += 2) {
+        load(ydy, yg, yfc);
         process(xdy, xg, xfc);
         after();
         if (st + 1 >= total) break;
         load(xdy, xg, xfc);
         process(ydy, yg, yfc);
-        after();
-        if (st + 2 >= total) break;
-        load(ydy, yg, yfc);
-        process(zdy, zg, zfc);
         after();
       }
       if (ntiles > 0) epilogue(ntiles - 1, (total - 1) % kAS);
@@ -819,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 8);
             cf[e] += __shfl_xor_sync(0xffffffffu, cf[e], 16);
           }
-          named_sync_transform();
+          named_sync_transform<kXWarps>();
           float* scratch = reinterpret_cast<float*>(s.aop[0]);  // [8 warps][8 chunks][16]
           if (lane < 8) {
             float* pp = scratch + (xw * 8 + c) * 16;
@@ -829,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pp[8 + e] = cf[e];
             }
           }
-          named_sync_transform();
+          named_sync_transform<kXWarps>();
           if (t < 128) {
             const int which = t >> 6;  // 0: dg, 1: dfc
             const int col = t & 63;
@@ -841,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               args.db_part[static_cast<int64_t>(split) * 2 * args.N + which * args.N + gc] = v;
             }
           }
-          named_sync_transform();  // the scratch is read before a later tile's stage reuses the slot
+          named_sync_transform<kXWarps>();  // the scratch is read before a later tile's stage reuses the slot
         }
 
         // ---------------------------------------------------------- epilogue
@@ -928,7 +939,10 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
   constexpr size_t smem = smem_bytes<MODE>();
   static_assert(MODE == kFX || Cfg<kFW>::kEntries == Cfg<kFW>::kAStages, "fw slots");
   static_assert(smem <= 232448, "fused kernel shared memory");
-  static_assert(128 * kCtlRegs + 256 * kXRegs <= kThreads * 168, "setmaxnreg split exceeds a 168-register launch");
+  using C = Cfg<MODE>;
+  constexpr int kThreads = C::kThreads;
+  static_assert(128 * kCtlRegs + (kThreads - 128) * C::kXRegs <= kThreads * C::kLaunchRegs,
+                "setmaxnreg split exceeds the launch's registers");
   cudaError_t err = cudaFuncSetAttribute(fused_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -940,7 +954,7 @@ cudaError_t launch(unsigned grid, cudaStream_t stream, const CUtensorMap& a, con
     cudaFuncAttributes fa;
     err = cudaFuncGetAttributes(&fa, fused_kernel<MODE>);
     if (err != cudaSuccess) return err;
-    if (static_cast<long long>(fa.numRegs) * kThreads < 128LL * kCtlRegs + 256LL * kXRegs)
+    if (static_cast<long long>(fa.numRegs) * kThreads < 128LL * kCtlRegs + (kThreads - 128LL) * C::kXRegs)
       return cudaErrorInvalidValue;
   }
   args.cluster_tiles = static_cast<int>(grid / kPair);
