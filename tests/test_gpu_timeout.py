@@ -66,7 +66,7 @@ def test_x_gemm_wait_runs_out(entry):
 @pytest.mark.parametrize("entry", [0, 1, 3])
 def test_fused_x_wait_runs_out(entry):
     swg = _swg()
-    shape = SWIGLU_CONFIGS["tiny"][0]  # one tile per CTA, two stages of four ring entries
+    shape = SWIGLU_CONFIGS["tiny"][0]  # one tile per CTA: two stages, four ring entries in all
     inp = swiglu_inputs(shape, device="cuda")
     swg.swg_inject_stall(swg.SWG_INJECT_FUSED_X, entry, LIMIT)
     swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"])
