@@ -240,8 +240,9 @@ swg_status swiglu_fwd(const void* x, const void* w_g, const void* w_fc,
  * than one wave of tiles, the x stage's last tiles run beside the w stage on a
  * library-owned side stream (forked from and joined back into `stream` within
  * the call, so the call stays ordered on `stream` and can be captured in a CUDA
- * graph) and the rest after it; every output is bit-identical to the two stage
- * calls.
+ * graph) and the rest after it; the w stage's split reduction then also runs on
+ * the side stream, in blocks that fit beside the x stage's persistent wave.
+ * Every output is bit-identical to the two stage calls.
  * Workspace: swiglu_bwd_workspace_size(M, K, N, flags) bytes; with non-NULL
  * dg/dfc the smaller figure swiglu_bwd_workspace_size(M, K, N, flags |
  * SWG_WS_DG_GIVEN) suffices. */

@@ -648,7 +648,7 @@ FxSplit fx_split(int64_t M, int64_t K, int64_t N, const swg::FwPlan& plan, int s
 // the enqueue of one call holds the lock)
 struct SideStream {
   cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, fw_done = nullptr;
 };
 std::mutex g_side_mu;
 SideStream g_side[64];
@@ -659,6 +659,7 @@ cudaError_t side_stream(int dev, SideStream** out) {
     cudaError_t e = cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fw_done, cudaEventDisableTiming);
     if (e != cudaSuccess) return e;
   }
   *out = &h;
@@ -769,8 +770,20 @@ swg_status swiglu_bwd(const void* x, const void* w_g, const void* w_fc, const vo
     if (side_stream(dev, &ss) != cudaSuccess) return SWG_ERR_CUDA;
     cudaError_t e = cudaEventRecord(ss->fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->side, ss->fork, 0);
-    if (e == cudaSuccess) e = fw();
+    if (e == cudaSuccess)
+      e = swg::launch_fused_w_kernel(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
+                                     static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(fc),
+                                     static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc), M, K, N, wp, fplan,
+                                     s, acc);
+    if (e == cudaSuccess) e = cudaEventRecord(ss->fw_done, s);
     if (e == cudaSuccess) e = fx(ss->side, sp.main_tiles, sp.main_tiles + sp.side_tiles, sp.side_ctas);
+    // the w stage's reduction, too, goes on the side stream, in blocks small enough to run beside the
+    // x stage's persistent wave, so that it leaves the critical path
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->side, ss->fw_done, 0);
+    if (e == cudaSuccess)
+      e = swg::launch_fused_w_reduce(wp, fplan, K, N, static_cast<uint16_t*>(dw_g), static_cast<uint16_t*>(dw_fc),
+                                     static_cast<uint16_t*>(db_g), static_cast<uint16_t*>(db_fc), ss->side, acc,
+                                     sms);
     if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->side);
     if (e == cudaSuccess) e = fx(s, 0, sp.main_tiles, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);

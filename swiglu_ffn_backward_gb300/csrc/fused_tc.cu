@@ -1004,7 +1004,9 @@ inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 // joins the fp32 sum before the rounding); the other blocks add the db partials db_part[s][2N] in
 // fp64 -- per column the splits s = r, r + 32, ... summed for each r < 32, those 32 sums then added
 // in order -- and round once to bf16. The same arithmetic as the separate dw and db reduces.
-__global__ void __launch_bounds__(256) fw_reduce_kernel(const float4* __restrict__ ws, int splits,
+// At most 32 registers a thread: a 64-thread block then fits on an SM beside a CTA of the fused x
+// stage (640 threads of 96 registers leave 1024 registers on each SM sub-partition).
+__global__ void __launch_bounds__(256, 8) fw_reduce_kernel(const float4* __restrict__ ws, int splits,
                                                         int64_t per_prob4, uint2* __restrict__ dw_g,
                                                         uint2* __restrict__ dw_fc, const float* __restrict__ db_part,
                                                         int64_t N, uint16_t* __restrict__ db_g,
@@ -1149,24 +1151,53 @@ cudaError_t launch_fw_kernel(const uint16_t* x, const uint16_t* dy, const uint16
 
 }  // namespace
 
-cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
-                           uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
-                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+namespace {
+void fw_parts(void* ws, const FwPlan& plan, int64_t K, int64_t N, float** dw_part, float** db_part) {
   const size_t dw_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * 2 * K * N * sizeof(float) : 0;
-  float* dw_part = static_cast<float*>(ws);
-  float* db_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(dw_bytes));
-  cudaError_t e = launch_fw_kernel(x, dy, g, fc, dw_g, dw_fc, M, K, N, dw_part, db_part, plan, stream, accumulate);
-  if (e != cudaSuccess) return e;
-  // both reductions in one launch (with one split the kernel wrote dw itself)
+  *dw_part = static_cast<float*>(ws);
+  *db_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(dw_bytes));
+}
+}  // namespace
+
+cudaError_t launch_fused_w_kernel(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                                  uint16_t* dw_g, uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws,
+                                  const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+  float *dw_part, *db_part;
+  fw_parts(ws, plan, K, N, &dw_part, &db_part);
+  return launch_fw_kernel(x, dy, g, fc, dw_g, dw_fc, M, K, N, dw_part, db_part, plan, stream, accumulate);
+}
+
+cudaError_t launch_fused_w_reduce(void* ws, const FwPlan& plan, int64_t K, int64_t N, uint16_t* dw_g,
+                                  uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, cudaStream_t stream,
+                                  bool accumulate, int beside_ctas) {
+  float *dw_part, *db_part;
+  fw_parts(ws, plan, K, N, &dw_part, &db_part);
   const int64_t per_prob4 = K * N / 4;
-  int64_t dw_blocks = plan.splits > 1 ? (2 * per_prob4 + 255) / 256 : 0;
-  if (dw_blocks > 4096) dw_blocks = 4096;
-  const int64_t db_blocks = (2 * N + 255) / 256;
-  fw_reduce_kernel<<<static_cast<unsigned>(dw_blocks + db_blocks), 256, 0, stream>>>(
+  // beside_ctas > 0: at most that many blocks of 64 threads (32 registers each, no shared memory), so that
+  // one fits on an SM beside a CTA of the x stage's persistent wave; the grid-stride loop takes the rest
+  int threads = 256;
+  int64_t cap = 4096;
+  if (beside_ctas > 0 && (2 * N + 63) / 64 < beside_ctas) {
+    threads = 64;
+    cap = beside_ctas - (2 * N + 63) / 64;
+  }
+  int64_t dw_blocks = plan.splits > 1 ? (2 * per_prob4 + threads - 1) / threads : 0;
+  if (dw_blocks > cap) dw_blocks = cap;
+  const int64_t db_blocks = (2 * N + threads - 1) / threads;
+  fw_reduce_kernel<<<static_cast<unsigned>(dw_blocks + db_blocks), static_cast<unsigned>(threads), 0, stream>>>(
       reinterpret_cast<const float4*>(dw_part), static_cast<int>(plan.splits), per_prob4,
       reinterpret_cast<uint2*>(dw_g), reinterpret_cast<uint2*>(dw_fc), db_part, N, db_g, db_fc, accumulate ? 1 : 0,
       static_cast<int>(dw_blocks));
   return cudaGetLastError();
+}
+
+cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                           uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
+                           int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate) {
+  cudaError_t e = launch_fused_w_kernel(x, dy, g, fc, dw_g, dw_fc, M, K, N, ws, plan, stream, accumulate);
+  if (e != cudaSuccess) return e;
+  // both reductions in one launch (with one split the kernel wrote dw itself)
+  return launch_fused_w_reduce(ws, plan, K, N, dw_g, dw_fc, db_g, db_fc, stream, accumulate, 0);
 }
 
 cudaError_t launch_fused_w_partials(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,

@@ -109,6 +109,16 @@ int64_t fused_w_ctas(int64_t K, int64_t N, const FwPlan& plan);
 cudaError_t launch_fused_w(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
                            uint16_t* dw_g, uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, int64_t M, int64_t K,
                            int64_t N, void* ws, const FwPlan& plan, cudaStream_t stream, bool accumulate = false);
+// the same in two parts, for a caller that runs the reduction on another stream: the kernel (dw, db
+// partials into ws; with one split it writes dw itself), then the reduction of ws into dw, db.
+// beside_ctas > 0 caps the reduction at that many 64-thread blocks that each fit beside a CTA of the
+// fused x stage (0: the grid of the one-stream form)
+cudaError_t launch_fused_w_kernel(const uint16_t* x, const uint16_t* dy, const uint16_t* g, const uint16_t* fc,
+                                  uint16_t* dw_g, uint16_t* dw_fc, int64_t M, int64_t K, int64_t N, void* ws,
+                                  const FwPlan& plan, cudaStream_t stream, bool accumulate);
+cudaError_t launch_fused_w_reduce(void* ws, const FwPlan& plan, int64_t K, int64_t N, uint16_t* dw_g,
+                                  uint16_t* dw_fc, uint16_t* db_g, uint16_t* db_fc, cudaStream_t stream,
+                                  bool accumulate, int beside_ctas);
 cudaError_t launch_w_split_reduce(const float* ws, int64_t splits, int64_t K, int64_t N, uint16_t* dw_g,
                                   uint16_t* dw_fc, cudaStream_t stream, bool accumulate = false);
 // the fused w stage's kernel alone (plan.splits >= 2): fp32 partials into dw_part [splits][2][K][N] and
