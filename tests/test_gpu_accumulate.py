@@ -5,7 +5,8 @@ The pages' b and w kernels add db and dw into outputs the caller zeroed
 micro-batches can be summed. With the flag, db_g, db_fc, dw_g, dw_fc become
 bf16(old + this call's sum) with one rounding; dx, dg, dfc are overwritten as
 without it. Checked here, for both chains, on shapes that take the direct
-bf16 epilogue (one M split) and the split-M reduction:
+bf16 epilogue (one M split) and the split-M reduction, and one that runs the
+fused chain's side stream (the w stage's reduction beside the x stage's wave):
 * db, dw against old + the oracle's sums (dw from the oracle's w stage fed the
   chain's own bf16 dg, dfc), within the output contract;
 * dx, dg, dfc bit-identical to a run without the flag;
@@ -24,8 +25,11 @@ from ._parity import assert_all, compare, to_f64
 pytestmark = pytest.mark.gpu
 
 SUMMED = ("db_g", "db_fc", "dw_g", "dw_fc")
+# M = 100000 at the pages' K, N takes the fused chain's side split: the x stage's last tiles and the
+# w stage's split reduction run on the library's side stream
 SHAPES = [SWIGLU_CONFIGS["tiny"][0], SWIGLU_CONFIGS["tail"][4],
-          SwigluShape("odd_M2_K520_N264", 2, 520, 264, 9, "tail")]
+          SwigluShape("odd_M2_K520_N264", 2, 520, 264, 9, "tail"),
+          SwigluShape("split_M100000", 100000, 512, 1024, 13, "pages")]
 
 
 def _swg():
