@@ -5,55 +5,60 @@
 // bf16 operands, fp32 accumulation in TMEM; g and fc are formed in fp32 with
 // the bias, y from those fp32 values, and each output is rounded once to bf16.
 //
-// One persistent tcgen05 GEMM, one CTA per SM, six warps:
-//   warp 0 lane 0   TMA producer: for every 64-wide block of K, the x tile
-//                   [128 m x 64 k] (K-major) and the W_g, W_fc tiles
-//                   [64 k x 128 n] (MN-major, two 64x64 boxes each) into a
-//                   4-deep ring, running across the CTA's tiles
-//   warp 1          TMEM allocation (512 columns = two accumulator buffers,
-//                   each g [128 x 128] | fc [128 x 128]); lane 0 issues
-//                   tcgen05.mma (M=128, N=256, K=16): the W_g and W_fc tiles
-//                   sit in four consecutive 64-column MN-major chunks, so one
-//                   instruction per K step computes both products from one
-//                   read of the x tile
-//   warps 2-5       epilogue: drain the finished buffer while the tensor core
-//                   fills the other one: bias (the tile's columns staged once
-//                   per tile in shared memory), SiLU, and per 32x32 block a
-//                   64-byte-swizzled staging buffer that the warp reads back
-//                   row-wise and stores with coalesced 16-byte global stores
-//                   (eight whole 64-byte row segments per instruction; rows
-//                   beyond M and columns beyond N are not written)
-// The CTA loops over output tiles [128 rows x 128 columns]; with K = 512 a
+// One persistent tcgen05 GEMM on CTA pairs (clusters of two, one pair per two
+// SMs), ten warps per CTA:
+//   warp 0 lane 0   TMA producer (both CTAs): for every 64-wide block of K,
+//                   this CTA's x rows [128 m x 64 k] (K-major) and its half of
+//                   the B operand [64 k x 128 n] (MN-major, two 64x64 boxes):
+//                   W_g in the leader, W_fc in the other CTA; a 6-deep ring
+//                   running across the pair's tiles, each stage's copies of
+//                   both CTAs counted on the leader's barrier
+//   warp 1          TMEM allocation (512 columns in each CTA = two accumulator
+//                   buffers, each g [128 x 128] | fc [128 x 128]); lane 0 of
+//                   the leader issues tcgen05.mma.cta_group::2 (M=256, N=256,
+//                   K=16): one instruction computes both products for the
+//                   pair's 256 rows, reading each W tile from one CTA only, so
+//                   each SM copies half the W bytes of a single-CTA tile
+//   warps 2-9       epilogue (both CTAs, each on its own 128 rows; two warps
+//                   per TMEM lane quarter, each on half of the tile's columns):
+//                   drain the finished buffer while the tensor cores fill the
+//                   other one: bias (the tile's columns staged once per tile in
+//                   shared memory), SiLU, and g, fc, y in turn through the
+//                   warp's 64-byte-swizzled 32x32 staging block, read back
+//                   row-wise and stored with coalesced 16-byte global stores
+//                   (rows beyond M and columns beyond N are not written)
+// The pair loops over output tiles [256 rows x 128 columns]; with K = 512 a
 // tile holds only eight K blocks, so the double-buffered accumulator is what
-// keeps the tensor core busy across tile boundaries.
+// keeps the tensor cores busy across tile boundaries.
 //
 // Every mbarrier wait is bounded; a timeout sets the module status word,
-// stops issuing, drains the CTA's own TMA copies, frees TMEM and returns.
+// stops issuing, drains the pair's TMA copies, frees TMEM and returns.
 #include "swg_device.cuh"
 #include "swg_launch.h"
 
 namespace swg {
 namespace {
 
-constexpr int BM = 128;   // rows of a tile
+constexpr int BM = 128;   // rows of a tile in each CTA of the pair
 constexpr int BN = 128;   // columns of n per product in a tile
 constexpr int BK = 64;    // reduction block
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;       // 16 KB
-constexpr int B_BYTES = 2 * BN * BK * 2;   // W_g | W_fc, 32 KB
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr uint32_t kTmemCols = 512;        // two buffers of [g | fc]
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB: this CTA's x rows
+constexpr int B_BYTES = BN * BK * 2;   // 16 KB: this CTA's half of [W_g | W_fc]
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr uint32_t kTmemCols = 512;    // two buffers of [g | fc] in each CTA
 
 struct __align__(1024) FwdSmem {
   uint8_t a[STAGES][A_BYTES];
   uint8_t b[STAGES][B_BYTES];
-  uint8_t stage[kEpiThreads / 32][3][2048];  // per epilogue warp: g, fc, y blocks [32 rows x 32 columns]
-  uint4 bias[kEpiThreads / 32][2][16];       // per epilogue warp: the tile's b_g, b_fc columns (8 per uint4)
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tmem_full[2];   // the tile's MMAs into this buffer are done
-  uint64_t tmem_empty[2];  // the epilogue has read this buffer out
+  uint8_t stage[kEpiWarps][2048];     // per epilogue warp: one [32 rows x 32 columns] block (g, fc, y in turn)
+  uint4 bias[kEpiWarps][2][16];       // per epilogue warp: the tile's b_g, b_fc columns (8 per uint4)
+  uint64_t full[STAGES];     // leader: both CTAs' copies of the stage have landed
+  uint64_t empty[STAGES];    // the pair MMAs reading the stage are done (committed to both CTAs)
+  uint64_t tmem_full[2];     // the tile's MMAs into this buffer are done (committed to both CTAs)
+  uint64_t tmem_empty[2];    // leader: both CTAs' epilogue warps have read this buffer out
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   volatile uint32_t issued, consumed;
@@ -64,7 +69,7 @@ struct FwdArgs {
   uint32_t* status;
   const uint16_t* bias[2]; // b_g, b_fc [N] or null
   uint16_t* out[3];        // g, fc, y [M, N]
-  int tiles, tiles_n, nkb;
+  int tiles, tiles_n, nkb; // pair tiles [256 rows x 128 columns], column tiles, K blocks
 };
 
 __device__ __forceinline__ void fwd_timeout(FwdSmem& s, uint32_t* status) {
@@ -94,6 +99,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   FwdSmem& s = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();  // rank in the pair
+  const bool leader = crank == 0;
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tmem_full[i], 1);
-      mbar_init(&s.tmem_empty[i], kEpiThreads);
+      mbar_init(&s.tmem_empty[i], 2 * kEpiWarps);
     }
     s.abort_flag = 0u;
     s.issued = s.consumed = 0u;
@@ -112,45 +121,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_wfc);
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&s.tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrival, commit or copy
   const uint32_t tmem = s.tmem_base;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const CUtensorMap* tw = leader ? &tm_wg : &tm_wfc;  // this CTA's half of the B operand
       uint32_t gj = 0;
-      for (int t = blockIdx.x; t < args.tiles && !s.abort_flag; t += gridDim.x) {
-        const int n0 = (t % args.tiles_n) * BN, m0 = (t / args.tiles_n) * BM;
+      for (int t = cluster; t < args.tiles && !s.abort_flag; t += nclusters) {
+        const int n0 = (t % args.tiles_n) * BN;
+        const int m0 = (t / args.tiles_n) * (2 * BM) + BM * static_cast<int>(crank);
         for (int kb = 0; kb < args.nkb && !s.abort_flag; ++kb, ++gj) {
           const int st = gj % STAGES;
           if (gj >= STAGES && !mbar_wait(&s.empty[st], ((gj / STAGES) - 1) & 1)) {
             fwd_timeout(s, args.status);
             break;
           }
-          mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+          // the leader's barrier counts both CTAs' copies of the stage
+          if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * (A_BYTES + B_BYTES));
+          const uint32_t full = cluster_addr(&s.full[st], 0);
           const int kr = kb * BK;
-          tma_load_2d(s.a[st], &tm_x, &s.full[st], kr, m0);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            tma_load_2d(s.b[st] + j * 8192, &tm_wg, &s.full[st], n0 + 64 * j, kr);
-            tma_load_2d(s.b[st] + 16384 + j * 8192, &tm_wfc, &s.full[st], n0 + 64 * j, kr);
-          }
+          tma_load_2d_pair(s.a[st], &tm_x, full, kr, m0);
+          tma_load_2d_pair(s.b[st], tw, full, n0, kr);
+          tma_load_2d_pair(s.b[st] + 8192, tw, full, n0 + 64, kr);
           s.issued = gj + 1;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, 2 * BN, 0, 1);  // A K-major, B = [W_g | W_fc] MN-major
+    if (lane == 0 && leader) {
+      // M = 256 over the pair, A K-major; B = [W_g (leader) | W_fc (other CTA)] MN-major
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, 2 * BN, 0, 1);
+      // a release goes to the barrier at the same offset in both CTAs
+      auto commit2 = [](uint64_t* bar) {
+        umma_commit_pair(cluster_addr(bar, 0));
+        umma_commit_pair(cluster_addr(bar, 1));
+      };
       uint32_t gj = 0, it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++it) {
+      for (int t = cluster; t < args.tiles && ok; t += nclusters, ++it) {
         const uint32_t buf = it & 1;
         if (it >= 2) {
           // the epilogue has read this buffer's previous tile out
@@ -160,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
-        const uint32_t d = tmem + buf * 256;  // g at d, fc at d + 128
+        const uint32_t d = tmem + buf * 256;  // in each CTA: g at d, fc at d + 128
         for (int kb = 0; kb < args.nkb; ++kb, ++gj) {
           const int st = gj % STAGES;
           if (!mbar_wait(&s.full[st], (gj / STAGES) & 1)) {
@@ -175,13 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-            // D[:, 0:128] = x W_g, D[:, 128:256] = x W_fc
-            umma_bf16(d, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024), idesc,
+            // D[:, 0:128] = x W_g, D[:, 128:256] = x W_fc, for the rows of each CTA
+            umma_pair(d, smem_desc(a_addr + 32 * k, 16, 1024), smem_desc(b_addr + 2048 * k, 8192, 1024), idesc,
                       acc);
           }
-          umma_commit(&s.empty[st]);
+          commit2(&s.empty[st]);
         }
-        if (ok) umma_commit(&s.tmem_full[buf]);
+        if (ok) commit2(&s.tmem_full[buf]);
       }
     }
   } else {
@@ -189,9 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     bool dead = false;
     uint32_t it = 0;
-    for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++it) {
+    for (int t = cluster; t < args.tiles; t += nclusters, ++it) {
       const uint32_t buf = it & 1;
-      const int n0 = (t % args.tiles_n) * BN, m0 = (t / args.tiles_n) * BM;
+      const int n0 = (t % args.tiles_n) * BN;
+      const int m0 = (t / args.tiles_n) * (2 * BM) + BM * static_cast<int>(crank);
       {
         // the tile's biases: lane l < 16 loads b_g columns n0 + 8l .. n0 + 8l + 7, lane 16 + l the same of b_fc
         // (zeros beyond N, where the store clips); read back below as warp-wide broadcasts
@@ -215,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tcgen05.ld is warp-collective: decide for the whole warp
       if (__all_sync(0xffffffffu, ready && !s.abort_flag)) {
         const uint32_t d = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
-        const uint32_t stg = smem_u32(s.stage[warp - 2][0]);
+        const uint32_t stg = smem_u32(s.stage[warp - 2]);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 2 * ((warp - 2) >> 2); c < 2 * ((warp - 2) >> 2) + 2; ++c) {
           uint32_t vg[32], vf[32];
           tmem_ld_32x32b_x32(d + c * 32, vg);
           tmem_ld_32x32b_x32(d + BN + c * 32, vf);
@@ -247,52 +265,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             rf[j] = make_uint4(of[0], of[1], of[2], of[3]);
             ry[j] = make_uint4(oy[0], oy[1], oy[2], oy[3]);
           }
-          __syncwarp();  // every lane has read the previous chunk back from the staging buffers
+          // each output in turn through the warp's staging block: this lane's row, 64-byte swizzle (16-byte
+          // chunk j ^ ((row >> 1) & 3)), then read back row-wise and stored coalesced: lane l takes the
+          // 16-byte chunk l & 3 of rows (l >> 2) + 8 i, so that each store writes eight whole 64-byte rows
+          const int k = lane & 3;
+          const bool col_ok = col + 8 * k < args.N;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // this lane's row of each 32x32 block, 64-byte swizzle: 16-byte chunk j ^ ((row >> 1) & 3)
-            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
-            sts128(stg + off, rg[j]);
-            sts128(stg + 2048 + off, rf[j]);
-            sts128(stg + 4096 + off, ry[j]);
-          }
-          __syncwarp();
-          // read the blocks back row-wise and store them coalesced: lane l takes the 16-byte chunk l & 3 of
-          // rows (l >> 2) + 8 i, so that each store writes eight whole 64-byte row segments
-          {
-            const int k = lane & 3;
-            const bool col_ok = col + 8 * k < args.N;
+          for (int o = 0; o < 3; ++o) {
+            __syncwarp();  // every lane has read the block back
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              sts128(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), o == 0 ? rg[j] : (o == 1 ? rf[j] : ry[j]));
+            __syncwarp();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = (lane >> 2) + 8 * i;
               const int row = m0 + q * 32 + r;
-              const uint32_t off = r * 64 + ((k ^ ((r >> 1) & 3)) << 4);
-              const uint4 vg = lds128(stg + off), vf = lds128(stg + 2048 + off), vy = lds128(stg + 4096 + off);
-              if (row < args.M && col_ok) {
-                const size_t o = static_cast<size_t>(row) * args.N + col + 8 * k;
-                stg128(args.out[0] + o, vg);
-                stg128(args.out[1] + o, vf);
-                stg128(args.out[2] + o, vy);
-              }
+              const uint4 v = lds128(stg + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
+              if (row < args.M && col_ok) stg128(args.out[o] + static_cast<size_t>(row) * args.N + col + 8 * k, v);
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&s.tmem_empty[buf]);  // this thread has read its rows of the buffer
+      __syncwarp();
+      if (lane == 0) {  // this warp has read its rows of the buffer: tell the leader's MMA issuer
+        if (leader)
+          mbar_arrive(&s.tmem_empty[buf]);
+        else
+          mbar_arrive_remote(cluster_addr(&s.tmem_empty[buf], 0));
+      }
     }
   }
 
   __syncthreads();
-  if (threadIdx.x == 0 && s.abort_flag) {
-    // drain: copies issued but never consumed must land before the CTA exits
-    for (uint32_t i = s.consumed; i < s.issued; ++i)
-      if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+  cluster_sync();  // both CTAs are done with their roles: no more remote arrivals or commits
+  if (leader && threadIdx.x == 0) {
+    const uint32_t peer_abort = ld_cluster_u32(&s.abort_flag, 1);
+    if (s.abort_flag || peer_abort) {
+      // drain: copies of either CTA that complete on the leader's barriers must land before
+      // either CTA exits
+      const uint32_t peer_issued = ld_cluster_u32(&s.issued, 1);
+      const uint32_t issued = s.issued > peer_issued ? s.issued : peer_issued;
+      for (uint32_t i = s.consumed; i < issued; ++i)
+        if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+    }
   }
+  cluster_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -317,17 +340,30 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   a.out[1] = fc;
   a.out[2] = y;
   a.tiles_n = static_cast<int>((N + BN - 1) / BN);
-  a.tiles = static_cast<int>(((M + BM - 1) / BM) * a.tiles_n);
+  a.tiles = static_cast<int>(((M + 2 * BM - 1) / (2 * BM)) * a.tiles_n);
   a.nkb = static_cast<int>((K + BK - 1) / BK);
   constexpr size_t smem = sizeof(FwdSmem) + 1024;
   static_assert(smem <= 232448, "forward kernel shared memory");
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  int grid = device_sm_count();
-  if (grid > a.tiles) grid = a.tiles;
-  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mx, mwg, mwfc, a);
-  return cudaGetLastError();
+  // one pair per two SMs, looping over the pair tiles
+  int clusters = device_sm_count() / 2;
+  if (clusters > a.tiles) clusters = a.tiles;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_kernel, mx, mwg, mwfc, a);
 }
 
 }  // namespace swg
