@@ -120,7 +120,8 @@ swg_status swg_check(swg_stream_t stream);
  *           unfused swiglu_bwd), SWG_INJECT_FUSED_X (the fused x kernel,
  *           swiglu_bwd_x_fused and the fused swiglu_bwd) or SWG_INJECT_FUSED_W
  *           (the fused w kernel on CTA pairs, swiglu_bwd_w_fused and the fused
- *           swiglu_bwd: both CTAs' producers stop at the entry).
+ *           swiglu_bwd: both CTAs' producers stop at the entry) or SWG_INJECT_FWD
+ *           (the forward on CTA pairs, swiglu_fwd: both producers stop).
  * SWG_INJECT_NONE disarms an armed, unused injection (entry and limit are then
  * ignored); a later call replaces it. Returns SWG_ERR_PARAM_INVALID for another
  * kernel, entry < 0 or a limit below 1024 cycles. For tests only. */
@@ -128,7 +129,8 @@ typedef enum {
   SWG_INJECT_NONE = 0,
   SWG_INJECT_X_GEMM = 1,
   SWG_INJECT_FUSED_X = 2,
-  SWG_INJECT_FUSED_W = 3
+  SWG_INJECT_FUSED_W = 3,
+  SWG_INJECT_FWD = 4
 } swg_inject_kernel;
 swg_status swg_inject_stall(swg_inject_kernel kernel, int64_t entry, int64_t wait_limit_cycles);
 

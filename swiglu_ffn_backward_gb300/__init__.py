@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     swg_check,
     swg_inject_stall,
     SWG_INJECT_FUSED_W,
+    SWG_INJECT_FWD,
     SWG_INJECT_FUSED_X,
     SWG_INJECT_X_GEMM,
     swiglu_bwd,

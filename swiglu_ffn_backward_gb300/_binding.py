@@ -250,6 +250,7 @@ def swiglu_bwd_w_fused(x, dy, g, fc, dw_g=None, dw_fc=None, db_g=None, db_fc=Non
 SWG_INJECT_X_GEMM = 1
 SWG_INJECT_FUSED_X = 2
 SWG_INJECT_FUSED_W = 3
+SWG_INJECT_FWD = 4
 
 
 def swg_inject_stall(kernel: int, entry: int, wait_limit_cycles: int) -> None:

@@ -100,7 +100,8 @@ swg_status swg_inject_stall(swg_inject_kernel kernel, int64_t entry, int64_t wai
     swg::arm_injection(0, -1, 0);
     return SWG_OK;
   }
-  if (kernel != SWG_INJECT_X_GEMM && kernel != SWG_INJECT_FUSED_X && kernel != SWG_INJECT_FUSED_W)
+  if (kernel != SWG_INJECT_X_GEMM && kernel != SWG_INJECT_FUSED_X && kernel != SWG_INJECT_FUSED_W &&
+      kernel != SWG_INJECT_FWD)
     return SWG_ERR_PARAM_INVALID;
   if (entry < 0 || wait_limit_cycles < 1024) return SWG_ERR_PARAM_INVALID;
   swg::arm_injection(static_cast<int>(kernel), entry, static_cast<long long>(wait_limit_cycles));

@@ -70,6 +70,8 @@ struct FwdArgs {
   const uint16_t* bias[2]; // b_g, b_fc [N] or null
   uint16_t* out[3];        // g, fc, y [M, N]
   int tiles, tiles_n, nkb; // pair tiles [256 rows x 128 columns], column tiles, K blocks
+  long long wait_limit;    // cycles before a pipeline wait gives up
+  int64_t stall_at;        // test injection: the producers stop before this ring entry (-1: never)
 };
 
 __device__ __forceinline__ void fwd_timeout(FwdSmem& s, uint32_t* status) {
@@ -135,12 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const CUtensorMap* tw = leader ? &tm_wg : &tm_wfc;  // this CTA's half of the B operand
       uint32_t gj = 0;
-      for (int t = cluster; t < args.tiles && !s.abort_flag; t += nclusters) {
+      bool stopped = false;
+      for (int t = cluster; t < args.tiles && !s.abort_flag && !stopped; t += nclusters) {
         const int n0 = (t % args.tiles_n) * BN;
         const int m0 = (t / args.tiles_n) * (2 * BM) + BM * static_cast<int>(crank);
         for (int kb = 0; kb < args.nkb && !s.abort_flag; ++kb, ++gj) {
+          if (static_cast<int64_t>(gj) == args.stall_at) {
+            stopped = true;
+            break;
+          }
           const int st = gj % STAGES;
-          if (gj >= STAGES && !mbar_wait(&s.empty[st], ((gj / STAGES) - 1) & 1)) {
+          if (gj >= STAGES && !mbar_wait(&s.empty[st], ((gj / STAGES) - 1) & 1, args.wait_limit)) {
             fwd_timeout(s, args.status);
             break;
           }
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t buf = it & 1;
         if (it >= 2) {
           // the epilogue has read this buffer's previous tile out
-          if (!mbar_wait(&s.tmem_empty[buf], ((it >> 1) - 1) & 1)) {
+          if (!mbar_wait(&s.tmem_empty[buf], ((it >> 1) - 1) & 1, args.wait_limit)) {
             fwd_timeout(s, args.status);
             break;
           }
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + buf * 256;  // in each CTA: g at d, fc at d + 128
         for (int kb = 0; kb < args.nkb; ++kb, ++gj) {
           const int st = gj % STAGES;
-          if (!mbar_wait(&s.full[st], (gj / STAGES) & 1)) {
+          if (!mbar_wait(&s.full[st], (gj / STAGES) & 1, args.wait_limit)) {
             fwd_timeout(s, args.status);
             ok = false;
             break;
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ready = false;
       if (!dead && !s.abort_flag) {
-        ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1);
+        ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1, args.wait_limit);
         if (!ready) {
           fwd_timeout(s, args.status);
           dead = true;
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t peer_issued = ld_cluster_u32(&s.issued, 1);
       const uint32_t issued = s.issued > peer_issued ? s.issued : peer_issued;
       for (uint32_t i = s.consumed; i < issued; ++i)
-        if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1)) break;
+        if (!mbar_wait(&s.full[i % STAGES], (i / STAGES) & 1, args.wait_limit)) break;
     }
   }
   cluster_sync();
@@ -339,6 +346,9 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   a.out[0] = g;
   a.out[1] = fc;
   a.out[2] = y;
+  const Injection inj = take_injection(4);
+  a.wait_limit = inj.wait_limit;
+  a.stall_at = inj.stall_at;
   a.tiles_n = static_cast<int>((N + BN - 1) / BN);
   a.tiles = static_cast<int>(((M + 2 * BM - 1) / (2 * BM)) * a.tiles_n);
   a.nkb = static_cast<int>((K + BK - 1) / BK);

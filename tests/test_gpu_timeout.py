@@ -26,11 +26,13 @@ LIMIT = 1 << 20  # cycles, about half a millisecond
 def test_injection_arguments_are_checked():
     from swiglu_ffn_backward_gb300 import _binding as b
     assert b.lib.swg_inject_stall(7, 1, LIMIT) == b.SWG_ERR_PARAM_INVALID
+    assert b.lib.swg_inject_stall(5, 1, LIMIT) == b.SWG_ERR_PARAM_INVALID
     assert b.lib.swg_inject_stall(b.SWG_INJECT_X_GEMM, -1, LIMIT) == b.SWG_ERR_PARAM_INVALID
     assert b.lib.swg_inject_stall(b.SWG_INJECT_X_GEMM, 1, 100) == b.SWG_ERR_PARAM_INVALID
     # arming and disarming touches host state only
     assert b.lib.swg_inject_stall(b.SWG_INJECT_FUSED_X, 3, LIMIT) == b.SWG_OK
     assert b.lib.swg_inject_stall(b.SWG_INJECT_FUSED_W, 0, LIMIT) == b.SWG_OK
+    assert b.lib.swg_inject_stall(b.SWG_INJECT_FWD, 2, LIMIT) == b.SWG_OK
     assert b.lib.swg_inject_stall(0, 0, 0) == b.SWG_OK
 
 
@@ -98,4 +100,27 @@ def test_fused_w_wait_runs_out(entry):
     h = {k: to_f64(v) for k, v in inp.items()}
     rdwg, rdwfc = oracle.swiglu_bwd_w(h["x"], to_f64(out["dg"]), to_f64(out["dfc"]))
     assert_all([compare("dw_g", out["dw_g"], rdwg), compare("dw_fc", out["dw_fc"], rdwfc)])
+    torch.cuda.synchronize()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("entry", [0, 1, 7])
+def test_forward_wait_runs_out(entry):
+    """The forward runs on CTA pairs (M=1024 K=512 N=256: eight pair tiles, one per pair, eight
+    K blocks each, six stage slots). Both CTAs' producers stop before the entry; the leader's MMA
+    wait runs out, then both CTAs' epilogue waits; both CTAs meet at the final cluster barriers. A
+    normal call afterwards matches the oracle."""
+    from synth import swiglu_fwd_biases
+    swg = _swg()
+    shape = SwigluShape("fwd_stall_M1024", 1024, 512, 256, 21, "tail")
+    inp = swiglu_inputs(shape, device="cuda")
+    b_g, b_fc = swiglu_fwd_biases(shape, device="cuda")
+    swg.swg_inject_stall(swg.SWG_INJECT_FWD, entry, LIMIT)
+    swg.swiglu_fwd(inp["x"], inp["w_g"], inp["w_fc"], b_g, b_fc)
+    _expect_timeout(swg)
+    out = swg.swiglu_fwd(inp["x"], inp["w_g"], inp["w_fc"], b_g, b_fc)
+    swg.swg_check()
+    g, fc, y = oracle.swiglu_fwd(to_f64(inp["x"]), to_f64(inp["w_g"]), to_f64(inp["w_fc"]), to_f64(b_g),
+                                 to_f64(b_fc))
+    assert_all([compare("g", out["g"], g), compare("fc", out["fc"], fc), compare("y", out["y"], y)])
     torch.cuda.synchronize()
