@@ -269,15 +269,19 @@ def test_w_stage_many_tiles_per_cta():
 
 
 @pytest.mark.gpu
-def test_fused_chain_side_split_matches_stage_calls():
+@pytest.mark.parametrize("N", [1024, 1000])
+def test_fused_chain_side_split_matches_stage_calls(N):
     """At M = 100000, K = 512, N = 1024 the fused whole-backward call runs the x stage's last tiles
-    beside the w stage (the w stage leaves SMs free and the x stage needs six waves): every output
-    must equal the two stage calls' bit for bit. The outputs start filled with a value no result
-    takes, so a tile the split left out would show."""
+    beside the w stage (the w stage leaves SMs free and the x stage needs six waves), and the w
+    stage's reduction on the side stream beside the x stage's wave: every output must equal the two
+    stage calls' bit for bit. N = 1000 leaves a ragged last column band. The outputs start filled
+    with a value no result takes, so a tile the split left out would show."""
     swg = _swg()
-    shape = SwigluShape("split_M100000", 100000, 512, 1024, 11, "pages")
+    shape = SwigluShape(f"split_M100000_N{N}", 100000, 512, N, 11, "pages")
     inp = swiglu_inputs(shape, device="cuda")
     M, K, N = shape.M, shape.K, shape.N
+    # FW, its reduction, and the x stage in two launches: the side stream is in use
+    assert swg.swiglu_bwd_kernel_count(M, K, N, swg.SWG_FUSED) == 4
     bf = dict(dtype=torch.bfloat16, device="cuda")
     dx = torch.empty((M, K), **bf)
     swg.swiglu_bwd_x_fused(inp["dy"], inp["g"], inp["fc"], inp["w_g"], inp["w_fc"], dx)
