@@ -22,11 +22,10 @@
 //   warps 2-9       epilogue (both CTAs, each on its own 128 rows; two warps
 //                   per TMEM lane quarter, each on half of the tile's columns):
 //                   drain the finished buffer while the tensor cores fill the
-//                   other one: bias (the tile's columns staged once per tile in
-//                   shared memory), SiLU, and g, fc, y in turn through the
-//                   warp's 64-byte-swizzled 32x32 staging block, read back
-//                   row-wise and stored with coalesced 16-byte global stores
-//                   (rows beyond M and columns beyond N are not written)
+//                   other one: bias (read through L1, the same address in every
+//                   lane), SiLU, and g, fc, y in turn through the warp's two
+//                   64-byte-swizzled 32x32 staging blocks, each written out by
+//                   a TMA store (rows beyond M and columns beyond N clipped)
 // The pair loops over output tiles [256 rows x 128 columns]; with K = 512 a
 // tile holds only eight K blocks, so the double-buffered accumulator is what
 // keeps the tensor cores busy across tile boundaries.
@@ -53,8 +52,7 @@ constexpr uint32_t kTmemCols = 512;    // two buffers of [g | fc] in each CTA
 struct __align__(1024) FwdSmem {
   uint8_t a[STAGES][A_BYTES];
   uint8_t b[STAGES][B_BYTES];
-  uint8_t stage[kEpiWarps][2048];     // per epilogue warp: one [32 rows x 32 columns] block (g, fc, y in turn)
-  uint4 bias[kEpiWarps][2][16];       // per epilogue warp: the tile's b_g, b_fc columns (8 per uint4)
+  uint8_t stage[kEpiWarps][2][2048];  // per epilogue warp: two [32 rows x 32 columns] blocks for TMA stores
   uint64_t full[STAGES];     // leader: both CTAs' copies of the stage have landed
   uint64_t empty[STAGES];    // the pair MMAs reading the stage are done (committed to both CTAs)
   uint64_t tmem_full[2];     // the tile's MMAs into this buffer are done (committed to both CTAs)
@@ -68,7 +66,6 @@ struct FwdArgs {
   int M, K, N;
   uint32_t* status;
   const uint16_t* bias[2]; // b_g, b_fc [N] or null
-  uint16_t* out[3];        // g, fc, y [M, N]
   int tiles, tiles_n, nkb; // pair tiles [256 rows x 128 columns], column tiles, K blocks
   long long wait_limit;    // cycles before a pipeline wait gives up
   int64_t stall_at;        // test injection: the producers stop before this ring entry (-1: never)
@@ -96,7 +93,9 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
-               const __grid_constant__ CUtensorMap tm_wfc, const FwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_wfc, const __grid_constant__ CUtensorMap tm_g,
+               const __grid_constant__ CUtensorMap tm_fc, const __grid_constant__ CUtensorMap tm_y,
+               const FwdArgs args) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& s = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -212,22 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     bool dead = false;
-    uint32_t it = 0;
+    uint32_t it = 0, nb = 0;  // tiles, staged blocks
     for (int t = cluster; t < args.tiles; t += nclusters, ++it) {
       const uint32_t buf = it & 1;
       const int n0 = (t % args.tiles_n) * BN;
       const int m0 = (t / args.tiles_n) * (2 * BM) + BM * static_cast<int>(crank);
-      {
-        // the tile's biases: lane l < 16 loads b_g columns n0 + 8l .. n0 + 8l + 7, lane 16 + l the same of b_fc
-        // (zeros beyond N, where the store clips); read back below as warp-wide broadcasts
-        const int which = lane >> 4, cb = n0 + 8 * (lane & 15);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        const uint16_t* bp = which ? args.bias[1] : args.bias[0];
-        if (cb < args.N && bp != nullptr) v = __ldg(reinterpret_cast<const uint4*>(bp + cb));
-        __syncwarp();  // every lane has read the previous tile's biases
-        s.bias[warp - 2][which][lane & 15] = v;
-        __syncwarp();
-      }
       bool ready = false;
       if (!dead && !s.abort_flag) {
         ready = mbar_wait(&s.tmem_full[buf], (it >> 1) & 1, args.wait_limit);
@@ -251,7 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 rg[4], rf[4], ry[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint4 bgv = s.bias[warp - 2][0][c * 4 + j], bfv = s.bias[warp - 2][1][c * 4 + j];
+            // the biases of these 8 columns, the same address in every lane (zeros beyond N, where the
+            // store clips)
+            const int cb = col + 8 * j;
+            uint4 bgv = make_uint4(0u, 0u, 0u, 0u), bfv = bgv;
+            if (cb < args.N) {
+              if (args.bias[0] != nullptr) bgv = __ldg(reinterpret_cast<const uint4*>(args.bias[0] + cb));
+              if (args.bias[1] != nullptr) bfv = __ldg(reinterpret_cast<const uint4*>(args.bias[1] + cb));
+            }
             const uint32_t bgw[4] = {bgv.x, bgv.y, bgv.z, bgv.w};
             const uint32_t bfw[4] = {bfv.x, bfv.y, bfv.z, bfv.w};
             uint32_t og[4], of[4], oy[4];
@@ -272,24 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             rf[j] = make_uint4(of[0], of[1], of[2], of[3]);
             ry[j] = make_uint4(oy[0], oy[1], oy[2], oy[3]);
           }
-          // each output in turn through the warp's staging block: this lane's row, 64-byte swizzle (16-byte
-          // chunk j ^ ((row >> 1) & 3)), then read back row-wise and stored coalesced: lane l takes the
-          // 16-byte chunk l & 3 of rows (l >> 2) + 8 i, so that each store writes eight whole 64-byte rows
-          const int k = lane & 3;
-          const bool col_ok = col + 8 * k < args.N;
+          // each output in turn through the warp's two staging blocks (this lane's row, 64-byte swizzle:
+          // 16-byte chunk j ^ ((row >> 1) & 3)), written out by a TMA store that clips rows beyond M and
+          // columns beyond N
 #pragma unroll
-          for (int o = 0; o < 3; ++o) {
-            __syncwarp();  // every lane has read the block back
+          for (int o = 0; o < 3; ++o, ++nb) {
+            uint8_t* blk = s.stage[warp - 2][nb & 1];
+            if (nb >= 2) {
+              if (lane == 0) bulk_wait_read<1>();  // the store that used this block has read it
+              __syncwarp();
+            }
+            const uint32_t sb = smem_u32(blk) + lane * 64;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              sts128(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), o == 0 ? rg[j] : (o == 1 ? rf[j] : ry[j]));
+              sts128(sb + ((j ^ ((lane >> 1) & 3)) << 4), o == 0 ? rg[j] : (o == 1 ? rf[j] : ry[j]));
+            fence_proxy_async_smem();
             __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = (lane >> 2) + 8 * i;
-              const int row = m0 + q * 32 + r;
-              const uint4 v = lds128(stg + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
-              if (row < args.M && col_ok) stg128(args.out[o] + static_cast<size_t>(row) * args.N + col + 8 * k, v);
+            if (lane == 0) {
+              if (m0 + q * 32 < args.M) tma_store_2d(o == 0 ? &tm_g : (o == 1 ? &tm_fc : &tm_y), blk, col, m0 + q * 32);
+              bulk_commit();
             }
           }
         }
@@ -303,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_remote(cluster_addr(&s.tmem_empty[buf], 0));
       }
     }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
   }
 
   __syncthreads();
@@ -331,10 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16_t* w_fc, const uint16_t* b_g,
                             const uint16_t* b_fc, uint16_t* g, uint16_t* fc, uint16_t* y, int64_t M, int64_t K,
                             int64_t N, cudaStream_t stream) {
-  CUtensorMap mx, mwg, mwfc;
+  CUtensorMap mx, mwg, mwfc, mg, mfc, my;
   const uint64_t rs = static_cast<uint64_t>(N) * 2;
   if (!encode_tmap_2d_bf16(&mx, x, K, M, static_cast<uint64_t>(K) * 2, BK, BM) ||
-      !encode_tmap_2d_bf16(&mwg, w_g, N, K, rs, 64, BK) || !encode_tmap_2d_bf16(&mwfc, w_fc, N, K, rs, 64, BK))
+      !encode_tmap_2d_bf16(&mwg, w_g, N, K, rs, 64, BK) || !encode_tmap_2d_bf16(&mwfc, w_fc, N, K, rs, 64, BK) ||
+      !encode_tmap_2d_bf16(&mg, g, N, M, rs, 32, 32, 64) || !encode_tmap_2d_bf16(&mfc, fc, N, M, rs, 32, 32, 64) ||
+      !encode_tmap_2d_bf16(&my, y, N, M, rs, 32, 32, 64))
     return cudaErrorInvalidValue;
   FwdArgs a{};
   a.M = static_cast<int>(M);
@@ -343,9 +342,6 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   a.status = status_word_ptr();
   a.bias[0] = b_g;
   a.bias[1] = b_fc;
-  a.out[0] = g;
-  a.out[1] = fc;
-  a.out[2] = y;
   const Injection inj = take_injection(4);
   a.wait_limit = inj.wait_limit;
   a.stall_at = inj.stall_at;
@@ -373,7 +369,7 @@ cudaError_t launch_fwd_gemm(const uint16_t* x, const uint16_t* w_g, const uint16
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_kernel, mx, mwg, mwfc, a);
+  return cudaLaunchKernelEx(&cfg, fwd_kernel, mx, mwg, mwfc, mg, mfc, my, a);
 }
 
 }  // namespace swg
